@@ -1,0 +1,175 @@
+"""CPU oracle for y = x . dequant(W)^T with an NVFP4 weight (binary64).
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  It shares no code
+with the CUDA path (``nvfp4_skinny_gb300``) and neither imports the other.
+
+The arithmetic lives in ``nvfp4_oracle.c`` (plain C, binary64, ascending-k
+sums, formats decoded from their bit fields).  This module only marshals
+numpy arrays into it.
+
+Sources: "10 Kernels" section 10.2 (E2M1 weight, E4M3 group scale per 16
+along K, 16-bit activations); "Module ops", Functions dequant_nvfp4_to_bf16,
+nvfp4_mmq_repack (E2M1 [n, k/2] with the low nibble = even k, E4M3
+[n, k/16]), w4a16_gemm (FP32 per-tensor scale, BF16 A [M, K]) and
+w4a16_tc_rows (output [m, n] = input [m, :] . W[n, :]^T).
+
+Tolerance: |y - y_ref| <= 4e-3 * sum_k |w_k x_k| + one bfloat16 ulp of
+|y_ref| per element (the stated acceptance bound for the GPU path).
+"""
+import ctypes
+import numpy as np
+
+from . import build as _build
+
+class Oracle:
+    """Marshalling wrapper around one build of the oracle library."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        d, i64, p = ctypes.c_double, ctypes.c_int64, ctypes.c_void_p
+        lib.nvfp4_oracle_e2m1.restype = d
+        lib.nvfp4_oracle_e2m1.argtypes = [ctypes.c_uint]
+        lib.nvfp4_oracle_e4m3.restype = d
+        lib.nvfp4_oracle_e4m3.argtypes = [ctypes.c_uint]
+        lib.nvfp4_oracle_bf16.restype = d
+        lib.nvfp4_oracle_bf16.argtypes = [ctypes.c_uint]
+        lib.nvfp4_oracle_weight.restype = d
+        lib.nvfp4_oracle_weight.argtypes = [p, p, ctypes.c_float, i64, i64, i64]
+        lib.nvfp4_oracle_linear.restype = None
+        lib.nvfp4_oracle_linear.argtypes = [i64, i64, i64, p, p, p, ctypes.c_float, p, p, ctypes.c_int]
+        lib.nvfp4_oracle_linear_at.restype = None
+        lib.nvfp4_oracle_linear_at.argtypes = [i64, i64, p, p, p, p, p, ctypes.c_float, p, p, ctypes.c_int]
+        lib.nvfp4_oracle_bf16_ulp.restype = d
+        lib.nvfp4_oracle_bf16_ulp.argtypes = [d]
+        lib.nvfp4_oracle_max_threads.restype = ctypes.c_int
+        lib.nvfp4_oracle_max_threads.argtypes = []
+        self.lib = lib
+        self.path = path
+
+    def e2m1(self, code: int) -> float:
+        """E2M1 value of a 4-bit code (OCP MX FP4)."""
+        return self.lib.nvfp4_oracle_e2m1(int(code))
+
+    def e4m3(self, byte: int) -> float:
+        """E4M3 value of one byte (OCP FP8 E4M3FN; 0x7F/0xFF are NaN)."""
+        return self.lib.nvfp4_oracle_e4m3(int(byte))
+
+    def bf16(self, bits: int) -> float:
+        """Value of a bfloat16 bit pattern."""
+        return self.lib.nvfp4_oracle_bf16(int(bits))
+
+    def weight(self, codes, scales, gs: float, K: int, n: int, k: int) -> float:
+        """Dequantised W[n, k] = E2M1(code) * E4M3(scale[n, k // 16]) * gs."""
+        codes, scales = _u8(codes), _u8(scales)
+        return self.lib.nvfp4_oracle_weight(_ptr(codes), _ptr(scales), float(np.float32(gs)), int(K), int(n), int(k))
+
+    def linear(self, x_bits, codes, scales, gs: float, threads: int = 0):
+        """Full product.  x_bits: uint16 [M, K] (bfloat16 bits); codes: uint8 [N, K/2];
+        scales: uint8 [N, K/16]; gs: float32 per-tensor scale.
+
+        Returns (y_ref, absdot), both float64 [M, N]."""
+        x_bits, codes, scales = _u16(x_bits), _u8(codes), _u8(scales)
+        M, K = x_bits.shape
+        N = codes.shape[0]
+        assert codes.shape == (N, K // 2) and scales.shape == (N, K // 16) and K % 16 == 0
+        y = np.empty((M, N), np.float64)
+        a = np.empty((M, N), np.float64)
+        self.lib.nvfp4_oracle_linear(M, N, K, _ptr(x_bits), _ptr(codes), _ptr(scales), float(np.float32(gs)),
+                                     _ptr(y), _ptr(a), int(threads))
+        return y, a
+
+    def linear_at(self, x_bits, codes, scales, gs: float, ms, ns, threads: int = 0):
+        """Sampled outputs (ms[i], ns[i]); returns (y_ref, absdot), float64 [count]."""
+        x_bits, codes, scales = _u16(x_bits), _u8(codes), _u8(scales)
+        M, K = x_bits.shape
+        N = codes.shape[0]
+        assert codes.shape == (N, K // 2) and scales.shape == (N, K // 16) and K % 16 == 0
+        ms = np.ascontiguousarray(ms, dtype=np.int64)
+        ns = np.ascontiguousarray(ns, dtype=np.int64)
+        assert ms.shape == ns.shape and ms.ndim == 1
+        assert (ms >= 0).all() and (ms < M).all() and (ns >= 0).all() and (ns < N).all()
+        y = np.empty(ms.shape, np.float64)
+        a = np.empty(ms.shape, np.float64)
+        self.lib.nvfp4_oracle_linear_at(K, ms.size, _ptr(ms), _ptr(ns), _ptr(x_bits), _ptr(codes), _ptr(scales),
+                                        float(np.float32(gs)), _ptr(y), _ptr(a), int(threads))
+        return y, a
+
+    def bf16_ulp(self, a) -> np.ndarray:
+        """One bfloat16 ulp at magnitude |a| (elementwise)."""
+        f = np.vectorize(self.lib.nvfp4_oracle_bf16_ulp, otypes=[np.float64])
+        return f(np.asarray(a, np.float64))
+
+    def tolerance(self, y_ref, absdot) -> np.ndarray:
+        """Per-element acceptance bound 4e-3 * sum|w x| + ulp_bf16(|y_ref|)."""
+        return 4e-3 * np.asarray(absdot, np.float64) + self.bf16_ulp(y_ref)
+
+    def max_threads(self) -> int:
+        """Threads the oracle's OpenMP runtime uses by default."""
+        return int(self.lib.nvfp4_oracle_max_threads())
+
+
+def _u8(a):
+    a = np.ascontiguousarray(a)
+    assert a.dtype == np.uint8
+    return a
+
+
+def _u16(a):
+    a = np.ascontiguousarray(a)
+    assert a.dtype == np.uint16, "x must be given as bfloat16 bit patterns (uint16)"
+    return a
+
+
+def _ptr(a):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+_default = None
+
+
+def default() -> Oracle:
+    """The oracle built from oracle/nvfp4_oracle.c (built on first use)."""
+    global _default
+    if _default is None:
+        _default = Oracle(_build.build())
+    return _default
+
+
+def e2m1(code):
+    return default().e2m1(code)
+
+
+def e4m3(byte):
+    return default().e4m3(byte)
+
+
+def bf16(bits):
+    return default().bf16(bits)
+
+
+def weight(codes, scales, gs, K, n, k):
+    return default().weight(codes, scales, gs, K, n, k)
+
+
+def linear(x_bits, codes, scales, gs, threads: int = 0):
+    return default().linear(x_bits, codes, scales, gs, threads)
+
+
+def linear_at(x_bits, codes, scales, gs, ms, ns, threads: int = 0):
+    return default().linear_at(x_bits, codes, scales, gs, ms, ns, threads)
+
+
+def bf16_ulp(a):
+    return default().bf16_ulp(a)
+
+
+def tolerance(y_ref, absdot):
+    return default().tolerance(y_ref, absdot)
+
+
+def max_threads():
+    return default().max_threads()
+
+
+__all__ = ["Oracle", "default", "e2m1", "e4m3", "bf16", "weight", "linear", "linear_at", "bf16_ulp", "tolerance", "max_threads"]
