@@ -1,0 +1,139 @@
+/*
+ * nvfp4_skinny.h -- C ABI of the GB300 (sm_103a) NVFP4 weight-only skinny projection.
+ *
+ * Operation
+ *   y[m, n] = sum_k x[m, k] * W[n, k],      0 <= m < M <= 32,  0 <= n < N,  0 <= k < K
+ *   W[n, k] = E2M1(code[n, k]) * E4M3(block_scale[n, k / 16]) * w_global_scale
+ *
+ *   Sources (web pages, section / entry):
+ *   - "10 Kernels" 10.2 "NVFP4 matrix products": 4-bit E2M1 weights with an
+ *     E4M3 group scale multiplied onto them, 16-bit activations, 1 to 32 rows
+ *     served by one skinny kernel;
+ *   - "10 Kernels" 10.1 "Row invariance": row r of an M-row product has the
+ *     same bits as the same row computed alone; the reduction order is fixed
+ *     by the weight shape (N, K), never by the row count; no atomics decide
+ *     the order of a sum; split-K partials are added in a fixed order;
+ *   - "Module ops" (rustdoc API index), Functions: w4a16_tc_rows (output
+ *     [m, n] = input [m, :] . W[n, :]^T for the row-major NVFP4 weight [n, k]),
+ *     w4a16_tc_rows_shape_ok (shape contract checked without a GPU; refuse
+ *     instead of producing stale output), w4a16_gemm (FP32 per-tensor scale),
+ *     nvfp4_mmq_repack (E2M1 [n, k/2], low nibble = even k; E4M3 [n, k/16]),
+ *     dequant_nvfp4_to_bf16 (the three factors of W).
+ *
+ * Data layout (all row-major, contiguous, no pitch):
+ *   x               bfloat16 [M, K]           device memory
+ *   w_codes         uint8    [N, K/2]         device; byte j of row n holds k = 2j
+ *                                              in bits 0..3 and k = 2j+1 in bits 4..7
+ *   w_block_scales  uint8    [N, K/16]        device; E4M3 (OCP E4M3FN) bytes,
+ *                                              finite and >= 0 (UE4M3 in use)
+ *   w_global_scale  float                      by value
+ *   y               bfloat16 [M, N] (NVFP4_OUT_BF16) or float [M, N] (NVFP4_OUT_F32), device
+ *
+ * Ownership and concurrency
+ *   The caller owns x, the weight buffers and y.  A plan owns host state and
+ *   one device workspace (converted activations, split-K partials, counters,
+ *   an error word), allocated by nvfp4_plan_create* on the device that is
+ *   current then; all later calls on the plan must run on that device.
+ *   nvfp4_skinny_linear never allocates, never synchronizes and only
+ *   enqueues kernels on `stream`, so it can be captured in a CUDA graph.
+ *   Calls that share a plan must not run concurrently (the workspace is
+ *   reused); calls on one stream are ordered and safe.
+ *
+ * Errors
+ *   Argument errors are detected on the host before anything is enqueued;
+ *   the call then returns a status and launches nothing.  A launch failure
+ *   returns NVFP4_ERR_CUDA.  Every wait inside the kernels is bounded: if one
+ *   runs out, the kernel records NVFP4_ERR_TIMEOUT in the plan's error word,
+ *   skips the remaining work and exits; nvfp4_plan_check reports it.
+ *
+ * Numerics
+ *   Activations are converted once per call to fp16 after multiplying each
+ *   row by a power of two chosen from that row's largest magnitude (exact for
+ *   every element within 2^-32 of the row maximum); weights are decoded to
+ *   fp16 (E2M1 x E4M3 is exact in fp16); products accumulate in fp32 on the
+ *   tensor cores; the power of two and w_global_scale are applied to the fp32
+ *   sum, which is then rounded to nearest-even bfloat16 (or returned as fp32).
+ */
+#ifndef NVFP4_SKINNY_H
+#define NVFP4_SKINNY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct nvfp4_plan* nvfp4_plan_t; /* opaque, host-owned */
+
+typedef enum {
+  NVFP4_OK = 0,
+  NVFP4_ERR_ARG = 1,     /* null plan / pointer, or out-of-range enum */
+  NVFP4_ERR_SHAPE = 2,   /* N < 1, K < 256, K not a multiple of 256, or too large */
+  NVFP4_ERR_ALIGN = 3,   /* x, y, w_codes or w_block_scales not 16-byte aligned */
+  NVFP4_ERR_M_RANGE = 4, /* M outside 1..32 */
+  NVFP4_ERR_CUDA = 5,    /* a CUDA runtime call failed (launch, allocation, query) */
+  NVFP4_ERR_NOMEM = 6,   /* host or device allocation failed */
+  NVFP4_ERR_TIMEOUT = 7  /* a bounded in-kernel wait ran out (reported by nvfp4_plan_check) */
+} nvfp4_status;
+
+typedef enum { NVFP4_OUT_BF16 = 0, NVFP4_OUT_F32 = 1 } nvfp4_out_dtype;
+
+/* Largest M a call accepts. */
+#define NVFP4_MAX_M 32
+
+/* Human-readable name of a status (static string, never NULL). */
+const char* nvfp4_status_string(nvfp4_status status);
+
+/* Version of this ABI (incremented on incompatible change). */
+int nvfp4_abi_version(void);
+
+/* Create a plan for an [N, K] weight with bfloat16 output.  The launch
+ * configuration (rows per block, k-step, split of K across blocks, grid) is a
+ * function of (N, K) and the device's SM count only, never of M.
+ * On success *out_plan receives the plan; on failure it is set to NULL. */
+nvfp4_status nvfp4_plan_create(int64_t N, int64_t K, nvfp4_plan_t* out_plan);
+
+/* Same, choosing the output element type (NVFP4_OUT_F32 for fp32 logits). */
+nvfp4_status nvfp4_plan_create_ex(int64_t N, int64_t K, nvfp4_out_dtype out_dtype, nvfp4_plan_t* out_plan);
+
+/* Free a plan and its workspace (NULL is ignored).  Synchronizes the device
+ * the plan was created on before freeing device memory. */
+void nvfp4_plan_destroy(nvfp4_plan_t plan);
+
+/* Enqueue y = x . dequant(W)^T on `stream` (a cudaStream_t; NULL = legacy
+ * default stream).  M is the number of activation rows (1..32).  See the
+ * header comment for layouts, ownership, errors and numerics. */
+nvfp4_status nvfp4_skinny_linear(nvfp4_plan_t plan, const void* x, int M, const uint8_t* w_codes,
+                                 const uint8_t* w_block_scales, float w_global_scale, void* y, void* stream);
+
+/* Synchronize `stream`, then read and clear the plan's device error word.
+ * Returns NVFP4_OK, NVFP4_ERR_TIMEOUT, or NVFP4_ERR_CUDA if the stream
+ * reported an error. */
+nvfp4_status nvfp4_plan_check(nvfp4_plan_t plan, void* stream);
+
+/* Description of a plan's launch configuration (for tests and benchmarks). */
+typedef struct {
+  int64_t N, K;
+  int32_t out_dtype;
+  int32_t rows_per_block;   /* weight rows per unit of work */
+  int32_t k_step;           /* k per unit of work */
+  int32_t stages;           /* shared-memory pipeline depth */
+  int32_t threads;          /* threads per block of the main kernel */
+  int32_t grid;             /* blocks of the main kernel (<= SM count) */
+  int32_t sm_count;
+  int32_t device;
+  int64_t row_blocks;       /* ceil(N / rows_per_block) */
+  int64_t k_steps;          /* K / k_step */
+  int64_t units;            /* row_blocks * k_steps, split evenly over the grid */
+  int64_t workspace_bytes;
+  int64_t smem_bytes;       /* dynamic shared memory of the main kernel */
+} nvfp4_plan_info;
+
+nvfp4_status nvfp4_plan_get_info(nvfp4_plan_t plan, nvfp4_plan_info* info);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_SKINNY_H */

@@ -1,0 +1,241 @@
+"""Thin ctypes binding over the C ABI in include/nvfp4_skinny.h and include/nvfp4_pack.h.
+
+Argument marshalling only: every step of the projection runs in the CUDA library
+(nvfp4_skinny_gb300/_build/libnvfp4skinny.so).  If that library is missing the
+functions raise; there is no fallback path.  Torch tensors are accepted for
+device buffers (their data pointers are passed through); streams default to
+torch's current CUDA stream.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+NVFP4_OK = 0
+NVFP4_ERR_ARG = 1
+NVFP4_ERR_SHAPE = 2
+NVFP4_ERR_ALIGN = 3
+NVFP4_ERR_M_RANGE = 4
+NVFP4_ERR_CUDA = 5
+NVFP4_ERR_NOMEM = 6
+NVFP4_ERR_TIMEOUT = 7
+NVFP4_OUT_BF16 = 0
+NVFP4_OUT_F32 = 1
+NVFP4_MAX_M = 32
+
+NVFP4_PACK_OK = 0
+NVFP4_PACK_ERR_ARG = -1
+NVFP4_PACK_ERR_VALUE = -2
+
+# every symbol the headers declare, per library
+CUDA_SYMBOLS = ("nvfp4_status_string", "nvfp4_abi_version", "nvfp4_plan_create", "nvfp4_plan_create_ex",
+                "nvfp4_plan_destroy", "nvfp4_skinny_linear", "nvfp4_plan_check", "nvfp4_plan_get_info")
+PACK_SYMBOLS = ("nvfp4_pack_codes", "nvfp4_unpack_codes", "nvfp4_e4m3_encode")
+
+
+class Nvfp4Error(RuntimeError):
+    """A non-OK status from the C ABI."""
+
+    def __init__(self, status, where=""):
+        self.status = int(status)
+        super().__init__("%s: %s" % (where, _status_string(self.status)) if where else _status_string(self.status))
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("N", ctypes.c_int64), ("K", ctypes.c_int64), ("out_dtype", ctypes.c_int32),
+                ("rows_per_block", ctypes.c_int32), ("k_step", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("threads", ctypes.c_int32), ("grid", ctypes.c_int32), ("sm_count", ctypes.c_int32),
+                ("device", ctypes.c_int32), ("row_blocks", ctypes.c_int64), ("k_steps", ctypes.c_int64),
+                ("units", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64), ("smem_bytes", ctypes.c_int64)]
+
+
+_cuda = None
+_pack = None
+
+
+def _lib_path(path):
+    if not os.path.exists(path):
+        raise ImportError("%s is not built: run nvfp4_skinny_gb300.build.build() (or __graft_entry__.build())"
+                          % path)
+    return path
+
+
+def cuda_lib():
+    """The CUDA library, loaded once.  Raises ImportError if it has not been built."""
+    global _cuda
+    if _cuda is None:
+        lib = ctypes.CDLL(_lib_path(_build.CUDA_LIB))
+        p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        lib.nvfp4_status_string.restype = ctypes.c_char_p
+        lib.nvfp4_status_string.argtypes = [i32]
+        lib.nvfp4_abi_version.restype = i32
+        lib.nvfp4_abi_version.argtypes = []
+        lib.nvfp4_plan_create.restype = i32
+        lib.nvfp4_plan_create.argtypes = [i64, i64, ctypes.POINTER(p)]
+        lib.nvfp4_plan_create_ex.restype = i32
+        lib.nvfp4_plan_create_ex.argtypes = [i64, i64, i32, ctypes.POINTER(p)]
+        lib.nvfp4_plan_destroy.restype = None
+        lib.nvfp4_plan_destroy.argtypes = [p]
+        lib.nvfp4_skinny_linear.restype = i32
+        lib.nvfp4_skinny_linear.argtypes = [p, p, i32, p, p, ctypes.c_float, p, p]
+        lib.nvfp4_plan_check.restype = i32
+        lib.nvfp4_plan_check.argtypes = [p, p]
+        lib.nvfp4_plan_get_info.restype = i32
+        lib.nvfp4_plan_get_info.argtypes = [p, ctypes.POINTER(PlanInfo)]
+        _cuda = lib
+    return _cuda
+
+
+def pack_lib():
+    """The host packer library, loaded once.  Raises ImportError if it has not been built."""
+    global _pack
+    if _pack is None:
+        lib = ctypes.CDLL(_lib_path(_build.PACK_LIB))
+        p, i64 = ctypes.c_void_p, ctypes.c_int64
+        lib.nvfp4_pack_codes.restype = ctypes.c_int
+        lib.nvfp4_pack_codes.argtypes = [p, i64, i64, p]
+        lib.nvfp4_unpack_codes.restype = ctypes.c_int
+        lib.nvfp4_unpack_codes.argtypes = [p, i64, i64, p]
+        lib.nvfp4_e4m3_encode.restype = ctypes.c_int
+        lib.nvfp4_e4m3_encode.argtypes = [p, i64, p, ctypes.POINTER(i64)]
+        _pack = lib
+    return _pack
+
+
+def _status_string(status):
+    try:
+        return cuda_lib().nvfp4_status_string(int(status)).decode()
+    except ImportError:
+        return "status %d" % int(status)
+
+
+def _ptr(t):
+    """Device (or host) address of a torch tensor, a numpy array or an int; None -> NULL."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if hasattr(t, "data_ptr"):
+        return t.data_ptr()
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data
+    raise TypeError("cannot take the address of %r" % type(t))
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status, where):
+    if status != NVFP4_OK:
+        raise Nvfp4Error(status, where)
+
+
+class Plan:
+    """Owns an nvfp4_plan_t; destroyed with the object (or by destroy())."""
+
+    def __init__(self, handle, N, K, out_dtype):
+        self.handle = handle
+        self.N, self.K, self.out_dtype = int(N), int(K), int(out_dtype)
+
+    def destroy(self):
+        if self.handle is not None:
+            cuda_lib().nvfp4_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+    @property
+    def as_parameter(self):
+        if self.handle is None:
+            raise ValueError("plan was destroyed")
+        return self.handle
+
+
+def nvfp4_status_string(status):
+    return _status_string(status)
+
+
+def nvfp4_abi_version():
+    return int(cuda_lib().nvfp4_abi_version())
+
+
+def nvfp4_plan_create(N, K):
+    """Plan for an [N, K] NVFP4 weight, bfloat16 output."""
+    return nvfp4_plan_create_ex(N, K, NVFP4_OUT_BF16)
+
+
+def nvfp4_plan_create_ex(N, K, out_dtype=NVFP4_OUT_BF16):
+    h = ctypes.c_void_p()
+    _check(cuda_lib().nvfp4_plan_create_ex(int(N), int(K), int(out_dtype), ctypes.byref(h)), "nvfp4_plan_create_ex")
+    return Plan(h.value, N, K, out_dtype)
+
+
+def nvfp4_plan_destroy(plan):
+    plan.destroy()
+
+
+def nvfp4_skinny_linear(plan, x, M, w_codes, w_block_scales, w_global_scale, y, stream=None, check=True):
+    """Enqueue y = x . dequant(W)^T.  Returns the status (raises on error when check=True)."""
+    st = cuda_lib().nvfp4_skinny_linear(plan.as_parameter if isinstance(plan, Plan) else plan, _ptr(x), int(M),
+                                        _ptr(w_codes), _ptr(w_block_scales), float(w_global_scale), _ptr(y),
+                                        _stream(stream))
+    if check:
+        _check(st, "nvfp4_skinny_linear")
+    return st
+
+
+def nvfp4_plan_check(plan, stream=None):
+    """Synchronise the stream and return the plan's device error status (and clear it)."""
+    return int(cuda_lib().nvfp4_plan_check(plan.as_parameter, _stream(stream)))
+
+
+def nvfp4_plan_get_info(plan):
+    info = PlanInfo()
+    _check(cuda_lib().nvfp4_plan_get_info(plan.as_parameter, ctypes.byref(info)), "nvfp4_plan_get_info")
+    return {f: getattr(info, f) for f, _ in PlanInfo._fields_}
+
+
+# --------------------------------------------------------------------------- packer
+
+def nvfp4_pack_codes(codes):
+    """uint8 [N, K] codes (0..15) -> uint8 [N, K/2] packed (low nibble = even k)."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    N, K = codes.shape
+    out = np.empty((N, K // 2), np.uint8)
+    st = pack_lib().nvfp4_pack_codes(codes.ctypes.data, N, K, out.ctypes.data)
+    if st != NVFP4_PACK_OK:
+        raise ValueError("nvfp4_pack_codes failed with %d" % st)
+    return out
+
+
+def nvfp4_unpack_codes(packed, K):
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    N = packed.shape[0]
+    out = np.empty((N, K), np.uint8)
+    st = pack_lib().nvfp4_unpack_codes(packed.ctypes.data, N, int(K), out.ctypes.data)
+    if st != NVFP4_PACK_OK:
+        raise ValueError("nvfp4_unpack_codes failed with %d" % st)
+    return out
+
+
+def nvfp4_e4m3_encode(scales):
+    """float32 array -> uint8 E4M3 bytes (RNE, saturating at 448).  Raises on NaN / negative."""
+    s = np.ascontiguousarray(scales, dtype=np.float32)
+    out = np.empty(s.shape, np.uint8)
+    bad = ctypes.c_int64(-1)
+    st = pack_lib().nvfp4_e4m3_encode(s.ctypes.data, s.size, out.ctypes.data, ctypes.byref(bad))
+    if st != NVFP4_PACK_OK:
+        raise ValueError("nvfp4_e4m3_encode refused element %d (status %d)" % (bad.value, st))
+    return out

@@ -1,0 +1,236 @@
+// C ABI of the skinny NVFP4 projection (declared and documented in include/nvfp4_skinny.h).
+// Host side: plan creation (work split from (N, K) and the SM count only), argument checks
+// before anything is enqueued, and the two launches of a call, both with programmatic
+// dependent launch so a kernel's weight prefetch can overlap the previous kernel's tail.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <new>
+
+#include "nvfp4_skinny.h"
+#include "skinny_kernels.cuh"
+
+namespace {
+
+constexpr int kAbiVersion = 1;
+
+struct Workspace {
+  uint8_t* x16 = nullptr;    // 32 rows x K fp16, operand layout
+  float* xs = nullptr;       // [32]
+  float* partials = nullptr; // [2 * grid][32][256]
+  int* counters = nullptr;   // [row_blocks]
+  int* err = nullptr;        // [1]
+  void* base = nullptr;
+  size_t bytes = 0;
+};
+
+}  // namespace
+
+struct nvfp4_plan {
+  int64_t N = 0, K = 0;
+  nvfp4_out_dtype out = NVFP4_OUT_BF16;
+  int device = 0;
+  int sm_count = 0;
+  int grid = 0;
+  int64_t row_blocks = 0, k_steps = 0, units = 0;
+  Workspace ws;
+};
+
+namespace {
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+nvfp4_status launch_call(nvfp4_plan* plan, const void* x, int M, const uint8_t* codes, const uint8_t* scales,
+                         float gs, void* y, cudaStream_t stream) {
+  const int m_groups = (M + 7) / 8;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+
+  cudaLaunchConfig_t cfg_prep = {};
+  cfg_prep.gridDim = dim3((unsigned)(m_groups * 8));
+  cfg_prep.blockDim = dim3(256);
+  cfg_prep.dynamicSmemBytes = 0;
+  cfg_prep.stream = stream;
+  cfg_prep.attrs = attr;
+  cfg_prep.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg_prep, nvfp4::x_prep_kernel, static_cast<const uint16_t*>(x), M, plan->K,
+                                     plan->ws.x16, plan->ws.xs);
+  if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+
+  nvfp4::MainParams p;
+  p.codes = codes;
+  p.scales = scales;
+  p.x16 = plan->ws.x16;
+  p.xs = plan->ws.xs;
+  p.y = y;
+  p.partials = plan->ws.partials;
+  p.counters = plan->ws.counters;
+  p.err = plan->ws.err;
+  p.gs = gs;
+  p.M = M;
+  p.m_groups = m_groups;
+  p.out_f32 = plan->out == NVFP4_OUT_F32 ? 1 : 0;
+  p.grid = plan->grid;
+  p.N = plan->N;
+  p.K = plan->K;
+  p.S = plan->k_steps;
+  p.units = plan->units;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)plan->grid);
+  cfg.blockDim = dim3(nvfp4::kThreads);
+  cfg.dynamicSmemBytes = nvfp4::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, nvfp4::skinny_kernel, p);
+  if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+  return NVFP4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* nvfp4_status_string(nvfp4_status status) {
+  switch (status) {
+    case NVFP4_OK: return "NVFP4_OK";
+    case NVFP4_ERR_ARG: return "NVFP4_ERR_ARG: null plan or pointer, or invalid enum";
+    case NVFP4_ERR_SHAPE: return "NVFP4_ERR_SHAPE: need N >= 1 and K a positive multiple of 256";
+    case NVFP4_ERR_ALIGN: return "NVFP4_ERR_ALIGN: x, y, w_codes and w_block_scales must be 16-byte aligned";
+    case NVFP4_ERR_M_RANGE: return "NVFP4_ERR_M_RANGE: M must be in 1..32";
+    case NVFP4_ERR_CUDA: return "NVFP4_ERR_CUDA: a CUDA runtime call failed";
+    case NVFP4_ERR_NOMEM: return "NVFP4_ERR_NOMEM: allocation failed";
+    case NVFP4_ERR_TIMEOUT: return "NVFP4_ERR_TIMEOUT: a bounded in-kernel wait ran out";
+  }
+  return "NVFP4_ERR_UNKNOWN";
+}
+
+int nvfp4_abi_version(void) { return kAbiVersion; }
+
+nvfp4_status nvfp4_plan_create_ex(int64_t N, int64_t K, nvfp4_out_dtype out_dtype, nvfp4_plan_t* out_plan) {
+  if (!out_plan) return NVFP4_ERR_ARG;
+  *out_plan = nullptr;
+  if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_F32) return NVFP4_ERR_ARG;
+  if (N < 1 || K < nvfp4::kKStep || K % nvfp4::kKStep != 0) return NVFP4_ERR_SHAPE;
+  // byte offsets of the largest row must stay far from int64 overflow, and row blocks fit an int counter array
+  if (N > (int64_t(1) << 40) / K || K > (int64_t(1) << 24)) return NVFP4_ERR_SHAPE;
+
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    return NVFP4_ERR_CUDA;
+  static bool smem_attr_set[64] = {false};
+  if (dev < 64 && !smem_attr_set[dev]) {
+    if (cudaFuncSetAttribute(nvfp4::skinny_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             nvfp4::kSmemBytes) != cudaSuccess)
+      return NVFP4_ERR_CUDA;
+    smem_attr_set[dev] = true;
+  }
+
+  nvfp4_plan* plan = new (std::nothrow) nvfp4_plan();
+  if (!plan) return NVFP4_ERR_NOMEM;
+  plan->N = N;
+  plan->K = K;
+  plan->out = out_dtype;
+  plan->device = dev;
+  plan->sm_count = sms;
+  plan->row_blocks = (N + nvfp4::kRowsPerBlock - 1) / nvfp4::kRowsPerBlock;
+  plan->k_steps = K / nvfp4::kKStep;
+  plan->units = plan->row_blocks * plan->k_steps;
+  plan->grid = (int)(plan->units < sms ? plan->units : sms);
+
+  const size_t x16_bytes = round_up((size_t)32 * (size_t)K * 2, 256);
+  const size_t xs_bytes = 256;
+  const size_t part_bytes = round_up((size_t)2 * plan->grid * nvfp4::kNmma * nvfp4::kRowsPerBlock * 4, 256);
+  const size_t cnt_bytes = round_up((size_t)plan->row_blocks * 4, 256);
+  const size_t err_bytes = 256;
+  const size_t total = x16_bytes + xs_bytes + part_bytes + cnt_bytes + err_bytes;
+  void* base = nullptr;
+  if (cudaMalloc(&base, total) != cudaSuccess) {
+    delete plan;
+    return NVFP4_ERR_NOMEM;
+  }
+  uint8_t* b = static_cast<uint8_t*>(base);
+  plan->ws.base = base;
+  plan->ws.bytes = total;
+  plan->ws.x16 = b;
+  plan->ws.xs = reinterpret_cast<float*>(b + x16_bytes);
+  plan->ws.partials = reinterpret_cast<float*>(b + x16_bytes + xs_bytes);
+  plan->ws.counters = reinterpret_cast<int*>(b + x16_bytes + xs_bytes + part_bytes);
+  plan->ws.err = reinterpret_cast<int*>(b + x16_bytes + xs_bytes + part_bytes + cnt_bytes);
+  if (cudaMemset(base, 0, total) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+    cudaFree(base);
+    delete plan;
+    return NVFP4_ERR_CUDA;
+  }
+  *out_plan = plan;
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_plan_create(int64_t N, int64_t K, nvfp4_plan_t* out_plan) {
+  return nvfp4_plan_create_ex(N, K, NVFP4_OUT_BF16, out_plan);
+}
+
+void nvfp4_plan_destroy(nvfp4_plan_t plan) {
+  if (!plan) return;
+  int prev = 0;
+  const bool have_prev = cudaGetDevice(&prev) == cudaSuccess;
+  if (cudaSetDevice(plan->device) == cudaSuccess) {
+    cudaDeviceSynchronize();
+    cudaFree(plan->ws.base);
+  }
+  if (have_prev) cudaSetDevice(prev);
+  delete plan;
+}
+
+nvfp4_status nvfp4_skinny_linear(nvfp4_plan_t plan, const void* x, int M, const uint8_t* w_codes,
+                                 const uint8_t* w_block_scales, float w_global_scale, void* y, void* stream) {
+  if (!plan || !x || !w_codes || !w_block_scales || !y) return NVFP4_ERR_ARG;
+  if (M < 1 || M > NVFP4_MAX_M) return NVFP4_ERR_M_RANGE;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(w_codes) || !aligned16(w_block_scales)) return NVFP4_ERR_ALIGN;
+  return launch_call(plan, x, M, w_codes, w_block_scales, w_global_scale, y, static_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_plan_check(nvfp4_plan_t plan, void* stream) {
+  if (!plan) return NVFP4_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return NVFP4_ERR_CUDA;
+  int err = 0;
+  if (cudaMemcpyAsync(&err, plan->ws.err, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (err != 0) {
+    const int zero = 0;
+    if (cudaMemcpyAsync(plan->ws.err, &zero, sizeof(int), cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+      return NVFP4_ERR_CUDA;
+    return NVFP4_ERR_TIMEOUT;
+  }
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_plan_get_info(nvfp4_plan_t plan, nvfp4_plan_info* info) {
+  if (!plan || !info) return NVFP4_ERR_ARG;
+  info->N = plan->N;
+  info->K = plan->K;
+  info->out_dtype = (int32_t)plan->out;
+  info->rows_per_block = nvfp4::kRowsPerBlock;
+  info->k_step = nvfp4::kKStep;
+  info->stages = nvfp4::kStages;
+  info->threads = nvfp4::kThreads;
+  info->grid = plan->grid;
+  info->sm_count = plan->sm_count;
+  info->device = plan->device;
+  info->row_blocks = plan->row_blocks;
+  info->k_steps = plan->k_steps;
+  info->units = plan->units;
+  info->workspace_bytes = (int64_t)plan->ws.bytes;
+  info->smem_bytes = nvfp4::kSmemBytes;
+  return NVFP4_OK;
+}
+
+}  // extern "C"

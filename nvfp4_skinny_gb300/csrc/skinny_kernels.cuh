@@ -1,0 +1,510 @@
+// Device kernels of the skinny NVFP4 projection y = x . dequant(W)^T on sm_103a.
+//
+//   x_prep_kernel   bf16 x [M, K] -> fp16 x16 in the tensor-core operand layout, each row
+//                   multiplied by a power of two 2^e_m chosen from that row's largest
+//                   magnitude (so the conversion is exact for every element within 2^-32
+//                   of it), plus xs[m] = 2^-e_m.
+//   skinny_kernel   persistent, one block per SM, warp-specialised:
+//                     warp 8       producer: bulk-async copies of weight rows (codes +
+//                                  block scales) and of x16 into a shared-memory ring;
+//                     warps 0-7    decoders: one weight row per thread; E2M1 x E4M3 -> fp16
+//                                  with the hardware converters (exact), written to tensor
+//                                  memory as the MMA's A operand;
+//                     warp 9       one thread issues tcgen05.mma (M=128, N=32, K=16, fp32
+//                                  accumulate in tensor memory) for two 128-row tiles;
+//                     warps 10-13  epilogue: tensor memory -> registers, times 2^-e_m and
+//                                  the per-tensor scale, rounded to bf16 (or fp32) and
+//                                  stored; split-K partials go to the workspace and the
+//                                  last block of a row block adds them in block order.
+//
+// Work split ("10 Kernels" 10.1 Row invariance): a unit is (row block of 256 weight rows,
+// k-step of 256).  The units, row-block-major, are split into `grid` contiguous, equal
+// ranges; grid = min(units, SMs).  Which block computes which part of a row's sum, the
+// order of the k16 MMAs inside a part, and the order in which parts are added all depend
+// on (N, K, grid) only.  Activation row m is column m of every MMA, and nothing a column
+// computes depends on another column, so a row's bits do not depend on M.
+#pragma once
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace nvfp4 {
+
+// ------------------------------------------------------------------ configuration
+constexpr int kTileRows = 128;                        // MMA M
+constexpr int kTiles = 2;                             // MMA tiles per row block
+constexpr int kRowsPerBlock = kTileRows * kTiles;     // 256
+constexpr int kKStep = 256;                           // k per unit and per ring stage
+constexpr int kSubK = 64;                             // k per tensor-memory A slot
+constexpr int kSubsPerStage = kKStep / kSubK;         // 4
+constexpr int kK16PerSub = kSubK / 16;                // 4
+constexpr int kNmma = 32;                             // activation rows per MMA (MMA N)
+constexpr int kStages = 3;                            // shared-memory ring depth
+constexpr int kASlots = 4;                            // tensor-memory A ring depth
+constexpr int kCodeRowBytes = kKStep / 2;             // 128 bytes of E2M1 codes per row per stage
+constexpr int kCodeRowPitch = kCodeRowBytes + 16;     // padded: conflict-free per-row reads
+constexpr int kScaleRowBytes = kKStep / 16;           // 16 E4M3 scales per row per stage
+constexpr int kXGroupBytes = 8 * kKStep * 2;          // 8 activation rows x 256 k x fp16 = 4 KB
+constexpr int kCodeStageBytes = kRowsPerBlock * kCodeRowPitch;    // 36864
+constexpr int kScaleStageBytes = kRowsPerBlock * kScaleRowBytes;  // 4096
+constexpr int kXStageBytes = 4 * kXGroupBytes;                    // 16384
+constexpr int kStageBytes = kCodeStageBytes + kScaleStageBytes + kXStageBytes;  // 57344
+constexpr int kXStageOffset = kCodeStageBytes + kScaleStageBytes;              // 40960 (1 KB aligned)
+
+constexpr int kDecodeWarps = 8;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kEpiWarp0 = 10;
+constexpr int kEpiWarps = 4;
+constexpr int kWarps = 14;
+constexpr int kThreads = kWarps * 32;  // 448
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAColBase = 0;    // A slot a, tile t: columns a*64 + t*32 .. +32
+constexpr uint32_t kDColBase = 256;  // D buffer d, tile t: columns 256 + d*64 + t*32 .. +32
+
+// barrier indices in the barrier array
+constexpr int kBarFull = 0;                       // [kStages]  producer -> consumers (tx)
+constexpr int kBarEmpty = kBarFull + kStages;     // [kStages]  8 decoder warps + 1 MMA commit
+constexpr int kBarAFull = kBarEmpty + kStages;    // [kASlots]  8 decoder warps -> MMA
+constexpr int kBarAEmpty = kBarAFull + kASlots;   // [kASlots]  MMA commit -> decoders
+constexpr int kBarDFull = kBarAEmpty + kASlots;   // [2]        MMA commit -> epilogue
+constexpr int kBarDEmpty = kBarDFull + 2;         // [2]        4 epilogue warps -> MMA
+constexpr int kBarFinal = kBarDEmpty + 2;         // [1]        MMA drain at exit
+constexpr int kNumBars = kBarFinal + 1;
+
+constexpr int kSmemRingBytes = kStages * kStageBytes;  // 172032
+constexpr int kSmemBarOffset = kSmemRingBytes;
+constexpr int kSmemMiscOffset = kSmemBarOffset + kNumBars * 8;
+constexpr int kSmemBytes = kSmemMiscOffset + 256 + 1024;  // misc + alignment slack
+
+// instruction descriptor: kind::f16, D = f32, A = B = f16, both K-major, N = 32, M = 128
+constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(kNmma >> 3) << 17) |
+                            ((uint32_t)(kTileRows >> 4) << 24);
+
+constexpr long long kWaitLimitCycles = 4000000000LL;  // ~2 s at 2 GHz: a bounded wait
+
+enum : int { kErrTimeout = 1 };
+
+struct MainParams {
+  const uint8_t* codes;   // [N, K/2]
+  const uint8_t* scales;  // [N, K/16]
+  const uint8_t* x16;     // workspace: 4 row groups x (16*K) bytes, operand layout
+  const float* xs;        // workspace [32]: 2^-e_m
+  void* y;                // [M, N] bf16 or f32
+  float* partials;        // workspace [2*grid][32][256]
+  int* counters;          // workspace [row_blocks], zero between calls
+  int* err;               // workspace error word
+  float gs;
+  int M;
+  int m_groups;  // ceil(M / 8): activation row groups copied per stage
+  int out_f32;
+  int grid;
+  int64_t N, K;
+  int64_t S;      // k-steps = K / 256
+  int64_t units;  // row_blocks * S
+};
+
+// ------------------------------------------------------------------ work split
+__device__ __forceinline__ int64_t unit_begin(int64_t p, int64_t T, int64_t G) { return p * T / G; }
+__device__ __forceinline__ int64_t block_of_unit(int64_t u, int64_t T, int64_t G) { return ((u + 1) * G - 1) / T; }
+__device__ __forceinline__ int partial_slot(int64_t p, int64_t rb, int64_t T, int64_t G, int64_t S) {
+  return (int)(2 * p + (rb == unit_begin(p, T, G) / S ? 0 : 1));
+}
+
+// ------------------------------------------------------------------ bounded waits
+struct Abort {
+  volatile int* flag;  // shared: set once any role gives up
+  int* err;            // global error word
+};
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Abort& ab) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (*ab.flag) return false;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      *ab.flag = 1;
+      atomicOr(ab.err, kErrTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+
+// UMMA shared-memory descriptor, K-major, no swizzle: core matrices of 8 rows x 16 bytes;
+// LBO = distance between the two k-halves of a k16 block, SBO = distance between 8-row groups.
+__device__ __forceinline__ uint64_t x_desc(uint32_t addr) {
+  constexpr uint64_t lbo = 128, sbo = kXGroupBytes;
+  return (uint64_t)((addr >> 4) & 0x3FFF) | (((lbo >> 4) & 0x3FFF) << 16) | (((sbo >> 4) & 0x3FFF) << 32) |
+         (1ull << 46);
+}
+
+// ------------------------------------------------------------------ activation conversion
+// One block per activation row m < 8 * ceil(M / 8); rows m >= M are written as zeros.
+// x16 layout: row group g = m / 8 owns bytes [g * 16K, (g + 1) * 16K); inside it, k16 block
+// j at j * 256, k-half h at + h * 128, row m % 8 at + (m % 8) * 16, 8 fp16 per 16 bytes.
+__global__ void __launch_bounds__(256) x_prep_kernel(const uint16_t* __restrict__ x, int M, int64_t K,
+                                                     uint8_t* __restrict__ x16, float* __restrict__ xs) {
+  ptx::grid_launch_dependents();
+  ptx::grid_dependency_wait();  // x is produced upstream; x16 / xs are read by the previous call
+  const int m = blockIdx.x;
+  const int64_t K8 = K / 8;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (int64_t)m * K);
+  __shared__ float red[8];
+  float amax = 0.f;
+  if (m < M) {
+    for (int64_t i = threadIdx.x; i < K8; i += blockDim.x) {
+      const uint4 v = __ldg(xr + i);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        amax = fmaxf(amax, fabsf(__uint_as_float(w[q] << 16)));
+        amax = fmaxf(amax, fabsf(__uint_as_float(w[q] & 0xFFFF0000u)));
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+  // amax = f * 2^E, f in [0.5, 1): e = 16 - E puts amax * 2^e in [2^15, 2^16).
+  int e = 0;
+  if (amax > 0.f && amax <= 3.4028234663852886e38f) {
+    int E;
+    (void)frexpf(amax, &E);
+    e = 16 - E;
+  }
+  const int e1 = e / 2, e2 = e - e1;
+  const float f1 = ldexpf(1.f, e1), f2 = ldexpf(1.f, e2);
+  uint8_t* grp = x16 + (int64_t)(m / 8) * 16 * K + (m % 8) * 16;
+  for (int64_t i = threadIdx.x; i < K8; i += blockDim.x) {
+    uint4 o = make_uint4(0u, 0u, 0u, 0u);
+    if (m < M) {
+      const uint4 v = __ldg(xr + i);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t r[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float lo = __uint_as_float(w[q] << 16) * f1 * f2;
+        const float hi = __uint_as_float(w[q] & 0xFFFF0000u) * f1 * f2;
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r[q]) : "f"(hi), "f"(lo));
+      }
+      o = make_uint4(r[0], r[1], r[2], r[3]);
+    }
+    *reinterpret_cast<uint4*>(grp + (i / 2) * 256 + (i % 2) * 128) = o;
+  }
+  if (threadIdx.x == 0) xs[m] = (m < M) ? ldexpf(1.f, -e) : 1.f;
+}
+
+// ------------------------------------------------------------------ main kernel
+__global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const MainParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSmemBarOffset);
+  uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + kSmemMiscOffset);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemMiscOffset + 4);
+  volatile int* fix_flag = reinterpret_cast<volatile int*>(smem + kSmemMiscOffset + 8);
+  float* xs_smem = reinterpret_cast<float*>(smem + kSmemMiscOffset + 128);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t smem_base = ptx::smem_addr(smem);
+  const uint32_t bar_base = ptx::smem_addr(bars);
+  auto bar = [&](int i) { return bar_base + 8u * (uint32_t)i; };
+
+  const int64_t T = p.units, G = p.grid, S = p.S;
+  const int64_t u_begin = unit_begin(blockIdx.x, T, G), u_end = unit_begin(blockIdx.x + 1, T, G);
+  const int n_local = (int)(u_end - u_begin);
+
+  // ---- set-up: barriers, x slots zeroed, tensor memory
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(bar(kBarFull + s), 1);
+      ptx::mbar_init(bar(kBarEmpty + s), kDecodeWarps + 1);
+    }
+    for (int a = 0; a < kASlots; ++a) {
+      ptx::mbar_init(bar(kBarAFull + a), kDecodeWarps);
+      ptx::mbar_init(bar(kBarAEmpty + a), 1);
+    }
+    for (int d = 0; d < 2; ++d) {
+      ptx::mbar_init(bar(kBarDFull + d), 1);
+      ptx::mbar_init(bar(kBarDEmpty + d), kEpiWarps);
+    }
+    ptx::mbar_init(bar(kBarFinal), 1);
+    *abort_flag = 0;
+    *fix_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  for (int s = 0; s < kStages; ++s) {
+    uint4* xz = reinterpret_cast<uint4*>(smem + s * kStageBytes + kXStageOffset);
+    for (int i = threadIdx.x; i < kXStageBytes / 16; i += kThreads) xz[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  ptx::fence_proxy_async_smem();
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_addr(tmem_base_smem), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  ptx::grid_launch_dependents();
+  const uint32_t tmem = *tmem_base_smem;
+  const Abort ab{abort_flag, p.err};
+
+  if (warp == kProducerWarp) {
+    // ================================================================ producer
+    const uint64_t pol_w = ptx::policy_evict_first();
+    const uint64_t pol_x = ptx::policy_evict_last();
+    const int64_t half_k = p.K / 2, sixteenth_k = p.K / 16;
+    const int prologue = n_local < kStages ? n_local : kStages;
+    auto issue_weights = [&](int i) {
+      const int64_t u = u_begin + i, rb = u / S, s = u % S;
+      const int st = i % kStages;
+      const int64_t row0 = rb * kRowsPerBlock;
+      const int valid = (int)((p.N - row0) < kRowsPerBlock ? (p.N - row0) : kRowsPerBlock);
+      const uint32_t stage = smem_base + (uint32_t)(st * kStageBytes);
+      const uint32_t fb = bar(kBarFull + st);
+      if (lane == 0)
+        ptx::mbar_arrive_expect_tx(fb, (uint32_t)valid * (kCodeRowBytes + kScaleRowBytes) +
+                                           (uint32_t)p.m_groups * kXGroupBytes);
+      __syncwarp();
+      for (int r = lane; r < valid; r += 32) {
+        const int64_t row = row0 + r;
+        ptx::bulk_g2s(stage + (uint32_t)(r * kCodeRowPitch), p.codes + row * half_k + s * kCodeRowBytes,
+                      kCodeRowBytes, fb, pol_w);
+        ptx::bulk_g2s(stage + (uint32_t)(kCodeStageBytes + r * kScaleRowBytes),
+                      p.scales + row * sixteenth_k + s * kScaleRowBytes, kScaleRowBytes, fb, pol_w);
+      }
+    };
+    auto issue_x = [&](int i) {
+      const int64_t s = (u_begin + i) % S;
+      const int st = i % kStages;
+      if (lane < p.m_groups)
+        ptx::bulk_g2s(smem_base + (uint32_t)(st * kStageBytes + kXStageOffset + lane * kXGroupBytes),
+                      p.x16 + (int64_t)lane * 16 * p.K + s * kXGroupBytes, kXGroupBytes, bar(kBarFull + st), pol_x);
+    };
+    // weights do not depend on earlier kernels: stream them before the dependency wait
+    for (int i = 0; i < prologue; ++i) issue_weights(i);
+    ptx::grid_dependency_wait();
+    for (int i = 0; i < prologue; ++i) issue_x(i);
+    bool ok = true;
+    for (int i = prologue; i < n_local && ok; ++i) {
+      const int st = i % kStages, round = i / kStages;
+      ok = wait_bar(bar(kBarEmpty + st), (uint32_t)((round & 1) ^ 1), ab);
+      if (!ok) break;
+      issue_weights(i);
+      issue_x(i);
+    }
+    // drain: the last fill of every stage must have landed before the block exits
+    for (int st = 0; st < kStages && st < n_local; ++st) {
+      const int last = st + ((n_local - 1 - st) / kStages) * kStages;
+      const int round = last / kStages;
+      wait_bar(bar(kBarFull + st), (uint32_t)(round & 1), ab);
+    }
+  } else if (warp < kDecodeWarps) {
+    // ================================================================ decoders
+    const int tile = warp >> 2, quad = warp & 3;
+    const int row_in_block = tile * kTileRows + quad * 32 + lane;
+    const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
+    int a_use = 0;
+    bool ok = true;
+    for (int i = 0; i < n_local && ok; ++i) {
+      const int st = i % kStages, round = i / kStages;
+      ok = wait_bar(bar(kBarFull + st), (uint32_t)(round & 1), ab);
+      if (!ok) break;
+      const uint8_t* stage = smem + st * kStageBytes;
+      const uint4* crow = reinterpret_cast<const uint4*>(stage + row_in_block * kCodeRowPitch);
+      uint4 c[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) c[q] = crow[q];
+      const uint4 sc = *reinterpret_cast<const uint4*>(stage + kCodeStageBytes + row_in_block * kScaleRowBytes);
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(kBarEmpty + st));
+      const uint32_t sw[4] = {sc.x, sc.y, sc.z, sc.w};
+#pragma unroll
+      for (int sub = 0; sub < kSubsPerStage; ++sub) {
+        // k [64 sub, 64 sub + 64): code words from c[2 sub], c[2 sub + 1]; scale blocks 4 sub .. 4 sub + 3
+        const uint32_t s0 = ptx::e4m3_pair(sw[sub], 0), s1 = ptx::e4m3_pair(sw[sub], 1);
+        const uint32_t s2 = ptx::e4m3_pair(sw[sub], 2), s3 = ptx::e4m3_pair(sw[sub], 3);
+        const uint4 lo = c[2 * sub], hi = c[2 * sub + 1];
+        uint32_t o[32];
+        ptx::e2m1x8_scaled(lo.x, s0, o[0], o[1], o[2], o[3]);
+        ptx::e2m1x8_scaled(lo.y, s0, o[4], o[5], o[6], o[7]);
+        ptx::e2m1x8_scaled(lo.z, s1, o[8], o[9], o[10], o[11]);
+        ptx::e2m1x8_scaled(lo.w, s1, o[12], o[13], o[14], o[15]);
+        ptx::e2m1x8_scaled(hi.x, s2, o[16], o[17], o[18], o[19]);
+        ptx::e2m1x8_scaled(hi.y, s2, o[20], o[21], o[22], o[23]);
+        ptx::e2m1x8_scaled(hi.z, s3, o[24], o[25], o[26], o[27]);
+        ptx::e2m1x8_scaled(hi.w, s3, o[28], o[29], o[30], o[31]);
+        const int slot = a_use % kASlots, around = a_use / kASlots;
+        ok = wait_bar(bar(kBarAEmpty + slot), (uint32_t)((around & 1) ^ 1), ab);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        ptx::tmem_st32(t_lane + kAColBase + (uint32_t)(slot * 64 + tile * 32), o);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar(kBarAFull + slot));
+        ++a_use;
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ================================================================ MMA issuer
+    if (lane == 0) {
+      int a_use = 0, dbuf = 0;
+      int d_use[2] = {0, 0};
+      bool ok = true;
+      for (int i = 0; i < n_local && ok; ++i) {
+        const int64_t u = u_begin + i, s = u % S;
+        const bool seg_start = (i == 0) || (s == 0);
+        const bool seg_end = (i == n_local - 1) || (s == S - 1);
+        const int st = i % kStages, round = i / kStages;
+        if (seg_start) {
+          ok = wait_bar(bar(kBarDEmpty + dbuf), (uint32_t)((d_use[dbuf] & 1) ^ 1), ab);
+          if (!ok) break;
+        }
+        ok = wait_bar(bar(kBarFull + st), (uint32_t)(round & 1), ab);
+        if (!ok) break;
+        const uint32_t xstage = smem_base + (uint32_t)(st * kStageBytes + kXStageOffset);
+        for (int sub = 0; sub < kSubsPerStage && ok; ++sub) {
+          const int slot = a_use % kASlots, around = a_use / kASlots;
+          ok = wait_bar(bar(kBarAFull + slot), (uint32_t)(around & 1), ab);
+          if (!ok) break;
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int t = 0; t < kTiles; ++t) {
+#pragma unroll
+            for (int kk = 0; kk < kK16PerSub; ++kk) {
+              const int j = sub * kK16PerSub + kk;
+              const uint32_t acc = (seg_start && sub == 0 && kk == 0) ? 0u : 1u;
+              ptx::mma_f16_ts(tmem + kDColBase + (uint32_t)(dbuf * 64 + t * 32),
+                              tmem + kAColBase + (uint32_t)(slot * 64 + t * 32 + kk * 8),
+                              x_desc(xstage + (uint32_t)(j * 256)), kIdesc, acc);
+            }
+          }
+          ptx::mma_commit(bar(kBarAEmpty + slot));
+          ++a_use;
+        }
+        if (!ok) break;
+        ptx::mma_commit(bar(kBarEmpty + st));
+        if (seg_end) {
+          ptx::mma_commit(bar(kBarDFull + dbuf));
+          ++d_use[dbuf];
+          dbuf ^= 1;
+        }
+      }
+      // drain every MMA issued before tensor memory is released
+      ptx::mma_commit(bar(kBarFinal));
+      wait_bar(bar(kBarFinal), 0u, ab);
+    }
+    __syncwarp();
+  } else {
+    // ================================================================ epilogue
+    const int quad = warp & 3;
+    const int etid = (warp - kEpiWarp0) * 32 + lane;  // 0..127
+    ptx::grid_dependency_wait();  // xs, partials, counters and y belong to the previous call until here
+    if (etid < 32) xs_smem[etid] = p.xs[etid];
+    ptx::named_bar_sync(1, kEpiWarps * 32);
+    const int M = p.M;
+    const float gs = p.gs;
+    int dbuf = 0;
+    int d_use[2] = {0, 0};
+    bool ok = true;
+    for (int i = 0; i < n_local && ok; ++i) {
+      const int64_t u = u_begin + i, rb = u / S, s = u % S;
+      const bool seg_end = (i == n_local - 1) || (s == S - 1);
+      if (!seg_end) continue;
+      ok = wait_bar(bar(kBarDFull + dbuf), (uint32_t)(d_use[dbuf] & 1), ab);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      uint32_t v0[32], v1[32];
+      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + kDColBase + (uint32_t)(dbuf * 64);
+      ptx::tmem_ld32(taddr, v0);
+      ptx::tmem_ld32(taddr + 32, v1);
+      ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(kBarDEmpty + dbuf));
+      ++d_use[dbuf];
+      dbuf ^= 1;
+
+      const int r0 = quad * 32 + lane, r1 = r0 + kTileRows;  // rows inside the row block
+      const int64_t n0 = rb * kRowsPerBlock + r0, n1 = rb * kRowsPerBlock + r1;
+      const int64_t pf = block_of_unit(rb * S, T, G), pl = block_of_unit(rb * S + S - 1, T, G);
+      if (pf == pl) {
+        // the whole K of this row block was summed here
+#pragma unroll
+        for (int m = 0; m < kNmma; ++m) {
+          if (m < M) {
+            const float a0 = __uint_as_float(v0[m]) * xs_smem[m] * gs;
+            const float a1 = __uint_as_float(v1[m]) * xs_smem[m] * gs;
+            if (p.out_f32) {
+              float* y = static_cast<float*>(p.y) + (int64_t)m * p.N;
+              if (n0 < p.N) y[n0] = a0;
+              if (n1 < p.N) y[n1] = a1;
+            } else {
+              uint16_t* y = static_cast<uint16_t*>(p.y) + (int64_t)m * p.N;
+              if (n0 < p.N) y[n0] = ptx::f32_to_bf16_rn(a0);
+              if (n1 < p.N) y[n1] = ptx::f32_to_bf16_rn(a1);
+            }
+          }
+        }
+      } else {
+        // split row block: publish this part, the last part to arrive adds all parts in block order
+        const int slot = partial_slot(blockIdx.x, rb, T, G, S);
+        float* part = p.partials + (int64_t)slot * (kNmma * kRowsPerBlock);
+#pragma unroll
+        for (int m = 0; m < kNmma; ++m) {
+          if (m < M) {
+            part[m * kRowsPerBlock + r0] = __uint_as_float(v0[m]) * xs_smem[m];
+            part[m * kRowsPerBlock + r1] = __uint_as_float(v1[m]) * xs_smem[m];
+          }
+        }
+        __threadfence();
+        ptx::named_bar_sync(1, kEpiWarps * 32);
+        if (etid == 0) {
+          const int old = atomicAdd(p.counters + rb, 1);
+          *fix_flag = (old == (int)(pl - pf)) ? 1 : 0;
+        }
+        ptx::named_bar_sync(1, kEpiWarps * 32);
+        if (*fix_flag) {
+          __threadfence();
+          for (int m = 0; m < M; ++m) {
+            float s0 = 0.f, s1 = 0.f;
+            for (int64_t q = pf; q <= pl; ++q) {
+              const float* pp = p.partials + (int64_t)partial_slot(q, rb, T, G, S) * (kNmma * kRowsPerBlock) +
+                                m * kRowsPerBlock;
+              s0 += __ldcg(pp + r0);
+              s1 += __ldcg(pp + r1);
+            }
+            s0 *= gs;
+            s1 *= gs;
+            if (p.out_f32) {
+              float* y = static_cast<float*>(p.y) + (int64_t)m * p.N;
+              if (n0 < p.N) y[n0] = s0;
+              if (n1 < p.N) y[n1] = s1;
+            } else {
+              uint16_t* y = static_cast<uint16_t*>(p.y) + (int64_t)m * p.N;
+              if (n0 < p.N) y[n0] = ptx::f32_to_bf16_rn(s0);
+              if (n1 < p.N) y[n1] = ptx::f32_to_bf16_rn(s1);
+            }
+          }
+          if (etid == 0) p.counters[rb] = 0;
+        }
+        ptx::named_bar_sync(1, kEpiWarps * 32);
+      }
+    }
+  }
+
+  // ---- teardown: every tensor-memory operation has completed (waited above)
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace nvfp4

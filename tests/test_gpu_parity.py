@@ -1,0 +1,262 @@
+"""CUDA path (through the C ABI) against the CPU oracle, element by element.
+
+Tolerance (stated acceptance bound): |y - y_ref| <= 4e-3 * sum_k |w_k x_k| + one bfloat16
+ulp of |y_ref|, per element.  Row invariance ("10 Kernels" 10.1) is a separate, bitwise gate.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_cases import Case, to_f64, within_tolerance
+from nvfp4_skinny_gb300 import binding as nb
+from nvfp4_skinny_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from nvfp4_skinny_gb300 import build
+    build.build()
+    torch.cuda.init()
+
+
+def _plan(N, K, f32=False):
+    return nb.nvfp4_plan_create_ex(N, K, nb.NVFP4_OUT_F32 if f32 else nb.NVFP4_OUT_BF16)
+
+
+def _full_check(case, plan, M=None):
+    M = case.M if M is None else M
+    y = case.run(plan, M)
+    torch.cuda.synchronize()
+    assert nb.nvfp4_plan_check(plan) == nb.NVFP4_OK
+    y_ref, absdot = case.oracle_full()
+    ok, ratio = within_tolerance(to_f64(y), y_ref[:M], absdot[:M])
+    assert ok, "max |err|/tol = %.3g" % ratio
+    return y
+
+
+# ------------------------------------------------------------------ small shapes, every element
+
+def test_tiny_workload():
+    """The tiny workload: N=256, K=512, M=1, gs=0.01."""
+    w = synth.WORKLOADS["tiny"].projections[0]
+    case = Case(w.N, w.K, 1, w.seed)
+    _full_check(case, _plan(w.N, w.K))
+
+
+@pytest.mark.parametrize("N,K", [(256, 256), (300, 768), (1000, 2048), (17, 512), (513, 1280)])
+@pytest.mark.parametrize("M", [1, 5, 8, 9, 16, 17, 31, 32])
+def test_small_shapes_all_elements(N, K, M):
+    """Several row blocks and k-steps, ragged last row block, every M band."""
+    case = Case(N, K, M, seed=100 + N + K + M, outlier_frac=0.01)
+    _full_check(case, _plan(N, K))
+
+
+def test_f32_output_small():
+    case = Case(640, 1024, 7, seed=7)
+    plan = _plan(640, 1024, f32=True)
+    y = case.run(plan)
+    torch.cuda.synchronize()
+    assert y.dtype == torch.float32
+    y_ref, absdot = case.oracle_full()
+    ok, ratio = within_tolerance(to_f64(y), y_ref, absdot)
+    assert ok, ratio
+
+
+def test_split_k_fixup_path_every_element():
+    """More units than SMs with row blocks split across blocks: N=2048, K=8192 (every element)."""
+    N, K, M = 2048, 8192, 9
+    plan = _plan(N, K)
+    info = nb.nvfp4_plan_get_info(plan)
+    assert info["units"] > info["grid"]
+    case = Case(N, K, M, seed=21)
+    _full_check(case, plan)
+
+
+# ------------------------------------------------------------------ edge cases
+
+def _case_with_x(N, K, xf32, seed=5, gs=None):
+    x = torch.as_tensor(np.asarray(xf32, np.float32)).to(torch.bfloat16)
+    return Case(N, K, x.shape[0], seed, x=x, gs=gs)
+
+
+def test_zero_rows_and_mixed_magnitudes():
+    K = 1024
+    rng = np.random.default_rng(3)
+    x = np.zeros((6, K), np.float32)
+    x[1] = rng.standard_normal(K) * 2.0 ** -100     # tiny row
+    x[2] = rng.standard_normal(K) * 2.0 ** 100      # huge row
+    x[3] = rng.standard_normal(K)
+    x[3, 7] = 3.0e4                                 # one large outlier
+    x[4] = rng.standard_normal(K) * 2.0 ** -120     # bf16 subnormal-range row
+    x[5, ::3] = 1.0
+    case = _case_with_x(384, K, x)
+    y = _full_check(case, _plan(384, K))
+    assert torch.all(y[0] == 0)
+
+
+def test_extreme_scales_and_codes():
+    N, K = 256, 512
+    codes = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, generator=torch.Generator().manual_seed(9))
+    scales = torch.full((N, K // 16), 0x7E, dtype=torch.uint8)   # 448, the E4M3 maximum
+    scales[::2] = 0x01                                           # 2^-9, the smallest subnormal
+    scales[5] = 0x00                                             # zero scale
+    codes[7] = 0x88                                              # -0 codes
+    x = synth.activations(4, K, 11)
+    case = Case(N, K, 4, 0, x=x, codes=codes, scales=scales, gs=1.0)
+    _full_check(case, _plan(N, K))
+
+
+@pytest.mark.parametrize("gs", [0.0, -1.0, 1.0e-3, 7.5])
+def test_global_scale_values(gs):
+    case = Case(256, 512, 3, seed=12, gs=gs)
+    _full_check(case, _plan(256, 512))
+
+
+# ------------------------------------------------------------------ row invariance (bitwise)
+
+def _row_invariance(N, K, seed, Ms=range(1, 33), f32=False):
+    plan = _plan(N, K, f32)
+    x_all = synth.activations(32, K, seed, outlier_frac=0.01).cuda()
+    case = Case(N, K, 32, seed, x=x_all.cpu())
+    singles = []
+    for r in range(32):
+        singles.append(case.run(plan, 1, x=x_all[r:r + 1].contiguous()))
+    for M in Ms:
+        y = case.run(plan, M, x=x_all[:M].contiguous())
+        for r in range(M):
+            assert torch.equal(y[r], singles[r][0]), "row %d differs at M=%d" % (r, M)
+    assert nb.nvfp4_plan_check(plan) == nb.NVFP4_OK
+
+
+def test_row_invariance_square():
+    _row_invariance(5120, 5120, seed=2)
+
+
+@pytest.mark.parametrize("N,K", [(7168, 5120), (5120, 17408), (300, 768)])
+def test_row_invariance_other_shapes(N, K):
+    _row_invariance(N, K, seed=N % 97, Ms=(1, 2, 8, 9, 16, 17, 24, 32))
+
+
+def test_row_invariance_head_f32():
+    _row_invariance(152064, 5120, seed=6, Ms=(1, 16, 17, 32), f32=True)
+
+
+# ------------------------------------------------------------------ determinism, graphs
+
+def test_repeat_and_graph_bit_identical():
+    N, K, M = 5120, 5120, 17
+    plan = _plan(N, K)
+    case = Case(N, K, M, seed=33)
+    y0 = case.run(plan)
+    y1 = case.run(plan)
+    torch.cuda.synchronize()
+    assert torch.equal(y0, y1)
+    s = torch.cuda.Stream()
+    yg = torch.empty_like(y0)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        nb.nvfp4_skinny_linear(plan, case.d_x, M, case.d_codes, case.d_scales, case.gs, yg, stream=s)  # warm
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            nb.nvfp4_skinny_linear(plan, case.d_x, M, case.d_codes, case.d_scales, case.gs, yg, stream=s)
+    yg.zero_()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(yg, y0)
+    assert nb.nvfp4_plan_check(plan) == nb.NVFP4_OK
+
+
+def test_back_to_back_different_plans():
+    """Calls of several plans queued on one stream (the decode-round pattern) give the
+    same bits as the same calls made one at a time."""
+    shapes = [(7168, 5120), (5120, 5120), (34816, 5120), (5120, 17408)]
+    plans = [_plan(N, K) for N, K in shapes]
+    cases = [Case(N, K, 16, seed=40 + i) for i, (N, K) in enumerate(shapes)]
+    alone = []
+    for pl, c in zip(plans, cases):
+        alone.append(c.run(pl))
+        torch.cuda.synchronize()
+    queued = [c.run(pl) for pl, c in zip(plans, cases)] * 1
+    queued += [c.run(pl) for pl, c in zip(plans, cases)]
+    torch.cuda.synchronize()
+    for i in range(len(shapes)):
+        assert torch.equal(queued[i], alone[i])
+        assert torch.equal(queued[i + len(shapes)], alone[i])
+
+
+# ------------------------------------------------------------------ full-size workloads, sampled
+
+def _sampled(case, plan, M, n_samples=384, seed=0):
+    y = case.run(plan, M)
+    torch.cuda.synchronize()
+    assert nb.nvfp4_plan_check(plan) == nb.NVFP4_OK
+    rng = np.random.default_rng(seed)
+    ms = np.concatenate([rng.integers(0, M, n_samples), np.full(4, M - 1)])
+    ns = np.concatenate([rng.integers(0, case.N, n_samples), [0, case.N - 1, case.N - 2, case.N // 2]])
+    y_ref, absdot = case.oracle_at(ms, ns)
+    yg = to_f64(y)[ms, ns]
+    ok, ratio = within_tolerance(yg, y_ref, absdot)
+    assert ok, "max |err|/tol = %.3g" % ratio
+
+
+@pytest.mark.parametrize("wl", ["square", "qkv_down", "wide_head"])
+def test_full_size_workloads_sampled(wl):
+    w = synth.WORKLOADS[wl]
+    for pj in w.projections:
+        plan = _plan(pj.N, pj.K, pj.f32_out)
+        x = synth.activations(32, pj.K, pj.seed, outlier_frac=w.outlier_frac)
+        case = Case(pj.N, pj.K, 32, pj.seed, x=x)
+        for M in w.Ms:
+            xm = case.d_x[:M].contiguous()
+            y = case.run(plan, M, x=xm)
+            torch.cuda.synchronize()
+            rng = np.random.default_rng(M)
+            ms = rng.integers(0, M, 256)
+            ns = rng.integers(0, pj.N, 256)
+            y_ref, absdot = case.oracle_at(ms, ns)
+            ok, ratio = within_tolerance(to_f64(y)[ms, ns], y_ref, absdot)
+            assert ok, (pj.name, M, ratio)
+        assert nb.nvfp4_plan_check(plan) == nb.NVFP4_OK
+
+
+def test_round_workload_first_layer_sampled():
+    """The decode-round shapes with their per-(layer, projection) seeds, layer 0."""
+    for pj in synth.WORKLOADS["round"].projections[:4]:
+        plan = _plan(pj.N, pj.K)
+        case = Case(pj.N, pj.K, 32, pj.seed)
+        _sampled(case, plan, 32, seed=pj.seed)
+
+
+# ------------------------------------------------------------------ argument errors (nothing launched)
+
+def test_argument_errors():
+    plan = _plan(256, 512)
+    case = Case(256, 512, 2, seed=1)
+    y = torch.empty((2, 256), dtype=torch.bfloat16, device="cuda")
+    lin = lambda **kw: nb.nvfp4_skinny_linear(
+        kw.get("plan", plan), kw.get("x", case.d_x), kw.get("M", 2), kw.get("codes", case.d_codes),
+        kw.get("scales", case.d_scales), 1.0, kw.get("y", y), check=False)
+    assert lin(M=0) == nb.NVFP4_ERR_M_RANGE
+    assert lin(M=33) == nb.NVFP4_ERR_M_RANGE
+    assert lin(x=0) == nb.NVFP4_ERR_ARG
+    assert lin(codes=0) == nb.NVFP4_ERR_ARG
+    assert lin(y=0) == nb.NVFP4_ERR_ARG
+    assert lin(plan=0) == nb.NVFP4_ERR_ARG
+    assert lin(x=case.d_x.data_ptr() + 2) == nb.NVFP4_ERR_ALIGN
+    assert lin(codes=case.d_codes.data_ptr() + 8) == nb.NVFP4_ERR_ALIGN
+    assert lin() == nb.NVFP4_OK
+    torch.cuda.synchronize()
+    assert nb.nvfp4_plan_check(plan) == nb.NVFP4_OK
+
+
+def test_plan_info_independent_of_M():
+    for N, K in [(5120, 5120), (152064, 5120), (256, 512), (5120, 17408)]:
+        info = nb.nvfp4_plan_get_info(_plan(N, K))
+        assert info["N"] == N and info["K"] == K
+        assert info["row_blocks"] == -(-N // info["rows_per_block"])
+        assert info["units"] == info["row_blocks"] * (K // info["k_step"])
+        assert info["grid"] == min(info["units"], info["sm_count"])
