@@ -2,6 +2,8 @@
 // Host side: plan creation (work split from (N, K) and the SM count only), argument checks
 // before anything is enqueued, and the two launches of a call, both with programmatic
 // dependent launch so a kernel's weight prefetch can overlap the previous kernel's tail.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -29,6 +31,11 @@ struct Workspace {
 
 struct nvfp4_plan {
   int64_t N = 0, K = 0;
+  // tensor maps of the last weight seen (host-side cache; encoding is host-only work)
+  const void* tm_codes_ptr = nullptr;
+  const void* tm_scales_ptr = nullptr;
+  CUtensorMap tm_codes;
+  CUtensorMap tm_scales;
   nvfp4_out_dtype out = NVFP4_OUT_BF16;
   int device = 0;
   int sm_count = 0;
@@ -41,11 +48,56 @@ namespace {
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+// uint8 matrix [rows, row_bytes] (row pitch = row_bytes), box [box_rows, box_bytes].
+bool encode_u8_2d(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_bytes,
+                  uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {row_bytes, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_bytes, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool prepare_tensor_maps(nvfp4_plan* plan, const uint8_t* codes, const uint8_t* scales) {
+  if (plan->tm_codes_ptr != codes) {
+    if (!encode_u8_2d(&plan->tm_codes, codes, (uint64_t)plan->K / 2, (uint64_t)plan->N, nvfp4::kCodeRowBytes,
+                      nvfp4::kRowsPerBlock, CU_TENSOR_MAP_SWIZZLE_128B))
+      return false;
+    plan->tm_codes_ptr = codes;
+  }
+  if (plan->tm_scales_ptr != scales) {
+    if (!encode_u8_2d(&plan->tm_scales, scales, (uint64_t)plan->K / 16, (uint64_t)plan->N, nvfp4::kScaleRowBytes,
+                      nvfp4::kRowsPerBlock, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return false;
+    plan->tm_scales_ptr = scales;
+  }
+  return true;
+}
+
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 nvfp4_status launch_call(nvfp4_plan* plan, const void* x, int M, const uint8_t* codes, const uint8_t* scales,
                          float gs, void* y, cudaStream_t stream) {
   const int m_groups = (M + 7) / 8;
+  if (!prepare_tensor_maps(plan, codes, scales)) return NVFP4_ERR_CUDA;  // before anything is enqueued
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -62,8 +114,8 @@ nvfp4_status launch_call(nvfp4_plan* plan, const void* x, int M, const uint8_t* 
   if (e != cudaSuccess) return NVFP4_ERR_CUDA;
 
   nvfp4::MainParams p;
-  p.codes = codes;
-  p.scales = scales;
+  p.tm_codes = plan->tm_codes;
+  p.tm_scales = plan->tm_scales;
   p.x16 = plan->ws.x16;
   p.xs = plan->ws.xs;
   p.y = y;
@@ -117,8 +169,8 @@ nvfp4_status nvfp4_plan_create_ex(int64_t N, int64_t K, nvfp4_out_dtype out_dtyp
   *out_plan = nullptr;
   if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_F32) return NVFP4_ERR_ARG;
   if (N < 1 || K < nvfp4::kKStep || K % nvfp4::kKStep != 0) return NVFP4_ERR_SHAPE;
-  // byte offsets of the largest row must stay far from int64 overflow, and row blocks fit an int counter array
-  if (N > (int64_t(1) << 40) / K || K > (int64_t(1) << 24)) return NVFP4_ERR_SHAPE;
+  // TMA row coordinates are 32-bit; byte offsets stay far from int64 overflow
+  if (N >= (int64_t(1) << 31) || K > (int64_t(1) << 24) || N > (int64_t(1) << 40) / K) return NVFP4_ERR_SHAPE;
 
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;

@@ -5,8 +5,9 @@
 //                   magnitude (so the conversion is exact for every element within 2^-32
 //                   of it), plus xs[m] = 2^-e_m.
 //   skinny_kernel   persistent, one block per SM, warp-specialised:
-//                     warp 8       producer: bulk-async copies of weight rows (codes +
-//                                  block scales) and of x16 into a shared-memory ring;
+//                     warp 8       producer: 2-D tensor copies (TMA) of a 256-row x 256-k
+//                                  block of codes (128-byte swizzle) and of its block
+//                                  scales, and bulk copies of x16, into a shared-memory ring;
 //                     warps 0-7    decoders: one weight row per thread; E2M1 x E4M3 -> fp16
 //                                  with the hardware converters (exact), written to tensor
 //                                  memory as the MMA's A operand;
@@ -25,6 +26,8 @@
 // computes depends on another column, so a row's bits do not depend on M.
 #pragma once
 
+#include <cuda.h>
+
 #include <cstdint>
 
 #include "ptx.cuh"
@@ -40,17 +43,16 @@ constexpr int kSubK = 64;                             // k per tensor-memory A s
 constexpr int kSubsPerStage = kKStep / kSubK;         // 4
 constexpr int kK16PerSub = kSubK / 16;                // 4
 constexpr int kNmma = 32;                             // activation rows per MMA (MMA N)
-constexpr int kStages = 3;                            // shared-memory ring depth
+constexpr int kStages = 4;                            // shared-memory ring depth
 constexpr int kASlots = 4;                            // tensor-memory A ring depth
 constexpr int kCodeRowBytes = kKStep / 2;             // 128 bytes of E2M1 codes per row per stage
-constexpr int kCodeRowPitch = kCodeRowBytes + 16;     // padded: conflict-free per-row reads
 constexpr int kScaleRowBytes = kKStep / 16;           // 16 E4M3 scales per row per stage
 constexpr int kXGroupBytes = 8 * kKStep * 2;          // 8 activation rows x 256 k x fp16 = 4 KB
-constexpr int kCodeStageBytes = kRowsPerBlock * kCodeRowPitch;    // 36864
+constexpr int kCodeStageBytes = kRowsPerBlock * kCodeRowBytes;    // 32768, 128-byte swizzled rows
 constexpr int kScaleStageBytes = kRowsPerBlock * kScaleRowBytes;  // 4096
 constexpr int kXStageBytes = 4 * kXGroupBytes;                    // 16384
-constexpr int kStageBytes = kCodeStageBytes + kScaleStageBytes + kXStageBytes;  // 57344
-constexpr int kXStageOffset = kCodeStageBytes + kScaleStageBytes;              // 40960 (1 KB aligned)
+constexpr int kStageBytes = kCodeStageBytes + kScaleStageBytes + kXStageBytes;  // 53248 (1 KB multiple)
+constexpr int kXStageOffset = kCodeStageBytes + kScaleStageBytes;              // 36864 (1 KB aligned)
 
 constexpr int kDecodeWarps = 8;
 constexpr int kProducerWarp = 8;
@@ -74,7 +76,7 @@ constexpr int kBarDEmpty = kBarDFull + 2;         // [2]        4 epilogue warps
 constexpr int kBarFinal = kBarDEmpty + 2;         // [1]        MMA drain at exit
 constexpr int kNumBars = kBarFinal + 1;
 
-constexpr int kSmemRingBytes = kStages * kStageBytes;  // 172032
+constexpr int kSmemRingBytes = kStages * kStageBytes;  // 212992
 constexpr int kSmemBarOffset = kSmemRingBytes;
 constexpr int kSmemMiscOffset = kSmemBarOffset + kNumBars * 8;
 constexpr int kSmemBytes = kSmemMiscOffset + 256 + 1024;  // misc + alignment slack
@@ -88,8 +90,8 @@ constexpr long long kWaitLimitCycles = 4000000000LL;  // ~2 s at 2 GHz: a bounde
 enum : int { kErrTimeout = 1 };
 
 struct MainParams {
-  const uint8_t* codes;   // [N, K/2]
-  const uint8_t* scales;  // [N, K/16]
+  CUtensorMap tm_codes;   // uint8 [N rows, K/2 bytes], box 128 B x 256 rows, 128-byte swizzle
+  CUtensorMap tm_scales;  // uint8 [N rows, K/16 bytes], box 16 B x 256 rows
   const uint8_t* x16;     // workspace: 4 row groups x (16*K) bytes, operand layout
   const float* xs;        // workspace [32]: 2^-e_m
   void* y;                // [M, N] bf16 or f32
@@ -202,7 +204,7 @@ __global__ void __launch_bounds__(256) x_prep_kernel(const uint16_t* __restrict_
 }
 
 // ------------------------------------------------------------------ main kernel
-__global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const MainParams p) {
+__global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_constant__ MainParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSmemBarOffset);
@@ -259,26 +261,24 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const MainParams p)
     // ================================================================ producer
     const uint64_t pol_w = ptx::policy_evict_first();
     const uint64_t pol_x = ptx::policy_evict_last();
-    const int64_t half_k = p.K / 2, sixteenth_k = p.K / 16;
     const int prologue = n_local < kStages ? n_local : kStages;
+    if (lane == 0) {
+      ptx::prefetch_tensormap(&p.tm_codes);
+      ptx::prefetch_tensormap(&p.tm_scales);
+    }
     auto issue_weights = [&](int i) {
       const int64_t u = u_begin + i, rb = u / S, s = u % S;
       const int st = i % kStages;
-      const int64_t row0 = rb * kRowsPerBlock;
-      const int valid = (int)((p.N - row0) < kRowsPerBlock ? (p.N - row0) : kRowsPerBlock);
       const uint32_t stage = smem_base + (uint32_t)(st * kStageBytes);
       const uint32_t fb = bar(kBarFull + st);
-      if (lane == 0)
-        ptx::mbar_arrive_expect_tx(fb, (uint32_t)valid * (kCodeRowBytes + kScaleRowBytes) +
-                                           (uint32_t)p.m_groups * kXGroupBytes);
-      __syncwarp();
-      for (int r = lane; r < valid; r += 32) {
-        const int64_t row = row0 + r;
-        ptx::bulk_g2s(stage + (uint32_t)(r * kCodeRowPitch), p.codes + row * half_k + s * kCodeRowBytes,
-                      kCodeRowBytes, fb, pol_w);
-        ptx::bulk_g2s(stage + (uint32_t)(kCodeStageBytes + r * kScaleRowBytes),
-                      p.scales + row * sixteenth_k + s * kScaleRowBytes, kScaleRowBytes, fb, pol_w);
+      if (lane == 0) {
+        // full boxes are always delivered (rows past N are zero-filled)
+        ptx::mbar_arrive_expect_tx(fb, (uint32_t)(kCodeStageBytes + kScaleStageBytes + p.m_groups * kXGroupBytes));
+        ptx::tma_load_2d(stage, &p.tm_codes, (int32_t)(s * kCodeRowBytes), (int32_t)(rb * kRowsPerBlock), fb, pol_w);
+        ptx::tma_load_2d(stage + kCodeStageBytes, &p.tm_scales, (int32_t)(s * kScaleRowBytes),
+                         (int32_t)(rb * kRowsPerBlock), fb, pol_w);
       }
+      __syncwarp();
     };
     auto issue_x = [&](int i) {
       const int64_t s = (u_begin + i) % S;
@@ -317,10 +317,12 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const MainParams p)
       ok = wait_bar(bar(kBarFull + st), (uint32_t)(round & 1), ab);
       if (!ok) break;
       const uint8_t* stage = smem + st * kStageBytes;
-      const uint4* crow = reinterpret_cast<const uint4*>(stage + row_in_block * kCodeRowPitch);
+      // 128-byte swizzle: 16-byte chunk q of row r sits at chunk q ^ (r % 8) of the row
+      const uint8_t* crow = stage + row_in_block * kCodeRowBytes;
+      const int swz = row_in_block & 7;
       uint4 c[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) c[q] = crow[q];
+      for (int q = 0; q < 8; ++q) c[q] = *reinterpret_cast<const uint4*>(crow + ((q ^ swz) << 4));
       const uint4 sc = *reinterpret_cast<const uint4*>(stage + kCodeStageBytes + row_in_block * kScaleRowBytes);
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar(kBarEmpty + st));
@@ -473,24 +475,37 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const MainParams p)
         ptx::named_bar_sync(1, kEpiWarps * 32);
         if (*fix_flag) {
           __threadfence();
-          for (int m = 0; m < M; ++m) {
-            float s0 = 0.f, s1 = 0.f;
-            for (int64_t q = pf; q <= pl; ++q) {
-              const float* pp = p.partials + (int64_t)partial_slot(q, rb, T, G, S) * (kNmma * kRowsPerBlock) +
-                                m * kRowsPerBlock;
-              s0 += __ldcg(pp + r0);
-              s1 += __ldcg(pp + r1);
+          // parts in block order; each part's values load independently, then add in order
+          float a0[kNmma], a1[kNmma];
+#pragma unroll
+          for (int m = 0; m < kNmma; ++m) a0[m] = a1[m] = 0.f;
+          for (int64_t q = pf; q <= pl; ++q) {
+            const float* pp = p.partials + (int64_t)partial_slot(q, rb, T, G, S) * (kNmma * kRowsPerBlock);
+            float t0[kNmma], t1[kNmma];
+#pragma unroll
+            for (int m = 0; m < kNmma; ++m) {
+              t0[m] = m < M ? __ldcg(pp + m * kRowsPerBlock + r0) : 0.f;
+              t1[m] = m < M ? __ldcg(pp + m * kRowsPerBlock + r1) : 0.f;
             }
-            s0 *= gs;
-            s1 *= gs;
-            if (p.out_f32) {
-              float* y = static_cast<float*>(p.y) + (int64_t)m * p.N;
-              if (n0 < p.N) y[n0] = s0;
-              if (n1 < p.N) y[n1] = s1;
-            } else {
-              uint16_t* y = static_cast<uint16_t*>(p.y) + (int64_t)m * p.N;
-              if (n0 < p.N) y[n0] = ptx::f32_to_bf16_rn(s0);
-              if (n1 < p.N) y[n1] = ptx::f32_to_bf16_rn(s1);
+#pragma unroll
+            for (int m = 0; m < kNmma; ++m) {
+              a0[m] += t0[m];
+              a1[m] += t1[m];
+            }
+          }
+#pragma unroll
+          for (int m = 0; m < kNmma; ++m) {
+            if (m < M) {
+              const float s0 = a0[m] * gs, s1 = a1[m] * gs;
+              if (p.out_f32) {
+                float* y = static_cast<float*>(p.y) + (int64_t)m * p.N;
+                if (n0 < p.N) y[n0] = s0;
+                if (n1 < p.N) y[n1] = s1;
+              } else {
+                uint16_t* y = static_cast<uint16_t*>(p.y) + (int64_t)m * p.N;
+                if (n0 < p.N) y[n0] = ptx::f32_to_bf16_rn(s0);
+                if (n1 < p.N) y[n1] = ptx::f32_to_bf16_rn(s1);
+              }
             }
           }
           if (etid == 0) p.counters[rb] = 0;
