@@ -74,7 +74,8 @@ typedef enum {
   NVFP4_ERR_M_RANGE = 4, /* M outside 1..32 */
   NVFP4_ERR_CUDA = 5,    /* a CUDA runtime call failed (launch, allocation, query) */
   NVFP4_ERR_NOMEM = 6,   /* host or device allocation failed */
-  NVFP4_ERR_TIMEOUT = 7  /* a bounded in-kernel wait ran out (reported by nvfp4_plan_check) */
+  NVFP4_ERR_TIMEOUT = 7, /* a bounded in-kernel wait ran out (reported by nvfp4_plan_check) */
+  NVFP4_ERR_SCRATCH_LIMIT = 8 /* nvfp4_skinny_linear_noalloc: the problem needs more than its fixed scratch */
 } nvfp4_status;
 
 typedef enum { NVFP4_OUT_BF16 = 0, NVFP4_OUT_F32 = 1 } nvfp4_out_dtype;
@@ -131,6 +132,39 @@ typedef struct {
 } nvfp4_plan_info;
 
 nvfp4_status nvfp4_plan_get_info(nvfp4_plan_t plan, nvfp4_plan_info* info);
+
+/* ---------------------------------------------------------------------------------------------
+ * Allocation-free variant.  The pages have no counterpart to this entry point; it exists for
+ * callers that must not allocate device memory during a call: code running inside another
+ * framework's memory pool or arena, callers that reserve all device memory up front, and
+ * contexts where a cudaMalloc would synchronise the device or fail.  The plan-based path
+ * allocates its workspace in nvfp4_plan_create*, so this entry point takes the shape directly.
+ *
+ * It computes the same y = x . dequant(W)^T with the same kernels, work split and numerics as
+ * nvfp4_skinny_linear, but its scratch (converted activations, split-K parts, split-K
+ * counters, an error word) lives in one fixed, statically sized device array inside the
+ * library.  Every GPU that loads the library holds that array, NVFP4_NOALLOC_SCRATCH_BYTES
+ * bytes, until the process exits.  Limits: K <= NVFP4_NOALLOC_MAX_K and
+ * N <= NVFP4_NOALLOC_MAX_N; larger problems are refused with NVFP4_ERR_SCRATCH_LIMIT before
+ * anything is enqueued.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * The first call on a device does a one-time set-up for that device (it looks up the device
+ * address of the scratch array and the SM count, and raises the kernel's shared-memory limit);
+ * make that first call before any stream capture on the device.  Every call on a device uses
+ * the same scratch, which keeps the previous call's contents; each call clears the parts that
+ * must start at zero (split-K counters and the error word) on `stream` before its kernels run.
+ * Calls that can overlap on the GPU (different streams without ordering between them) race on
+ * that scratch and give wrong results: order them.  In-kernel timeouts are not reported by this
+ * entry point.  Arguments, layouts and the other status codes are those of nvfp4_skinny_linear;
+ * N and K are the weight's shape and out_dtype the element type of y.
+ * ------------------------------------------------------------------------------------------- */
+#define NVFP4_NOALLOC_MAX_K 32768
+#define NVFP4_NOALLOC_MAX_N 4194304
+#define NVFP4_NOALLOC_SCRATCH_BYTES 12648960 /* about 12.1 MiB */
+
+nvfp4_status nvfp4_skinny_linear_noalloc(int64_t N, int64_t K, nvfp4_out_dtype out_dtype, const void* x, int M,
+                                         const uint8_t* w_codes, const uint8_t* w_block_scales, float w_global_scale,
+                                         void* y, void* stream);
 
 #ifdef __cplusplus
 }

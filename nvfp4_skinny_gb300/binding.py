@@ -21,6 +21,9 @@ NVFP4_ERR_M_RANGE = 4
 NVFP4_ERR_CUDA = 5
 NVFP4_ERR_NOMEM = 6
 NVFP4_ERR_TIMEOUT = 7
+NVFP4_ERR_SCRATCH_LIMIT = 8
+NVFP4_NOALLOC_MAX_K = 32768
+NVFP4_NOALLOC_MAX_N = 4194304
 NVFP4_OUT_BF16 = 0
 NVFP4_OUT_F32 = 1
 NVFP4_MAX_M = 32
@@ -31,7 +34,8 @@ NVFP4_PACK_ERR_VALUE = -2
 
 # every symbol the headers declare, per library
 CUDA_SYMBOLS = ("nvfp4_status_string", "nvfp4_abi_version", "nvfp4_plan_create", "nvfp4_plan_create_ex",
-                "nvfp4_plan_destroy", "nvfp4_skinny_linear", "nvfp4_plan_check", "nvfp4_plan_get_info")
+                "nvfp4_plan_destroy", "nvfp4_skinny_linear", "nvfp4_plan_check", "nvfp4_plan_get_info",
+                "nvfp4_skinny_linear_noalloc")
 PACK_SYMBOLS = ("nvfp4_pack_codes", "nvfp4_unpack_codes", "nvfp4_e4m3_encode")
 
 
@@ -84,6 +88,8 @@ def cuda_lib():
         lib.nvfp4_plan_check.argtypes = [p, p]
         lib.nvfp4_plan_get_info.restype = i32
         lib.nvfp4_plan_get_info.argtypes = [p, ctypes.POINTER(PlanInfo)]
+        lib.nvfp4_skinny_linear_noalloc.restype = i32
+        lib.nvfp4_skinny_linear_noalloc.argtypes = [i64, i64, i32, p, i32, p, p, ctypes.c_float, p, p]
         _cuda = lib
     return _cuda
 
@@ -193,6 +199,19 @@ def nvfp4_skinny_linear(plan, x, M, w_codes, w_block_scales, w_global_scale, y, 
                                         _stream(stream))
     if check:
         _check(st, "nvfp4_skinny_linear")
+    return st
+
+
+def nvfp4_skinny_linear_noalloc(N, K, out_dtype, x, M, w_codes, w_block_scales, w_global_scale, y, stream=None,
+                                check=True):
+    """Allocation-free call for callers that cannot allocate device memory: same result as
+    nvfp4_skinny_linear, scratch in the library's fixed device array (see the header for its
+    size, limits and the rule that calls must not overlap on the GPU)."""
+    st = cuda_lib().nvfp4_skinny_linear_noalloc(int(N), int(K), int(out_dtype), _ptr(x), int(M), _ptr(w_codes),
+                                                _ptr(w_block_scales), float(w_global_scale), _ptr(y),
+                                                _stream(stream))
+    if check:
+        _check(st, "nvfp4_skinny_linear_noalloc")
     return st
 
 

@@ -8,6 +8,7 @@
 
 #include <cstdint>
 #include <cstdlib>
+#include <mutex>
 #include <new>
 
 #include "nvfp4_skinny.h"
@@ -158,6 +159,8 @@ const char* nvfp4_status_string(nvfp4_status status) {
     case NVFP4_ERR_CUDA: return "NVFP4_ERR_CUDA: a CUDA runtime call failed";
     case NVFP4_ERR_NOMEM: return "NVFP4_ERR_NOMEM: allocation failed";
     case NVFP4_ERR_TIMEOUT: return "NVFP4_ERR_TIMEOUT: a bounded in-kernel wait ran out";
+    case NVFP4_ERR_SCRATCH_LIMIT:
+      return "NVFP4_ERR_SCRATCH_LIMIT: the allocation-free entry point takes K <= 32768 and N <= 4194304";
   }
   return "NVFP4_ERR_UNKNOWN";
 }
@@ -286,3 +289,147 @@ nvfp4_status nvfp4_plan_get_info(nvfp4_plan_t plan, nvfp4_plan_info* info) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------------------------
+// Allocation-free entry point (declared in include/nvfp4_skinny.h).  Its scratch is one fixed
+// device array in this file, laid out exactly like a plan's workspace for the largest problem
+// it accepts: activations (32 x K fp16), 2^-e factors, error word, split-K counters, parts.
+namespace {
+
+constexpr int64_t kNaMaxK = NVFP4_NOALLOC_MAX_K;
+constexpr int64_t kNaMaxN = NVFP4_NOALLOC_MAX_N;
+constexpr int64_t kNaMaxRowBlocks = kNaMaxN / nvfp4::kRowsPerBlock;
+constexpr int kNaMaxGrid = 160;  // at most this many blocks (GB300 has 152 SMs)
+constexpr size_t kNaX16Bytes = (size_t)32 * kNaMaxK * 2;
+constexpr size_t kNaXsBytes = 256;
+constexpr size_t kNaErrBytes = 256;
+constexpr size_t kNaCounterBytes = (size_t)kNaMaxRowBlocks * 4;
+constexpr size_t kNaPartBytes = (size_t)2 * kNaMaxGrid * nvfp4::kNmma * nvfp4::kRowsPerBlock * 4;
+constexpr size_t kNaScratchBytes = kNaX16Bytes + kNaXsBytes + kNaErrBytes + kNaCounterBytes + kNaPartBytes;
+static_assert(kNaScratchBytes == NVFP4_NOALLOC_SCRATCH_BYTES, "header states the scratch size");
+
+struct NoAllocDevice {
+  bool ready = false;
+  uint8_t* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+  int sms = 0;
+};
+constexpr int kNaMaxDevices = 64;
+NoAllocDevice g_na_devices[kNaMaxDevices];
+std::mutex g_na_mutex;
+
+}  // namespace
+
+// The scratch itself.  In host code this name is only a stand-in for the symbol: its device
+// address comes from cudaGetSymbolAddress during the per-device set-up below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNaScratchBytes];
+
+namespace {
+
+// One-time set-up of the current device; returns NVFP4_OK and the device record.
+nvfp4_status noalloc_device(NoAllocDevice** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (dev < 0 || dev >= kNaMaxDevices) return NVFP4_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_na_mutex);
+  NoAllocDevice& d = g_na_devices[dev];
+  if (!d.ready) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return NVFP4_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+      return NVFP4_ERR_CUDA;
+    if (cudaFuncSetAttribute(nvfp4::skinny_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             nvfp4::kSmemBytes) != cudaSuccess)
+      return NVFP4_ERR_CUDA;
+    d.scratch = static_cast<uint8_t*>(ptr);
+    d.sms = sms;
+    d.ready = true;
+  }
+  *out = &d;
+  return NVFP4_OK;
+}
+
+}  // namespace
+
+extern "C" nvfp4_status nvfp4_skinny_linear_noalloc(int64_t N, int64_t K, nvfp4_out_dtype out_dtype, const void* x,
+                                                    int M, const uint8_t* w_codes, const uint8_t* w_block_scales,
+                                                    float w_global_scale, void* y, void* stream) {
+  if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_F32) return NVFP4_ERR_ARG;
+  if (!x || !w_codes || !w_block_scales || !y) return NVFP4_ERR_ARG;
+  if (M < 1 || M > NVFP4_MAX_M) return NVFP4_ERR_M_RANGE;
+  if (N < 1 || K < nvfp4::kKStep || K % nvfp4::kKStep != 0) return NVFP4_ERR_SHAPE;
+  if (K > kNaMaxK || N > kNaMaxN) return NVFP4_ERR_SCRATCH_LIMIT;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(w_codes) || !aligned16(w_block_scales)) return NVFP4_ERR_ALIGN;
+
+  NoAllocDevice* d = nullptr;
+  const nvfp4_status st = noalloc_device(&d);
+  if (st != NVFP4_OK) return st;
+
+  const int64_t row_blocks = (N + nvfp4::kRowsPerBlock - 1) / nvfp4::kRowsPerBlock;
+  const int64_t k_steps = K / nvfp4::kKStep;
+  const int64_t units = row_blocks * k_steps;
+  int64_t grid = units < d->sms ? units : d->sms;
+  if (grid > kNaMaxGrid) grid = kNaMaxGrid;
+
+  uint8_t* base = d->scratch;
+  uint8_t* x16 = base;
+  float* xs = reinterpret_cast<float*>(base + kNaX16Bytes);
+  int* err = reinterpret_cast<int*>(base + kNaX16Bytes + kNaXsBytes);
+  int* counters = reinterpret_cast<int*>(base + kNaX16Bytes + kNaXsBytes + kNaErrBytes);
+  float* parts = reinterpret_cast<float*>(base + kNaX16Bytes + kNaXsBytes + kNaErrBytes + kNaCounterBytes);
+
+  CUtensorMap tm_codes, tm_scales;
+  if (!encode_u8_2d(&tm_codes, w_codes, (uint64_t)K / 2, (uint64_t)N, nvfp4::kCodeRowBytes, nvfp4::kRowsPerBlock,
+                    CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_u8_2d(&tm_scales, w_block_scales, (uint64_t)K / 16, (uint64_t)N, nvfp4::kScaleRowBytes,
+                    nvfp4::kRowsPerBlock, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return NVFP4_ERR_CUDA;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // what must start at zero: the split-K counters of this shape and the error word
+  if (cudaMemsetAsync(counters, 0, (size_t)row_blocks * sizeof(int), s) != cudaSuccess ||
+      cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess)
+    return NVFP4_ERR_CUDA;
+
+  const int m_groups = (M + 7) / 8;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg_prep = {};
+  cfg_prep.gridDim = dim3((unsigned)(m_groups * 8));
+  cfg_prep.blockDim = dim3(256);
+  cfg_prep.stream = s;
+  cfg_prep.attrs = attr;
+  cfg_prep.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg_prep, nvfp4::x_prep_kernel, static_cast<const uint16_t*>(x), M, K, x16, xs) !=
+      cudaSuccess)
+    return NVFP4_ERR_CUDA;
+
+  nvfp4::MainParams p;
+  p.tm_codes = tm_codes;
+  p.tm_scales = tm_scales;
+  p.x16 = x16;
+  p.xs = xs;
+  p.y = y;
+  p.partials = parts;
+  p.counters = counters;
+  p.err = err;
+  p.gs = w_global_scale;
+  p.M = M;
+  p.m_groups = m_groups;
+  p.out_f32 = out_dtype == NVFP4_OUT_F32 ? 1 : 0;
+  p.grid = (int)grid;
+  p.N = N;
+  p.K = K;
+  p.S = k_steps;
+  p.units = units;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(nvfp4::kThreads);
+  cfg.dynamicSmemBytes = nvfp4::kSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, nvfp4::skinny_kernel, p) != cudaSuccess) return NVFP4_ERR_CUDA;
+  return NVFP4_OK;
+}
