@@ -160,7 +160,7 @@ nvfp4_status nvfp4_plan_get_info(nvfp4_plan_t plan, nvfp4_plan_info* info);
  * ------------------------------------------------------------------------------------------- */
 #define NVFP4_NOALLOC_MAX_K 32768
 #define NVFP4_NOALLOC_MAX_N 4194304
-#define NVFP4_NOALLOC_SCRATCH_BYTES 12648960 /* about 12.1 MiB */
+#define NVFP4_NOALLOC_SCRATCH_BYTES 12714496 /* about 12.1 MiB */
 
 nvfp4_status nvfp4_skinny_linear_noalloc(int64_t N, int64_t K, nvfp4_out_dtype out_dtype, const void* x, int M,
                                          const uint8_t* w_codes, const uint8_t* w_block_scales, float w_global_scale,

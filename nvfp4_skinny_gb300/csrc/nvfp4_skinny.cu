@@ -22,7 +22,7 @@ struct Workspace {
   uint8_t* x16 = nullptr;    // 32 rows x K fp16, operand layout
   float* xs = nullptr;       // [32]
   float* partials = nullptr; // [2 * grid][32][256]
-  int* counters = nullptr;   // [row_blocks]
+  int* counters = nullptr;   // [2][row_blocks]
   int* err = nullptr;        // [1]
   void* base = nullptr;
   size_t bytes = 0;
@@ -105,7 +105,7 @@ nvfp4_status launch_call(nvfp4_plan* plan, const void* x, int M, const uint8_t* 
 
   cudaLaunchConfig_t cfg_prep = {};
   cfg_prep.gridDim = dim3((unsigned)(m_groups * 8));
-  cfg_prep.blockDim = dim3(256);
+  cfg_prep.blockDim = dim3(nvfp4::kPrepThreads);
   cfg_prep.dynamicSmemBytes = 0;
   cfg_prep.stream = stream;
   cfg_prep.attrs = attr;
@@ -132,6 +132,7 @@ nvfp4_status launch_call(nvfp4_plan* plan, const void* x, int M, const uint8_t* 
   p.K = plan->K;
   p.S = plan->k_steps;
   p.units = plan->units;
+  p.row_blocks = plan->row_blocks;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)plan->grid);
@@ -202,7 +203,7 @@ nvfp4_status nvfp4_plan_create_ex(int64_t N, int64_t K, nvfp4_out_dtype out_dtyp
   const size_t x16_bytes = round_up((size_t)32 * (size_t)K * 2, 256);
   const size_t xs_bytes = 256;
   const size_t part_bytes = round_up((size_t)2 * plan->grid * nvfp4::kNmma * nvfp4::kRowsPerBlock * 4, 256);
-  const size_t cnt_bytes = round_up((size_t)plan->row_blocks * 4, 256);
+  const size_t cnt_bytes = round_up((size_t)plan->row_blocks * 2 * 4, 256);
   const size_t err_bytes = 256;
   const size_t total = x16_bytes + xs_bytes + part_bytes + cnt_bytes + err_bytes;
   void* base = nullptr;
@@ -259,8 +260,9 @@ nvfp4_status nvfp4_plan_check(nvfp4_plan_t plan, void* stream) {
   if (cudaMemcpyAsync(&err, plan->ws.err, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return NVFP4_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return NVFP4_ERR_CUDA;
   if (err != 0) {
-    const int zero = 0;
-    if (cudaMemcpyAsync(plan->ws.err, &zero, sizeof(int), cudaMemcpyHostToDevice, s) != cudaSuccess ||
+    // an aborted call may leave split-K counters behind: clear them with the error word
+    if (cudaMemsetAsync(plan->ws.err, 0, sizeof(int), s) != cudaSuccess ||
+        cudaMemsetAsync(plan->ws.counters, 0, (size_t)plan->row_blocks * 2 * sizeof(int), s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
       return NVFP4_ERR_CUDA;
     return NVFP4_ERR_TIMEOUT;
@@ -303,7 +305,7 @@ constexpr int kNaMaxGrid = 160;  // at most this many blocks (GB300 has 152 SMs)
 constexpr size_t kNaX16Bytes = (size_t)32 * kNaMaxK * 2;
 constexpr size_t kNaXsBytes = 256;
 constexpr size_t kNaErrBytes = 256;
-constexpr size_t kNaCounterBytes = (size_t)kNaMaxRowBlocks * 4;
+constexpr size_t kNaCounterBytes = (size_t)kNaMaxRowBlocks * 2 * 4;
 constexpr size_t kNaPartBytes = (size_t)2 * kNaMaxGrid * nvfp4::kNmma * nvfp4::kRowsPerBlock * 4;
 constexpr size_t kNaScratchBytes = kNaX16Bytes + kNaXsBytes + kNaErrBytes + kNaCounterBytes + kNaPartBytes;
 static_assert(kNaScratchBytes == NVFP4_NOALLOC_SCRATCH_BYTES, "header states the scratch size");
@@ -387,7 +389,7 @@ extern "C" nvfp4_status nvfp4_skinny_linear_noalloc(int64_t N, int64_t K, nvfp4_
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // what must start at zero: the split-K counters of this shape and the error word
-  if (cudaMemsetAsync(counters, 0, (size_t)row_blocks * sizeof(int), s) != cudaSuccess ||
+  if (cudaMemsetAsync(counters, 0, (size_t)row_blocks * 2 * sizeof(int), s) != cudaSuccess ||
       cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess)
     return NVFP4_ERR_CUDA;
 
@@ -397,7 +399,7 @@ extern "C" nvfp4_status nvfp4_skinny_linear_noalloc(int64_t N, int64_t K, nvfp4_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg_prep = {};
   cfg_prep.gridDim = dim3((unsigned)(m_groups * 8));
-  cfg_prep.blockDim = dim3(256);
+  cfg_prep.blockDim = dim3(nvfp4::kPrepThreads);
   cfg_prep.stream = s;
   cfg_prep.attrs = attr;
   cfg_prep.numAttrs = 1;
@@ -423,6 +425,7 @@ extern "C" nvfp4_status nvfp4_skinny_linear_noalloc(int64_t N, int64_t K, nvfp4_
   p.K = K;
   p.S = k_steps;
   p.units = units;
+  p.row_blocks = row_blocks;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(nvfp4::kThreads);

@@ -11,12 +11,21 @@
 //                     warps 0-7    decoders: one weight row per thread; E2M1 x E4M3 -> fp16
 //                                  with the hardware converters (exact), written to tensor
 //                                  memory as the MMA's A operand;
-//                     warp 9       one thread issues tcgen05.mma (M=128, N=32, K=16, fp32
-//                                  accumulate in tensor memory) for two 128-row tiles;
+//                     warps 9, 14  one thread each issues tcgen05.mma (M=128, N=32, K=16,
+//                                  fp32 accumulation in tensor memory) for one of the two
+//                                  128-row tiles (an issuing thread sustains one such MMA
+//                                  per ~44 cycles; two issuers halve that per tile pair).
+//                                  An issuer never reads shared memory: any such read waits
+//                                  for its MMAs in flight, so it learns that an A slot is
+//                                  full, or a D buffer free, from hardware named barriers
+//                                  and reports completions with tcgen05.commit;
 //                     warps 10-13  epilogue: tensor memory -> registers, times 2^-e_m and
 //                                  the per-tensor scale, rounded to bf16 (or fp32) and
-//                                  stored; split-K partials go to the workspace and the
-//                                  last block of a row block adds them in block order.
+//                                  stored.  A row block split over several blocks: each
+//                                  part goes to the workspace during the main loop; at the
+//                                  end of its range every contributing block waits for all
+//                                  parts, then adds its own slice of the rows, parts in
+//                                  block order (the same order whoever arrives last).
 //
 // Work split ("10 Kernels" 10.1 Row invariance): a unit is (row block of 256 weight rows,
 // k-step of 256).  The units, row-block-major, are split into `grid` contiguous, equal
@@ -56,25 +65,30 @@ constexpr int kXStageOffset = kCodeStageBytes + kScaleStageBytes;              /
 
 constexpr int kDecodeWarps = 8;
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;    // issues tile 0's MMAs; also allocates tensor memory
 constexpr int kEpiWarp0 = 10;
 constexpr int kEpiWarps = 4;
-constexpr int kWarps = 14;
-constexpr int kThreads = kWarps * 32;  // 448
+constexpr int kMmaWarp1 = 14;  // issues tile 1's MMAs
+constexpr int kWarps = 15;
+constexpr int kThreads = kWarps * 32;  // 480
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAColBase = 0;    // A slot a, tile t: columns a*64 + t*32 .. +32
 constexpr uint32_t kDColBase = 256;  // D buffer d, tile t: columns 256 + d*64 + t*32 .. +32
 
-// barrier indices in the barrier array
-constexpr int kBarFull = 0;                       // [kStages]  producer -> consumers (tx)
-constexpr int kBarEmpty = kBarFull + kStages;     // [kStages]  8 decoder warps + 1 MMA commit
-constexpr int kBarAFull = kBarEmpty + kStages;    // [kASlots]  8 decoder warps -> MMA
-constexpr int kBarAEmpty = kBarAFull + kASlots;   // [kASlots]  MMA commit -> decoders
-constexpr int kBarDFull = kBarAEmpty + kASlots;   // [2]        MMA commit -> epilogue
-constexpr int kBarDEmpty = kBarDFull + 2;         // [2]        4 epilogue warps -> MMA
-constexpr int kBarFinal = kBarDEmpty + 2;         // [1]        MMA drain at exit
-constexpr int kNumBars = kBarFinal + 1;
+// mbarrier indices in the barrier array
+constexpr int kBarFull = 0;                               // [kStages]  producer -> consumers (tx)
+constexpr int kBarEmpty = kBarFull + kStages;             // [kStages]  8 decoder warps + 2 MMA commits
+constexpr int kBarAEmpty = kBarEmpty + kStages;           // [kASlots][tile]  MMA commit -> decoders
+constexpr int kBarDFull = kBarAEmpty + kASlots * kTiles;  // [2]        2 MMA commits -> epilogue
+constexpr int kBarFinal = kBarDFull + 2;                  // [tile]     MMA drain at exit
+constexpr int kNumBars = kBarFinal + kTiles;
+
+// hardware named barriers (0 is __syncthreads)
+constexpr uint32_t kNbEpi = 1;  // the 4 epilogue warps
+__device__ __forceinline__ uint32_t nb_afull(int slot, int tile) { return 2u + (uint32_t)(slot * kTiles + tile); }
+__device__ __forceinline__ uint32_t nb_dempty(int dbuf, int tile) { return 10u + (uint32_t)(dbuf * kTiles + tile); }
+constexpr uint32_t kNbPairThreads = 4 * 32 + 32;  // 4 decoder (or epilogue) warps + 1 issuer warp
 
 constexpr int kSmemRingBytes = kStages * kStageBytes;  // 212992
 constexpr int kSmemBarOffset = kSmemRingBytes;
@@ -96,7 +110,7 @@ struct MainParams {
   const float* xs;        // workspace [32]: 2^-e_m
   void* y;                // [M, N] bf16 or f32
   float* partials;        // workspace [2*grid][32][256]
-  int* counters;          // workspace [row_blocks], zero between calls
+  int* counters;          // workspace [2][row_blocks]: parts published, blocks done; zero between calls
   int* err;               // workspace error word
   float gs;
   int M;
@@ -106,6 +120,7 @@ struct MainParams {
   int64_t N, K;
   int64_t S;      // k-steps = K / 256
   int64_t units;  // row_blocks * S
+  int64_t row_blocks;
 };
 
 // ------------------------------------------------------------------ work split
@@ -121,11 +136,14 @@ struct Abort {
   int* err;            // global error word
 };
 
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Abort& ab) {
+// Bounded wait.  With honor_abort, it returns false at once after another role gave up.
+// Waits that decide when a named-barrier arrival may be made pass honor_abort = false:
+// they keep waiting (still bounded) so that arrivals and the issuers' syncs stay paired.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Abort& ab, bool honor_abort = true) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!ptx::mbar_try_wait(bar, parity)) {
-    if (*ab.flag) return false;
+    if (honor_abort && *ab.flag) return false;
     if (clock64() - t0 > kWaitLimitCycles) {
       *ab.flag = 1;
       atomicOr(ab.err, kErrTimeout);
@@ -144,27 +162,45 @@ __device__ __forceinline__ uint64_t x_desc(uint32_t addr) {
 }
 
 // ------------------------------------------------------------------ activation conversion
-// One block per activation row m < 8 * ceil(M / 8); rows m >= M are written as zeros.
+// One 128-thread block per activation row m < 8 * ceil(M / 8); rows m >= M are written as
+// zeros.  Small on purpose (<= 32 registers per thread): a block fits on an SM beside a block
+// of the main kernel, so converting the next call's activations never displaces one.  Pass 1
+// finds the row's largest magnitude, pass 2 (re-reading through L1) scales, converts, stores.
 // x16 layout: row group g = m / 8 owns bytes [g * 16K, (g + 1) * 16K); inside it, k16 block
 // j at j * 256, k-half h at + h * 128, row m % 8 at + (m % 8) * 16, 8 fp16 per 16 bytes.
-__global__ void __launch_bounds__(256) x_prep_kernel(const uint16_t* __restrict__ x, int M, int64_t K,
-                                                     uint8_t* __restrict__ x16, float* __restrict__ xs) {
+constexpr int kPrepThreads = 128;
+
+__device__ __forceinline__ float bf16x2_absmax(uint32_t w, float a) {
+  a = fmaxf(a, fabsf(__uint_as_float(w << 16)));
+  return fmaxf(a, fabsf(__uint_as_float(w & 0xFFFF0000u)));
+}
+
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, float f1, float f2) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t r[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float lo = __uint_as_float(w[q] << 16) * f1 * f2;
+    const float hi = __uint_as_float(w[q] & 0xFFFF0000u) * f1 * f2;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r[q]) : "f"(hi), "f"(lo));
+  }
+  return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+__global__ void __launch_bounds__(kPrepThreads, 16) x_prep_kernel(const uint16_t* __restrict__ x, int M, int64_t K,
+                                                                  uint8_t* __restrict__ x16, float* __restrict__ xs) {
   ptx::grid_launch_dependents();
   ptx::grid_dependency_wait();  // x is produced upstream; x16 / xs are read by the previous call
   const int m = blockIdx.x;
   const int64_t K8 = K / 8;
   const uint4* xr = reinterpret_cast<const uint4*>(x + (int64_t)m * K);
-  __shared__ float red[8];
+  __shared__ float red[kPrepThreads / 32];
   float amax = 0.f;
   if (m < M) {
-    for (int64_t i = threadIdx.x; i < K8; i += blockDim.x) {
-      const uint4 v = __ldg(xr + i);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        amax = fmaxf(amax, fabsf(__uint_as_float(w[q] << 16)));
-        amax = fmaxf(amax, fabsf(__uint_as_float(w[q] & 0xFFFF0000u)));
-      }
+#pragma unroll 4
+    for (int64_t i = threadIdx.x; i < K8; i += kPrepThreads) {
+      const uint4 w = __ldg(xr + i);
+      amax = bf16x2_absmax(w.x, bf16x2_absmax(w.y, bf16x2_absmax(w.z, bf16x2_absmax(w.w, amax))));
     }
   }
 #pragma unroll
@@ -173,7 +209,7 @@ __global__ void __launch_bounds__(256) x_prep_kernel(const uint16_t* __restrict_
   __syncthreads();
   amax = red[0];
 #pragma unroll
-  for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+  for (int i = 1; i < kPrepThreads / 32; ++i) amax = fmaxf(amax, red[i]);
   // amax = f * 2^E, f in [0.5, 1): e = 16 - E puts amax * 2^e in [2^15, 2^16).
   int e = 0;
   if (amax > 0.f && amax <= 3.4028234663852886e38f) {
@@ -184,21 +220,10 @@ __global__ void __launch_bounds__(256) x_prep_kernel(const uint16_t* __restrict_
   const int e1 = e / 2, e2 = e - e1;
   const float f1 = ldexpf(1.f, e1), f2 = ldexpf(1.f, e2);
   uint8_t* grp = x16 + (int64_t)(m / 8) * 16 * K + (m % 8) * 16;
-  for (int64_t i = threadIdx.x; i < K8; i += blockDim.x) {
-    uint4 o = make_uint4(0u, 0u, 0u, 0u);
-    if (m < M) {
-      const uint4 v = __ldg(xr + i);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      uint32_t r[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float lo = __uint_as_float(w[q] << 16) * f1 * f2;
-        const float hi = __uint_as_float(w[q] & 0xFFFF0000u) * f1 * f2;
-        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r[q]) : "f"(hi), "f"(lo));
-      }
-      o = make_uint4(r[0], r[1], r[2], r[3]);
-    }
-    *reinterpret_cast<uint4*>(grp + (i / 2) * 256 + (i % 2) * 128) = o;
+#pragma unroll 4
+  for (int64_t i = threadIdx.x; i < K8; i += kPrepThreads) {
+    const uint4 w = m < M ? __ldg(xr + i) : make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(grp + (i / 2) * 256 + (i % 2) * 128) = bf16x8_to_f16x8(w, f1, f2);
   }
   if (threadIdx.x == 0) xs[m] = (m < M) ? ldexpf(1.f, -e) : 1.f;
 }
@@ -226,17 +251,11 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(bar(kBarFull + s), 1);
-      ptx::mbar_init(bar(kBarEmpty + s), kDecodeWarps + 1);
+      ptx::mbar_init(bar(kBarEmpty + s), kDecodeWarps + kTiles);
     }
-    for (int a = 0; a < kASlots; ++a) {
-      ptx::mbar_init(bar(kBarAFull + a), kDecodeWarps);
-      ptx::mbar_init(bar(kBarAEmpty + a), 1);
-    }
-    for (int d = 0; d < 2; ++d) {
-      ptx::mbar_init(bar(kBarDFull + d), 1);
-      ptx::mbar_init(bar(kBarDEmpty + d), kEpiWarps);
-    }
-    ptx::mbar_init(bar(kBarFinal), 1);
+    for (int a = 0; a < kASlots * kTiles; ++a) ptx::mbar_init(bar(kBarAEmpty + a), 1);
+    for (int d = 0; d < 2; ++d) ptx::mbar_init(bar(kBarDFull + d), kTiles);
+    for (int t = 0; t < kTiles; ++t) ptx::mbar_init(bar(kBarFinal + t), 1);
     *abort_flag = 0;
     *fix_flag = 0;
     ptx::fence_mbar_init();
@@ -312,26 +331,29 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
     int a_use = 0;
     bool ok = true;
-    for (int i = 0; i < n_local && ok; ++i) {
+    // Every unit and sub-slot is walked even after an abort, so the A-full arrivals always
+    // pair with the issuer's syncs; after an abort the decoded data is simply not stored.
+    for (int i = 0; i < n_local; ++i) {
       const int st = i % kStages, round = i / kStages;
-      ok = wait_bar(bar(kBarFull + st), (uint32_t)(round & 1), ab);
-      if (!ok) break;
+      if (ok) ok = wait_bar(bar(kBarFull + st), (uint32_t)(round & 1), ab);
+      ok = __all_sync(0xffffffffu, ok);
       const uint8_t* stage = smem + st * kStageBytes;
       // 128-byte swizzle: 16-byte chunk q of row r sits at chunk q ^ (r % 8) of the row
       const uint8_t* crow = stage + row_in_block * kCodeRowBytes;
       const int swz = row_in_block & 7;
       uint4 c[8];
+      uint4 sc = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) c[q] = *reinterpret_cast<const uint4*>(crow + ((q ^ swz) << 4));
-      const uint4 sc = *reinterpret_cast<const uint4*>(stage + kCodeStageBytes + row_in_block * kScaleRowBytes);
+      for (int q = 0; q < 8; ++q) c[q] = ok ? *reinterpret_cast<const uint4*>(crow + ((q ^ swz) << 4)) : sc;
+      if (ok) sc = *reinterpret_cast<const uint4*>(stage + kCodeStageBytes + row_in_block * kScaleRowBytes);
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar(kBarEmpty + st));
-      const uint32_t sw[4] = {sc.x, sc.y, sc.z, sc.w};
+      const uint32_t sw4[4] = {sc.x, sc.y, sc.z, sc.w};
 #pragma unroll
       for (int sub = 0; sub < kSubsPerStage; ++sub) {
         // k [64 sub, 64 sub + 64): code words from c[2 sub], c[2 sub + 1]; scale blocks 4 sub .. 4 sub + 3
-        const uint32_t s0 = ptx::e4m3_pair(sw[sub], 0), s1 = ptx::e4m3_pair(sw[sub], 1);
-        const uint32_t s2 = ptx::e4m3_pair(sw[sub], 2), s3 = ptx::e4m3_pair(sw[sub], 3);
+        const uint32_t s0 = ptx::e4m3_pair(sw4[sub], 0), s1 = ptx::e4m3_pair(sw4[sub], 1);
+        const uint32_t s2 = ptx::e4m3_pair(sw4[sub], 2), s3 = ptx::e4m3_pair(sw4[sub], 3);
         const uint4 lo = c[2 * sub], hi = c[2 * sub + 1];
         uint32_t o[32];
         ptx::e2m1x8_scaled(lo.x, s0, o[0], o[1], o[2], o[3]);
@@ -343,65 +365,67 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
         ptx::e2m1x8_scaled(hi.z, s3, o[24], o[25], o[26], o[27]);
         ptx::e2m1x8_scaled(hi.w, s3, o[28], o[29], o[30], o[31]);
         const int slot = a_use % kASlots, around = a_use / kASlots;
-        ok = wait_bar(bar(kBarAEmpty + slot), (uint32_t)((around & 1) ^ 1), ab);
-        if (!ok) break;
-        ptx::tc_fence_after();
-        ptx::tmem_st32(t_lane + kAColBase + (uint32_t)(slot * 64 + tile * 32), o);
-        ptx::tmem_wait_st();
+        // the slot's previous MMAs must have completed before it is overwritten (and before the
+        // next arrival on its named barrier): this wait ignores the abort flag
+        const bool freed = wait_bar(bar(kBarAEmpty + slot * kTiles + tile), (uint32_t)((around & 1) ^ 1), ab, false);
+        if (__all_sync(0xffffffffu, ok && freed)) {
+          ptx::tc_fence_after();
+          ptx::tmem_st32(t_lane + kAColBase + (uint32_t)(slot * 64 + tile * 32), o);
+          ptx::tmem_wait_st();
+        }
         ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar(kBarAFull + slot));
+        ptx::named_bar_arrive(nb_afull(slot, tile), kNbPairThreads);
         ++a_use;
       }
     }
-  } else if (warp == kMmaWarp) {
-    // ================================================================ MMA issuer
-    if (lane == 0) {
-      int a_use = 0, dbuf = 0;
-      int d_use[2] = {0, 0};
-      bool ok = true;
-      for (int i = 0; i < n_local && ok; ++i) {
-        const int64_t u = u_begin + i, s = u % S;
-        const bool seg_start = (i == 0) || (s == 0);
-        const bool seg_end = (i == n_local - 1) || (s == S - 1);
-        const int st = i % kStages, round = i / kStages;
-        if (seg_start) {
-          ok = wait_bar(bar(kBarDEmpty + dbuf), (uint32_t)((d_use[dbuf] & 1) ^ 1), ab);
-          if (!ok) break;
-        }
-        ok = wait_bar(bar(kBarFull + st), (uint32_t)(round & 1), ab);
-        if (!ok) break;
-        const uint32_t xstage = smem_base + (uint32_t)(st * kStageBytes + kXStageOffset);
-        for (int sub = 0; sub < kSubsPerStage && ok; ++sub) {
-          const int slot = a_use % kASlots, around = a_use / kASlots;
-          ok = wait_bar(bar(kBarAFull + slot), (uint32_t)(around & 1), ab);
-          if (!ok) break;
-          ptx::tc_fence_after();
-#pragma unroll
-          for (int t = 0; t < kTiles; ++t) {
-#pragma unroll
-            for (int kk = 0; kk < kK16PerSub; ++kk) {
-              const int j = sub * kK16PerSub + kk;
-              const uint32_t acc = (seg_start && sub == 0 && kk == 0) ? 0u : 1u;
-              ptx::mma_f16_ts(tmem + kDColBase + (uint32_t)(dbuf * 64 + t * 32),
-                              tmem + kAColBase + (uint32_t)(slot * 64 + t * 32 + kk * 8),
-                              x_desc(xstage + (uint32_t)(j * 256)), kIdesc, acc);
-            }
-          }
-          ptx::mma_commit(bar(kBarAEmpty + slot));
-          ++a_use;
-        }
-        if (!ok) break;
-        ptx::mma_commit(bar(kBarEmpty + st));
-        if (seg_end) {
-          ptx::mma_commit(bar(kBarDFull + dbuf));
-          ++d_use[dbuf];
-          dbuf ^= 1;
-        }
+  } else if (warp == kMmaWarp || warp == kMmaWarp1) {
+    // ================================================================ MMA issuers (one per tile)
+    // The whole warp walks the schedule (named barriers are warp-wide); lane 0 issues.  No
+    // shared-memory reads here: A-full and D-free come from named barriers, completions go out
+    // through tcgen05.commit.  The issuer has no abort path: MMAs on stale data are harmless,
+    // and its commits keep every other role's waits completing.
+    const int t = warp == kMmaWarp ? 0 : 1;
+    int a_use = 0, dbuf = 0;
+    int d_use0 = 0, d_use1 = 0;
+    for (int i = 0; i < n_local; ++i) {
+      const int64_t u = u_begin + i, s = u % S;
+      const bool seg_start = (i == 0) || (s == 0);
+      const bool seg_end = (i == n_local - 1) || (s == S - 1);
+      const int st = i % kStages;
+      if (seg_start) {
+        if ((dbuf ? d_use1 : d_use0) > 0) ptx::named_bar_sync(nb_dempty(dbuf, t), kNbPairThreads);
+        ptx::tc_fence_after();
       }
-      // drain every MMA issued before tensor memory is released
-      ptx::mma_commit(bar(kBarFinal));
-      wait_bar(bar(kBarFinal), 0u, ab);
+      const uint32_t xstage = smem_base + (uint32_t)(st * kStageBytes + kXStageOffset);
+      const uint32_t d_tmem = tmem + kDColBase + (uint32_t)(dbuf * 64 + t * 32);
+#pragma unroll
+      for (int sub = 0; sub < kSubsPerStage; ++sub) {
+        const int slot = a_use % kASlots;
+        ptx::named_bar_sync(nb_afull(slot, t), kNbPairThreads);
+        ptx::tc_fence_after();
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < kK16PerSub; ++kk) {
+            const int j = sub * kK16PerSub + kk;
+            const uint32_t acc = (seg_start && sub == 0 && kk == 0) ? 0u : 1u;
+            ptx::mma_f16_ts(d_tmem, tmem + kAColBase + (uint32_t)(slot * 64 + t * 32 + kk * 8),
+                            x_desc(xstage + (uint32_t)(j * 256)), kIdesc, acc);
+          }
+          ptx::mma_commit(bar(kBarAEmpty + slot * kTiles + t));
+        }
+        ++a_use;
+      }
+      if (lane == 0) ptx::mma_commit(bar(kBarEmpty + st));
+      if (seg_end) {
+        if (lane == 0) ptx::mma_commit(bar(kBarDFull + dbuf));
+        if (dbuf) ++d_use1; else ++d_use0;
+        dbuf ^= 1;
+      }
+    }
+    // drain every MMA issued before tensor memory is released
+    if (lane == 0) {
+      ptx::mma_commit(bar(kBarFinal + t));
+      wait_bar(bar(kBarFinal + t), 0u, ab, false);
     }
     __syncwarp();
   } else {
@@ -415,13 +439,20 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
     const float gs = p.gs;
     int dbuf = 0;
     int d_use[2] = {0, 0};
+    int n_seg = 0;
+    for (int i = 0; i < n_local; ++i)
+      if (i == n_local - 1 || (u_begin + i) % S == S - 1) ++n_seg;
+    int seg = 0;
     bool ok = true;
-    for (int i = 0; i < n_local && ok; ++i) {
+    int64_t pend[2] = {0, 0};  // split row blocks of this block's range (its first and last)
+    int n_pend = 0;
+    for (int i = 0; i < n_local; ++i) {
       const int64_t u = u_begin + i, rb = u / S, s = u % S;
       const bool seg_end = (i == n_local - 1) || (s == S - 1);
       if (!seg_end) continue;
-      ok = wait_bar(bar(kBarDFull + dbuf), (uint32_t)(d_use[dbuf] & 1), ab);
-      if (!ok) break;
+      // D must be complete before it is read and before the D-free arrival: ignores the abort flag
+      const bool full = wait_bar(bar(kBarDFull + dbuf), (uint32_t)(d_use[dbuf] & 1), ab, false);
+      ok = ok && full;
       ptx::tc_fence_after();
       uint32_t v0[32], v1[32];
       const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + kDColBase + (uint32_t)(dbuf * 64);
@@ -429,15 +460,21 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
       ptx::tmem_ld32(taddr + 32, v1);
       ptx::tmem_wait_ld();
       ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(kBarDEmpty + dbuf));
+      // the issuers wait for this buffer again only if a later segment of this block uses it
+      if (seg + 2 < n_seg) {
+        ptx::named_bar_arrive(nb_dempty(dbuf, 0), kNbPairThreads);
+        ptx::named_bar_arrive(nb_dempty(dbuf, 1), kNbPairThreads);
+      }
       ++d_use[dbuf];
       dbuf ^= 1;
+      ++seg;
+      ok = __all_sync(0xffffffffu, ok);
 
       const int r0 = quad * 32 + lane, r1 = r0 + kTileRows;  // rows inside the row block
       const int64_t n0 = rb * kRowsPerBlock + r0, n1 = rb * kRowsPerBlock + r1;
       const int64_t pf = block_of_unit(rb * S, T, G), pl = block_of_unit(rb * S + S - 1, T, G);
       if (pf == pl) {
+        if (!ok) continue;
         // the whole K of this row block was summed here
 #pragma unroll
         for (int m = 0; m < kNmma; ++m) {
@@ -456,62 +493,94 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
           }
         }
       } else {
-        // split row block: publish this part, the last part to arrive adds all parts in block order
+        // split row block: publish this part; the sums are formed after the main loop
         const int slot = partial_slot(blockIdx.x, rb, T, G, S);
         float* part = p.partials + (int64_t)slot * (kNmma * kRowsPerBlock);
 #pragma unroll
         for (int m = 0; m < kNmma; ++m) {
-          if (m < M) {
+          if (ok && m < M) {
             part[m * kRowsPerBlock + r0] = __uint_as_float(v0[m]) * xs_smem[m];
             part[m * kRowsPerBlock + r1] = __uint_as_float(v1[m]) * xs_smem[m];
           }
         }
         __threadfence();
-        ptx::named_bar_sync(1, kEpiWarps * 32);
-        if (etid == 0) {
-          const int old = atomicAdd(p.counters + rb, 1);
-          *fix_flag = (old == (int)(pl - pf)) ? 1 : 0;
-        }
-        ptx::named_bar_sync(1, kEpiWarps * 32);
-        if (*fix_flag) {
-          __threadfence();
-          // parts in block order; each part's values load independently, then add in order
-          float a0[kNmma], a1[kNmma];
-#pragma unroll
-          for (int m = 0; m < kNmma; ++m) a0[m] = a1[m] = 0.f;
-          for (int64_t q = pf; q <= pl; ++q) {
-            const float* pp = p.partials + (int64_t)partial_slot(q, rb, T, G, S) * (kNmma * kRowsPerBlock);
-            float t0[kNmma], t1[kNmma];
-#pragma unroll
-            for (int m = 0; m < kNmma; ++m) {
-              t0[m] = m < M ? __ldcg(pp + m * kRowsPerBlock + r0) : 0.f;
-              t1[m] = m < M ? __ldcg(pp + m * kRowsPerBlock + r1) : 0.f;
-            }
-#pragma unroll
-            for (int m = 0; m < kNmma; ++m) {
-              a0[m] += t0[m];
-              a1[m] += t1[m];
-            }
+        ptx::named_bar_sync(kNbEpi, kEpiWarps * 32);
+        if (etid == 0 && ok) atomicAdd(p.counters + rb, 1);  // release: every thread fenced its stores
+        if (n_pend < 2) pend[n_pend++] = rb;
+      }
+    }
+    // Split row blocks: wait until every contributing block has published its part, then add
+    // this block's slice of the rows (part q of the block order is always added q-th).  Every
+    // block publishes all of its parts before it waits here, so the waits end.
+    for (int k = 0; k < n_pend; ++k) {
+      const int64_t rb = pend[k];
+      const int64_t pf = block_of_unit(rb * S, T, G), pl = block_of_unit(rb * S + S - 1, T, G);
+      const int nseg = (int)(pl - pf + 1);
+      if (etid == 0) {
+        bool arrived = ptx::ld_acquire_gpu(p.counters + rb) >= nseg;
+        const long long t0 = clock64();
+        while (!arrived && !*abort_flag) {
+          __nanosleep(64);
+          arrived = ptx::ld_acquire_gpu(p.counters + rb) >= nseg;
+          if (!arrived && clock64() - t0 > kWaitLimitCycles) {
+            *abort_flag = 1;
+            atomicOr(p.err, kErrTimeout);
           }
+        }
+        *fix_flag = arrived ? 1 : 0;
+      }
+      ptx::named_bar_sync(kNbEpi, kEpiWarps * 32);
+      if (*fix_flag) {
+        __threadfence();
+        const int q = (int)(blockIdx.x - pf);
+        // this block's slice: whole groups of 4 rows (the 64 groups of the row block split over nseg)
+        const int g_lo = q * (kRowsPerBlock / 4) / nseg, g_hi = (q + 1) * (kRowsPerBlock / 4) / nseg;
+        const int groups = g_hi - g_lo;
+        for (int o = etid; o < groups * M; o += kEpiWarps * 32) {
+          const int r = 4 * (g_lo + o % groups), m = o / groups;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          // up to 8 parts in flight at once, added strictly in block order
+          for (int64_t q0 = pf; q0 <= pl; q0 += 8) {
+            float4 t[8];
 #pragma unroll
-          for (int m = 0; m < kNmma; ++m) {
-            if (m < M) {
-              const float s0 = a0[m] * gs, s1 = a1[m] * gs;
-              if (p.out_f32) {
-                float* y = static_cast<float*>(p.y) + (int64_t)m * p.N;
-                if (n0 < p.N) y[n0] = s0;
-                if (n1 < p.N) y[n1] = s1;
-              } else {
-                uint16_t* y = static_cast<uint16_t*>(p.y) + (int64_t)m * p.N;
-                if (n0 < p.N) y[n0] = ptx::f32_to_bf16_rn(s0);
-                if (n1 < p.N) y[n1] = ptx::f32_to_bf16_rn(s1);
+            for (int j = 0; j < 8; ++j)
+              if (q0 + j <= pl)
+                t[j] = __ldcg(reinterpret_cast<const float4*>(
+                    p.partials + (int64_t)partial_slot(q0 + j, rb, T, G, S) * (kNmma * kRowsPerBlock) +
+                    m * kRowsPerBlock + r));
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              if (q0 + j <= pl) {
+                acc.x += t[j].x;
+                acc.y += t[j].y;
+                acc.z += t[j].z;
+                acc.w += t[j].w;
               }
             }
           }
-          if (etid == 0) p.counters[rb] = 0;
+          const float v[4] = {acc.x * gs, acc.y * gs, acc.z * gs, acc.w * gs};
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int64_t n = rb * kRowsPerBlock + r + c;
+            if (n < p.N) {
+              if (p.out_f32)
+                static_cast<float*>(p.y)[(int64_t)m * p.N + n] = v[c];
+              else
+                static_cast<uint16_t*>(p.y)[(int64_t)m * p.N + n] = ptx::f32_to_bf16_rn(v[c]);
+            }
+          }
         }
-        ptx::named_bar_sync(1, kEpiWarps * 32);
       }
+      ptx::named_bar_sync(kNbEpi, kEpiWarps * 32);
+      // the last block to finish this row block clears its counters for the next call
+      if (etid == 0 && *fix_flag) {
+        const int done = atomicAdd(p.counters + p.row_blocks + rb, 1);
+        if (done == nseg - 1) {
+          p.counters[rb] = 0;
+          p.counters[p.row_blocks + rb] = 0;
+        }
+      }
+      ptx::named_bar_sync(kNbEpi, kEpiWarps * 32);
     }
   }
 
