@@ -48,12 +48,12 @@ constexpr int kTileRows = 128;                        // MMA M
 constexpr int kTiles = 2;                             // MMA tiles per row block
 constexpr int kRowsPerBlock = kTileRows * kTiles;     // 256
 constexpr int kKStep = 256;                           // k per unit and per ring stage
-constexpr int kSubK = 64;                             // k per tensor-memory A slot
-constexpr int kSubsPerStage = kKStep / kSubK;         // 4
-constexpr int kK16PerSub = kSubK / 16;                // 4
+constexpr int kSubK = 128;                            // k per tensor-memory A slot (8 MMAs per hand-off)
+constexpr int kSubsPerStage = kKStep / kSubK;         // 2
+constexpr int kK16PerSub = kSubK / 16;                // 8
 constexpr int kNmma = 32;                             // activation rows per MMA (MMA N)
 constexpr int kStages = 4;                            // shared-memory ring depth
-constexpr int kASlots = 4;                            // tensor-memory A ring depth
+constexpr int kASlots = 3;                            // tensor-memory A ring depth (1.5 stages)
 constexpr int kCodeRowBytes = kKStep / 2;             // 128 bytes of E2M1 codes per row per stage
 constexpr int kScaleRowBytes = kKStep / 16;           // 16 E4M3 scales per row per stage
 constexpr int kXGroupBytes = 8 * kKStep * 2;          // 8 activation rows x 256 k x fp16 = 4 KB
@@ -73,8 +73,10 @@ constexpr int kWarps = 15;
 constexpr int kThreads = kWarps * 32;  // 480
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAColBase = 0;    // A slot a, tile t: columns a*64 + t*32 .. +32
-constexpr uint32_t kDColBase = 256;  // D buffer d, tile t: columns 256 + d*64 + t*32 .. +32
+constexpr uint32_t kASlotCols = kSubK / 2 * kTiles;  // 128: 2 fp16 per 32-bit column, both tiles
+constexpr uint32_t kAColBase = 0;    // A slot a, tile t: columns a*128 + t*64 .. +64
+constexpr uint32_t kDColBase = kASlots * kASlotCols;  // 384; D buffer d, tile t: 384 + d*64 + t*32 .. +32
+static_assert(kDColBase + 2 * kTiles * kNmma <= kTmemCols, "tensor memory budget");
 
 // mbarrier indices in the barrier array
 constexpr int kBarFull = 0;                               // [kStages]  producer -> consumers (tx)
@@ -87,7 +89,8 @@ constexpr int kNumBars = kBarFinal + kTiles;
 // hardware named barriers (0 is __syncthreads)
 constexpr uint32_t kNbEpi = 1;  // the 4 epilogue warps
 __device__ __forceinline__ uint32_t nb_afull(int slot, int tile) { return 2u + (uint32_t)(slot * kTiles + tile); }
-__device__ __forceinline__ uint32_t nb_dempty(int dbuf, int tile) { return 10u + (uint32_t)(dbuf * kTiles + tile); }
+__device__ __forceinline__ uint32_t nb_dempty(int dbuf, int tile) { return 2u + kASlots * kTiles + (uint32_t)(dbuf * kTiles + tile); }
+static_assert(2 + kASlots * kTiles + 2 * kTiles <= 16, "hardware named barriers");
 constexpr uint32_t kNbPairThreads = 4 * 32 + 32;  // 4 decoder (or epilogue) warps + 1 issuer warp
 
 constexpr int kSmemRingBytes = kStages * kStageBytes;  // 212992
@@ -351,28 +354,31 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
       const uint32_t sw4[4] = {sc.x, sc.y, sc.z, sc.w};
 #pragma unroll
       for (int sub = 0; sub < kSubsPerStage; ++sub) {
-        // k [64 sub, 64 sub + 64): code words from c[2 sub], c[2 sub + 1]; scale blocks 4 sub .. 4 sub + 3
-        const uint32_t s0 = ptx::e4m3_pair(sw4[sub], 0), s1 = ptx::e4m3_pair(sw4[sub], 1);
-        const uint32_t s2 = ptx::e4m3_pair(sw4[sub], 2), s3 = ptx::e4m3_pair(sw4[sub], 3);
-        const uint4 lo = c[2 * sub], hi = c[2 * sub + 1];
-        uint32_t o[32];
-        ptx::e2m1x8_scaled(lo.x, s0, o[0], o[1], o[2], o[3]);
-        ptx::e2m1x8_scaled(lo.y, s0, o[4], o[5], o[6], o[7]);
-        ptx::e2m1x8_scaled(lo.z, s1, o[8], o[9], o[10], o[11]);
-        ptx::e2m1x8_scaled(lo.w, s1, o[12], o[13], o[14], o[15]);
-        ptx::e2m1x8_scaled(hi.x, s2, o[16], o[17], o[18], o[19]);
-        ptx::e2m1x8_scaled(hi.y, s2, o[20], o[21], o[22], o[23]);
-        ptx::e2m1x8_scaled(hi.z, s3, o[24], o[25], o[26], o[27]);
-        ptx::e2m1x8_scaled(hi.w, s3, o[28], o[29], o[30], o[31]);
         const int slot = a_use % kASlots, around = a_use / kASlots;
         // the slot's previous MMAs must have completed before it is overwritten (and before the
         // next arrival on its named barrier): this wait ignores the abort flag
         const bool freed = wait_bar(bar(kBarAEmpty + slot * kTiles + tile), (uint32_t)((around & 1) ^ 1), ab, false);
-        if (__all_sync(0xffffffffu, ok && freed)) {
-          ptx::tc_fence_after();
-          ptx::tmem_st32(t_lane + kAColBase + (uint32_t)(slot * 64 + tile * 32), o);
-          ptx::tmem_wait_st();
+        const bool store = __all_sync(0xffffffffu, ok && freed);
+        if (store) ptx::tc_fence_after();
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          // k [128 sub + 64 hh, +64): code words c[4 sub + 2 hh], c[4 sub + 2 hh + 1]; 4 scale blocks
+          const uint32_t sw = sw4[2 * sub + hh];
+          const uint32_t s0 = ptx::e4m3_pair(sw, 0), s1 = ptx::e4m3_pair(sw, 1);
+          const uint32_t s2 = ptx::e4m3_pair(sw, 2), s3 = ptx::e4m3_pair(sw, 3);
+          const uint4 lo = c[4 * sub + 2 * hh], hi = c[4 * sub + 2 * hh + 1];
+          uint32_t o[32];
+          ptx::e2m1x8_scaled(lo.x, s0, o[0], o[1], o[2], o[3]);
+          ptx::e2m1x8_scaled(lo.y, s0, o[4], o[5], o[6], o[7]);
+          ptx::e2m1x8_scaled(lo.z, s1, o[8], o[9], o[10], o[11]);
+          ptx::e2m1x8_scaled(lo.w, s1, o[12], o[13], o[14], o[15]);
+          ptx::e2m1x8_scaled(hi.x, s2, o[16], o[17], o[18], o[19]);
+          ptx::e2m1x8_scaled(hi.y, s2, o[20], o[21], o[22], o[23]);
+          ptx::e2m1x8_scaled(hi.z, s3, o[24], o[25], o[26], o[27]);
+          ptx::e2m1x8_scaled(hi.w, s3, o[28], o[29], o[30], o[31]);
+          if (store) ptx::tmem_st32(t_lane + kAColBase + (uint32_t)(slot * kASlotCols + tile * 64 + hh * 32), o);
         }
+        if (store) ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::named_bar_arrive(nb_afull(slot, tile), kNbPairThreads);
         ++a_use;
@@ -408,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
           for (int kk = 0; kk < kK16PerSub; ++kk) {
             const int j = sub * kK16PerSub + kk;
             const uint32_t acc = (seg_start && sub == 0 && kk == 0) ? 0u : 1u;
-            ptx::mma_f16_ts(d_tmem, tmem + kAColBase + (uint32_t)(slot * 64 + t * 32 + kk * 8),
+            ptx::mma_f16_ts(d_tmem, tmem + kAColBase + (uint32_t)(slot * kASlotCols + t * 64 + kk * 8),
                             x_desc(xstage + (uint32_t)(j * 256)), kIdesc, acc);
           }
           ptx::mma_commit(bar(kBarAEmpty + slot * kTiles + t));
