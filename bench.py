@@ -242,8 +242,8 @@ def run_ours(args, rank, world):
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "algorithmic_bytes_per_launch": int(avg_bytes), "peak_source": peak_src,
-                "timing": "CUDA events on the launching stream over the timed region; a call = x_prep + "
-                          "skinny_kernel (PDL-overlapped), so this bounds the main kernel from below"}
+                "timing": "CUDA events on the launching stream over the timed region; a call is one "
+                          "skinny_kernel launch (back-to-back launches overlap through PDL)"}
 
     # ---------------- e2e through the public call: pinned host x in, host y out, every call
     e2e = run_e2e(args, proj, x_all, stream, world)

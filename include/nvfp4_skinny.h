@@ -31,11 +31,15 @@
  *
  * Ownership and concurrency
  *   The caller owns x, the weight buffers and y.  A plan owns host state and
- *   one device workspace (converted activations, split-K partials, counters,
- *   an error word), allocated by nvfp4_plan_create* on the device that is
+ *   one device workspace (split-K partials, counters, an error word),
+ *   allocated by nvfp4_plan_create* on the device that is
  *   current then; all later calls on the plan must run on that device.
  *   nvfp4_skinny_linear never allocates, never synchronizes and only
- *   enqueues kernels on `stream`, so it can be captured in a CUDA graph.
+ *   enqueues one kernel on `stream`, so it can be captured in a CUDA graph.
+ *   The kernel is launched with programmatic dependent launch: it starts
+ *   reading the weights before the previous kernel on the stream has
+ *   finished (x, y and the workspace are touched only after it has), so
+ *   the weights must not be written by a kernel still running on `stream`.
  *   Calls that share a plan must not run concurrently (the workspace is
  *   reused); calls on one stream are ordered and safe.
  *
@@ -47,12 +51,14 @@
  *   skips the remaining work and exits; nvfp4_plan_check reports it.
  *
  * Numerics
- *   Activations are converted once per call to fp16 after multiplying each
- *   row by a power of two chosen from that row's largest magnitude (exact for
- *   every element within 2^-32 of the row maximum); weights are decoded to
- *   fp16 (E2M1 x E4M3 is exact in fp16); products accumulate in fp32 on the
- *   tensor cores; the power of two and w_global_scale are applied to the fp32
- *   sum, which is then rounded to nearest-even bfloat16 (or returned as fp32).
+ *   For every 256-wide k-step, each activation row is converted to fp16 after
+ *   multiplying it by a power of two chosen from its largest magnitude in
+ *   that k-step (exact for every element within 2^-33 of that maximum);
+ *   weights are decoded to fp16 (E2M1 x E4M3 is exact in fp16); products
+ *   accumulate in fp32 on the tensor cores; each k-step's fp32 sum is
+ *   multiplied back by the inverse power of two (exact) and added in a fixed
+ *   order; w_global_scale multiplies the total, which is then rounded to
+ *   nearest-even bfloat16 (or returned as fp32).
  */
 #ifndef NVFP4_SKINNY_H
 #define NVFP4_SKINNY_H
@@ -141,8 +147,8 @@ nvfp4_status nvfp4_plan_get_info(nvfp4_plan_t plan, nvfp4_plan_info* info);
  * allocates its workspace in nvfp4_plan_create*, so this entry point takes the shape directly.
  *
  * It computes the same y = x . dequant(W)^T with the same kernels, work split and numerics as
- * nvfp4_skinny_linear, but its scratch (converted activations, split-K parts, split-K
- * counters, an error word) lives in one fixed, statically sized device array inside the
+ * nvfp4_skinny_linear, but its scratch (split-K parts, split-K counters, an error word) lives
+ * in one fixed, statically sized device array inside the
  * library.  Every GPU that loads the library holds that array, NVFP4_NOALLOC_SCRATCH_BYTES
  * bytes, until the process exits.  Limits: K <= NVFP4_NOALLOC_MAX_K and
  * N <= NVFP4_NOALLOC_MAX_N; larger problems are refused with NVFP4_ERR_SCRATCH_LIMIT before
@@ -160,7 +166,7 @@ nvfp4_status nvfp4_plan_get_info(nvfp4_plan_t plan, nvfp4_plan_info* info);
  * ------------------------------------------------------------------------------------------- */
 #define NVFP4_NOALLOC_MAX_K 32768
 #define NVFP4_NOALLOC_MAX_N 4194304
-#define NVFP4_NOALLOC_SCRATCH_BYTES 12714496 /* about 12.1 MiB */
+#define NVFP4_NOALLOC_SCRATCH_BYTES 10617088 /* about 10.1 MiB */
 
 nvfp4_status nvfp4_skinny_linear_noalloc(int64_t N, int64_t K, nvfp4_out_dtype out_dtype, const void* x, int M,
                                          const uint8_t* w_codes, const uint8_t* w_block_scales, float w_global_scale,

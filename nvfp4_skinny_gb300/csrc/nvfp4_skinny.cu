@@ -1,7 +1,7 @@
 // C ABI of the skinny NVFP4 projection (declared and documented in include/nvfp4_skinny.h).
 // Host side: plan creation (work split from (N, K) and the SM count only), argument checks
-// before anything is enqueued, and the two launches of a call, both with programmatic
-// dependent launch so a kernel's weight prefetch can overlap the previous kernel's tail.
+// before anything is enqueued, and the one launch of a call, with programmatic dependent
+// launch so that a call's weight stream starts while the previous call's kernel finishes.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -19,8 +19,6 @@ namespace {
 constexpr int kAbiVersion = 1;
 
 struct Workspace {
-  uint8_t* x16 = nullptr;    // 32 rows x K fp16, operand layout
-  float* xs = nullptr;       // [32]
   float* partials = nullptr; // [2 * grid][32][256]
   int* counters = nullptr;   // [2][row_blocks]
   int* err = nullptr;        // [1]
@@ -95,55 +93,57 @@ bool prepare_tensor_maps(nvfp4_plan* plan, const uint8_t* codes, const uint8_t* 
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-nvfp4_status launch_call(nvfp4_plan* plan, const void* x, int M, const uint8_t* codes, const uint8_t* scales,
-                         float gs, void* y, cudaStream_t stream) {
-  const int m_groups = (M + 7) / 8;
-  if (!prepare_tensor_maps(plan, codes, scales)) return NVFP4_ERR_CUDA;  // before anything is enqueued
+cudaError_t set_smem_limits() {
+  cudaError_t e = cudaFuncSetAttribute(nvfp4::skinny_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       nvfp4::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(nvfp4::skinny_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              nvfp4::kSmemBytes);
+}
+
+// The one launch of a call (shared by the plan and allocation-free entry points).
+nvfp4_status launch_main(const CUtensorMap& tm_codes, const CUtensorMap& tm_scales, const void* x, int M, float gs,
+                         void* y, float* partials, int* counters, int* err, int out_f32, int grid, int64_t N,
+                         int64_t K, int64_t row_blocks, cudaStream_t stream) {
+  nvfp4::MainParams p;
+  p.tm_codes = tm_codes;
+  p.tm_scales = tm_scales;
+  p.x = static_cast<const uint16_t*>(x);
+  p.y = y;
+  p.partials = partials;
+  p.counters = counters;
+  p.err = err;
+  p.gs = gs;
+  p.M = M;
+  p.out_f32 = out_f32;
+  p.grid = grid;
+  p.N = N;
+  p.K = K;
+  p.S = K / nvfp4::kKStep;
+  p.units = row_blocks * p.S;
+  p.row_blocks = row_blocks;
+
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-
-  cudaLaunchConfig_t cfg_prep = {};
-  cfg_prep.gridDim = dim3((unsigned)(m_groups * 8));
-  cfg_prep.blockDim = dim3(nvfp4::kPrepThreads);
-  cfg_prep.dynamicSmemBytes = 0;
-  cfg_prep.stream = stream;
-  cfg_prep.attrs = attr;
-  cfg_prep.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg_prep, nvfp4::x_prep_kernel, static_cast<const uint16_t*>(x), M, plan->K,
-                                     plan->ws.x16, plan->ws.xs);
-  if (e != cudaSuccess) return NVFP4_ERR_CUDA;
-
-  nvfp4::MainParams p;
-  p.tm_codes = plan->tm_codes;
-  p.tm_scales = plan->tm_scales;
-  p.x16 = plan->ws.x16;
-  p.xs = plan->ws.xs;
-  p.y = y;
-  p.partials = plan->ws.partials;
-  p.counters = plan->ws.counters;
-  p.err = plan->ws.err;
-  p.gs = gs;
-  p.M = M;
-  p.m_groups = m_groups;
-  p.out_f32 = plan->out == NVFP4_OUT_F32 ? 1 : 0;
-  p.grid = plan->grid;
-  p.N = plan->N;
-  p.K = plan->K;
-  p.S = plan->k_steps;
-  p.units = plan->units;
-  p.row_blocks = plan->row_blocks;
-
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)plan->grid);
+  cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(nvfp4::kThreads);
   cfg.dynamicSmemBytes = nvfp4::kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, nvfp4::skinny_kernel, p);
-  if (e != cudaSuccess) return NVFP4_ERR_CUDA;
-  return NVFP4_OK;
+  const cudaError_t e = M <= 16 ? cudaLaunchKernelEx(&cfg, nvfp4::skinny_kernel<16>, p)
+                                : cudaLaunchKernelEx(&cfg, nvfp4::skinny_kernel<32>, p);
+  return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+nvfp4_status launch_call(nvfp4_plan* plan, const void* x, int M, const uint8_t* codes, const uint8_t* scales,
+                         float gs, void* y, cudaStream_t stream) {
+  if (!prepare_tensor_maps(plan, codes, scales)) return NVFP4_ERR_CUDA;  // before anything is enqueued
+  return launch_main(plan->tm_codes, plan->tm_scales, x, M, gs, y, plan->ws.partials, plan->ws.counters,
+                     plan->ws.err, plan->out == NVFP4_OUT_F32 ? 1 : 0, plan->grid, plan->N, plan->K,
+                     plan->row_blocks, stream);
 }
 
 }  // namespace
@@ -182,8 +182,7 @@ nvfp4_status nvfp4_plan_create_ex(int64_t N, int64_t K, nvfp4_out_dtype out_dtyp
     return NVFP4_ERR_CUDA;
   static bool smem_attr_set[64] = {false};
   if (dev < 64 && !smem_attr_set[dev]) {
-    if (cudaFuncSetAttribute(nvfp4::skinny_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             nvfp4::kSmemBytes) != cudaSuccess)
+    if (set_smem_limits() != cudaSuccess)
       return NVFP4_ERR_CUDA;
     smem_attr_set[dev] = true;
   }
@@ -200,12 +199,10 @@ nvfp4_status nvfp4_plan_create_ex(int64_t N, int64_t K, nvfp4_out_dtype out_dtyp
   plan->units = plan->row_blocks * plan->k_steps;
   plan->grid = (int)(plan->units < sms ? plan->units : sms);
 
-  const size_t x16_bytes = round_up((size_t)32 * (size_t)K * 2, 256);
-  const size_t xs_bytes = 256;
   const size_t part_bytes = round_up((size_t)2 * plan->grid * nvfp4::kNmma * nvfp4::kRowsPerBlock * 4, 256);
   const size_t cnt_bytes = round_up((size_t)plan->row_blocks * 2 * 4, 256);
   const size_t err_bytes = 256;
-  const size_t total = x16_bytes + xs_bytes + part_bytes + cnt_bytes + err_bytes;
+  const size_t total = part_bytes + cnt_bytes + err_bytes;
   void* base = nullptr;
   if (cudaMalloc(&base, total) != cudaSuccess) {
     delete plan;
@@ -214,11 +211,9 @@ nvfp4_status nvfp4_plan_create_ex(int64_t N, int64_t K, nvfp4_out_dtype out_dtyp
   uint8_t* b = static_cast<uint8_t*>(base);
   plan->ws.base = base;
   plan->ws.bytes = total;
-  plan->ws.x16 = b;
-  plan->ws.xs = reinterpret_cast<float*>(b + x16_bytes);
-  plan->ws.partials = reinterpret_cast<float*>(b + x16_bytes + xs_bytes);
-  plan->ws.counters = reinterpret_cast<int*>(b + x16_bytes + xs_bytes + part_bytes);
-  plan->ws.err = reinterpret_cast<int*>(b + x16_bytes + xs_bytes + part_bytes + cnt_bytes);
+  plan->ws.partials = reinterpret_cast<float*>(b);
+  plan->ws.counters = reinterpret_cast<int*>(b + part_bytes);
+  plan->ws.err = reinterpret_cast<int*>(b + part_bytes + cnt_bytes);
   if (cudaMemset(base, 0, total) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     cudaFree(base);
     delete plan;
@@ -294,20 +289,18 @@ nvfp4_status nvfp4_plan_get_info(nvfp4_plan_t plan, nvfp4_plan_info* info) {
 
 // ------------------------------------------------------------------------------------------------
 // Allocation-free entry point (declared in include/nvfp4_skinny.h).  Its scratch is one fixed
-// device array in this file, laid out exactly like a plan's workspace for the largest problem
-// it accepts: activations (32 x K fp16), 2^-e factors, error word, split-K counters, parts.
+// device array in this file, laid out like a plan's workspace for the largest problem it
+// accepts: error word, split-K counters, parts.
 namespace {
 
 constexpr int64_t kNaMaxK = NVFP4_NOALLOC_MAX_K;
 constexpr int64_t kNaMaxN = NVFP4_NOALLOC_MAX_N;
 constexpr int64_t kNaMaxRowBlocks = kNaMaxN / nvfp4::kRowsPerBlock;
 constexpr int kNaMaxGrid = 160;  // at most this many blocks (GB300 has 152 SMs)
-constexpr size_t kNaX16Bytes = (size_t)32 * kNaMaxK * 2;
-constexpr size_t kNaXsBytes = 256;
 constexpr size_t kNaErrBytes = 256;
 constexpr size_t kNaCounterBytes = (size_t)kNaMaxRowBlocks * 2 * 4;
 constexpr size_t kNaPartBytes = (size_t)2 * kNaMaxGrid * nvfp4::kNmma * nvfp4::kRowsPerBlock * 4;
-constexpr size_t kNaScratchBytes = kNaX16Bytes + kNaXsBytes + kNaErrBytes + kNaCounterBytes + kNaPartBytes;
+constexpr size_t kNaScratchBytes = kNaErrBytes + kNaCounterBytes + kNaPartBytes;
 static_assert(kNaScratchBytes == NVFP4_NOALLOC_SCRATCH_BYTES, "header states the scratch size");
 
 struct NoAllocDevice {
@@ -340,8 +333,7 @@ nvfp4_status noalloc_device(NoAllocDevice** out) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
       return NVFP4_ERR_CUDA;
-    if (cudaFuncSetAttribute(nvfp4::skinny_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             nvfp4::kSmemBytes) != cudaSuccess)
+    if (set_smem_limits() != cudaSuccess)
       return NVFP4_ERR_CUDA;
     d.scratch = static_cast<uint8_t*>(ptr);
     d.sms = sms;
@@ -374,11 +366,9 @@ extern "C" nvfp4_status nvfp4_skinny_linear_noalloc(int64_t N, int64_t K, nvfp4_
   if (grid > kNaMaxGrid) grid = kNaMaxGrid;
 
   uint8_t* base = d->scratch;
-  uint8_t* x16 = base;
-  float* xs = reinterpret_cast<float*>(base + kNaX16Bytes);
-  int* err = reinterpret_cast<int*>(base + kNaX16Bytes + kNaXsBytes);
-  int* counters = reinterpret_cast<int*>(base + kNaX16Bytes + kNaXsBytes + kNaErrBytes);
-  float* parts = reinterpret_cast<float*>(base + kNaX16Bytes + kNaXsBytes + kNaErrBytes + kNaCounterBytes);
+  int* err = reinterpret_cast<int*>(base);
+  int* counters = reinterpret_cast<int*>(base + kNaErrBytes);
+  float* parts = reinterpret_cast<float*>(base + kNaErrBytes + kNaCounterBytes);
 
   CUtensorMap tm_codes, tm_scales;
   if (!encode_u8_2d(&tm_codes, w_codes, (uint64_t)K / 2, (uint64_t)N, nvfp4::kCodeRowBytes, nvfp4::kRowsPerBlock,
@@ -393,46 +383,6 @@ extern "C" nvfp4_status nvfp4_skinny_linear_noalloc(int64_t N, int64_t K, nvfp4_
       cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess)
     return NVFP4_ERR_CUDA;
 
-  const int m_groups = (M + 7) / 8;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg_prep = {};
-  cfg_prep.gridDim = dim3((unsigned)(m_groups * 8));
-  cfg_prep.blockDim = dim3(nvfp4::kPrepThreads);
-  cfg_prep.stream = s;
-  cfg_prep.attrs = attr;
-  cfg_prep.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg_prep, nvfp4::x_prep_kernel, static_cast<const uint16_t*>(x), M, K, x16, xs) !=
-      cudaSuccess)
-    return NVFP4_ERR_CUDA;
-
-  nvfp4::MainParams p;
-  p.tm_codes = tm_codes;
-  p.tm_scales = tm_scales;
-  p.x16 = x16;
-  p.xs = xs;
-  p.y = y;
-  p.partials = parts;
-  p.counters = counters;
-  p.err = err;
-  p.gs = w_global_scale;
-  p.M = M;
-  p.m_groups = m_groups;
-  p.out_f32 = out_dtype == NVFP4_OUT_F32 ? 1 : 0;
-  p.grid = (int)grid;
-  p.N = N;
-  p.K = K;
-  p.S = k_steps;
-  p.units = units;
-  p.row_blocks = row_blocks;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(nvfp4::kThreads);
-  cfg.dynamicSmemBytes = nvfp4::kSmemBytes;
-  cfg.stream = s;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, nvfp4::skinny_kernel, p) != cudaSuccess) return NVFP4_ERR_CUDA;
-  return NVFP4_OK;
+  return launch_main(tm_codes, tm_scales, x, M, w_global_scale, y, parts, counters, err,
+                     out_dtype == NVFP4_OUT_F32 ? 1 : 0, (int)grid, N, K, row_blocks, s);
 }

@@ -1,38 +1,35 @@
-// Device kernels of the skinny NVFP4 projection y = x . dequant(W)^T on sm_103a.
+// Device kernel of the skinny NVFP4 projection y = x . dequant(W)^T on sm_103a.
 //
-//   x_prep_kernel   bf16 x [M, K] -> fp16 x16 in the tensor-core operand layout, each row
-//                   multiplied by a power of two 2^e_m chosen from that row's largest
-//                   magnitude (so the conversion is exact for every element within 2^-32
-//                   of it), plus xs[m] = 2^-e_m.
-//   skinny_kernel   persistent, one block per SM, warp-specialised:
-//                     warp 8       producer: 2-D tensor copies (TMA) of a 256-row x 256-k
-//                                  block of codes (128-byte swizzle) and of its block
-//                                  scales, and bulk copies of x16, into a shared-memory ring;
-//                     warps 0-7    decoders: one weight row per thread; E2M1 x E4M3 -> fp16
-//                                  with the hardware converters (exact), written to tensor
-//                                  memory as the MMA's A operand;
-//                     warps 9, 14  one thread each issues tcgen05.mma (M=128, N=32, K=16,
-//                                  fp32 accumulation in tensor memory) for one of the two
-//                                  128-row tiles (an issuing thread sustains one such MMA
-//                                  per ~44 cycles; two issuers halve that per tile pair).
-//                                  An issuer never reads shared memory: any such read waits
-//                                  for its MMAs in flight, so it learns that an A slot is
-//                                  full, or a D buffer free, from hardware named barriers
-//                                  and reports completions with tcgen05.commit;
-//                     warps 10-13  epilogue: tensor memory -> registers, times 2^-e_m and
-//                                  the per-tensor scale, rounded to bf16 (or fp32) and
-//                                  stored.  A row block split over several blocks: each
-//                                  part goes to the workspace during the main loop; at the
-//                                  end of its range every contributing block waits for all
-//                                  parts, then adds its own slice of the rows, parts in
-//                                  block order (the same order whoever arrives last).
+// One persistent, warp-specialised kernel per call, one block per SM, 16 warps (4 per SM
+// sub-partition, so each thread may hold 128 registers):
+//   warps 0-7    decoders: one weight row per thread; E2M1 x E4M3 -> fp16 with the hardware
+//                converters (exact: at most 6 significant bits), written to tensor memory as the
+//                MMA's A operand, one k-half (128 k) of a unit at a time.  The weights arrive by
+//                2-D tensor copies (TMA) of a 256-row x 256-k block of codes (128-byte swizzle)
+//                and of its block scales into a 4-stage shared-memory ring; the last decoder
+//                warp to take a stage's bytes into registers issues the stage's next copy;
+//   warps 8-11   activations and epilogue: bulk copies of the unit's bf16 activation rows,
+//                conversion to fp16 times 2^e with e chosen per (row, unit) from the largest
+//                magnitude (exact for every element within 2^-33 of it), and after each unit:
+//                tensor memory -> registers, the unit's sums times 2^-e added to an fp32
+//                accumulator.  At the end of a row block's k-range: times the per-tensor
+//                scale, rounded and stored; a row block split over several blocks is
+//                published and reduced at the end of the block's range;
+//   warps 12-15  MMA issuers, one per (128-row tile, k-half): tcgen05.mma M=128, N=32, K=16,
+//                fp32 accumulation in tensor memory, 8 per unit each.  Four issuers keep the
+//                tensor core fed at N=32 (one issuing thread sustains about one such MMA per
+//                44 cycles, four reach one per ~16 SM-wide).  An issuer never reads shared
+//                memory (a read waits for its MMAs in flight): it learns that operands are
+//                ready from hardware named barriers and reports completions through
+//                tcgen05.commit.
 //
 // Work split ("10 Kernels" 10.1 Row invariance): a unit is (row block of 256 weight rows,
-// k-step of 256).  The units, row-block-major, are split into `grid` contiguous, equal
-// ranges; grid = min(units, SMs).  Which block computes which part of a row's sum, the
-// order of the k16 MMAs inside a part, and the order in which parts are added all depend
-// on (N, K, grid) only.  Activation row m is column m of every MMA, and nothing a column
-// computes depends on another column, so a row's bits do not depend on M.
+// k-step of 256).  The units, row-block-major, are split into `grid` contiguous, equal ranges;
+// grid = min(units, SMs).  Which block computes which part of a row's sum, the order of the
+// MMAs inside a unit, the order in which units and parts are added all depend on (N, K,
+// grid) only.  Activation row m is column m of every MMA, its exponent e depends on row m
+// alone, and nothing a column computes depends on another column, so a row's bits do not
+// depend on M.
 #pragma once
 
 #include <cuda.h>
@@ -44,59 +41,66 @@
 namespace nvfp4 {
 
 // ------------------------------------------------------------------ configuration
-constexpr int kTileRows = 128;                        // MMA M
-constexpr int kTiles = 2;                             // MMA tiles per row block
-constexpr int kRowsPerBlock = kTileRows * kTiles;     // 256
-constexpr int kKStep = 256;                           // k per unit and per ring stage
-constexpr int kSubK = 128;                            // k per tensor-memory A slot (8 MMAs per hand-off)
-constexpr int kSubsPerStage = kKStep / kSubK;         // 2
-constexpr int kK16PerSub = kSubK / 16;                // 8
-constexpr int kNmma = 32;                             // activation rows per MMA (MMA N)
-constexpr int kStages = 4;                            // shared-memory ring depth
-constexpr int kASlots = 3;                            // tensor-memory A ring depth (1.5 stages)
-constexpr int kCodeRowBytes = kKStep / 2;             // 128 bytes of E2M1 codes per row per stage
-constexpr int kScaleRowBytes = kKStep / 16;           // 16 E4M3 scales per row per stage
-constexpr int kXGroupBytes = 8 * kKStep * 2;          // 8 activation rows x 256 k x fp16 = 4 KB
+constexpr int kTileRows = 128;                      // MMA M
+constexpr int kTiles = 2;                           // MMA tiles per row block
+constexpr int kRowsPerBlock = kTileRows * kTiles;   // 256
+constexpr int kKStep = 256;                         // k per unit
+constexpr int kHalves = 2;                          // k-halves per unit: one A slot and one issuer each
+constexpr int kHalfK = kKStep / kHalves;            // 128
+constexpr int kK16PerHalf = kHalfK / 16;            // 8 MMAs per issuer per unit
+constexpr int kNmma = 32;                           // activation rows per MMA (MMA N)
+constexpr int kStages = 4;                          // weight ring depth
+constexpr int kCodeRowBytes = kKStep / 2;           // 128 bytes of E2M1 codes per row per unit
+constexpr int kScaleRowBytes = kKStep / 16;         // 16 E4M3 scales per row per unit
 constexpr int kCodeStageBytes = kRowsPerBlock * kCodeRowBytes;    // 32768, 128-byte swizzled rows
 constexpr int kScaleStageBytes = kRowsPerBlock * kScaleRowBytes;  // 4096
-constexpr int kXStageBytes = 4 * kXGroupBytes;                    // 16384
-constexpr int kStageBytes = kCodeStageBytes + kScaleStageBytes + kXStageBytes;  // 53248 (1 KB multiple)
-constexpr int kXStageOffset = kCodeStageBytes + kScaleStageBytes;              // 36864 (1 KB aligned)
+constexpr int kWStageBytes = kCodeStageBytes + kScaleStageBytes;  // 36864
+constexpr int kXBufs = 2;                           // activation buffers (one per unit in flight)
+constexpr int kXGroupBytes = 8 * kKStep * 2;        // 8 activation rows x 256 k x fp16 = 4 KB
+constexpr int kX16Bytes = (kNmma / 8) * kXGroupBytes;             // 16384: operand layout
+constexpr int kXRawPitch = kKStep * 2 + 16;         // 528: bf16 row + 16 bytes (conflict-free reads)
+constexpr int kXRawBytes = kNmma * kXRawPitch;      // 16896
 
 constexpr int kDecodeWarps = 8;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;    // issues tile 0's MMAs; also allocates tensor memory
-constexpr int kEpiWarp0 = 10;
+constexpr int kEpiWarp0 = 8;  // also allocates and frees tensor memory
 constexpr int kEpiWarps = 4;
-constexpr int kMmaWarp1 = 14;  // issues tile 1's MMAs
-constexpr int kWarps = 15;
-constexpr int kThreads = kWarps * 32;  // 480
+constexpr int kMmaWarp0 = 12;
+constexpr int kMmaWarps = 4;
+constexpr int kWarps = 16;
+constexpr int kThreads = kWarps * 32;  // 512
+static_assert(kMmaWarp0 + kMmaWarps == kWarps, "warp roles");
 
+// tensor memory: A slot (half h, tile t) = 64 columns of fp16 pairs (128 k); D buffer d holds
+// one 32-column accumulator per (tile, half)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kASlotCols = kSubK / 2 * kTiles;  // 128: 2 fp16 per 32-bit column, both tiles
-constexpr uint32_t kAColBase = 0;    // A slot a, tile t: columns a*128 + t*64 .. +64
-constexpr uint32_t kDColBase = kASlots * kASlotCols;  // 384; D buffer d, tile t: 384 + d*64 + t*32 .. +32
-static_assert(kDColBase + 2 * kTiles * kNmma <= kTmemCols, "tensor memory budget");
+__device__ __forceinline__ uint32_t a_col(int h, int t) { return (uint32_t)(h * 128 + t * 64); }
+__device__ __forceinline__ uint32_t d_col(int d, int t, int h) {
+  return 256u + (uint32_t)(d * 128 + (t * kHalves + h) * kNmma);
+}
 
-// mbarrier indices in the barrier array
-constexpr int kBarFull = 0;                               // [kStages]  producer -> consumers (tx)
-constexpr int kBarEmpty = kBarFull + kStages;             // [kStages]  8 decoder warps + 2 MMA commits
-constexpr int kBarAEmpty = kBarEmpty + kStages;           // [kASlots][tile]  MMA commit -> decoders
-constexpr int kBarDFull = kBarAEmpty + kASlots * kTiles;  // [2]        2 MMA commits -> epilogue
-constexpr int kBarFinal = kBarDFull + 2;                  // [tile]     MMA drain at exit
-constexpr int kNumBars = kBarFinal + kTiles;
+// shared memory
+constexpr int kSmemX16 = kStages * kWStageBytes;            // 147456
+constexpr int kSmemXRaw = kSmemX16 + kXBufs * kX16Bytes;    // 180224
+constexpr int kSmemBar = kSmemXRaw + kXBufs * kXRawBytes;   // 214016
+// mbarrier indices
+constexpr int kBarFull = 0;                                  // [kStages]  weight copies (tx) -> decoders
+constexpr int kBarAEmpty = kBarFull + kStages;               // [half][tile]  MMA commit -> decoders
+constexpr int kBarUnit = kBarAEmpty + kHalves * kTiles;      // [kXBufs]   4 MMA commits -> epilogue
+constexpr int kBarXRaw = kBarUnit + kXBufs;                  // [kXBufs]   activation copies (tx)
+constexpr int kBarFinal = kBarXRaw + kXBufs;                 // [issuer]   MMA drain at exit
+constexpr int kNumBars = kBarFinal + kMmaWarps;
+constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
+// misc: +0 tensor-memory base, +4 abort flag, +8 fix-up flag, +16 stage release counts
+// [kStages], +128 xs[kXBufs][32] (2^-e), +384 xf[kXBufs][32][2] (2^e as two factors)
+constexpr int kSmemBytes = kSmemMisc + 1024 + 1024;  // misc + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory per block");
 
 // hardware named barriers (0 is __syncthreads)
 constexpr uint32_t kNbEpi = 1;  // the 4 epilogue warps
-__device__ __forceinline__ uint32_t nb_afull(int slot, int tile) { return 2u + (uint32_t)(slot * kTiles + tile); }
-__device__ __forceinline__ uint32_t nb_dempty(int dbuf, int tile) { return 2u + kASlots * kTiles + (uint32_t)(dbuf * kTiles + tile); }
-static_assert(2 + kASlots * kTiles + 2 * kTiles <= 16, "hardware named barriers");
-constexpr uint32_t kNbPairThreads = 4 * 32 + 32;  // 4 decoder (or epilogue) warps + 1 issuer warp
-
-constexpr int kSmemRingBytes = kStages * kStageBytes;  // 212992
-constexpr int kSmemBarOffset = kSmemRingBytes;
-constexpr int kSmemMiscOffset = kSmemBarOffset + kNumBars * 8;
-constexpr int kSmemBytes = kSmemMiscOffset + 256 + 1024;  // misc + alignment slack
+__device__ __forceinline__ uint32_t nb_afull(int h, int t) { return 2u + (uint32_t)(h * kTiles + t); }
+__device__ __forceinline__ uint32_t nb_ready(int d) { return 6u + (uint32_t)d; }
+constexpr uint32_t kNbAFullThreads = 4 * 32 + 32;    // 4 decoder warps + 1 issuer warp
+constexpr uint32_t kNbReadyThreads = 4 * 32 + 4 * 32;  // 4 epilogue warps + 4 issuer warps
 
 // instruction descriptor: kind::f16, D = f32, A = B = f16, both K-major, N = 32, M = 128
 constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(kNmma >> 3) << 17) |
@@ -109,15 +113,13 @@ enum : int { kErrTimeout = 1 };
 struct MainParams {
   CUtensorMap tm_codes;   // uint8 [N rows, K/2 bytes], box 128 B x 256 rows, 128-byte swizzle
   CUtensorMap tm_scales;  // uint8 [N rows, K/16 bytes], box 16 B x 256 rows
-  const uint8_t* x16;     // workspace: 4 row groups x (16*K) bytes, operand layout
-  const float* xs;        // workspace [32]: 2^-e_m
+  const uint16_t* x;      // bf16 [M, K]
   void* y;                // [M, N] bf16 or f32
   float* partials;        // workspace [2*grid][32][256]
   int* counters;          // workspace [2][row_blocks]: parts published, blocks done; zero between calls
   int* err;               // workspace error word
   float gs;
   int M;
-  int m_groups;  // ceil(M / 8): activation row groups copied per stage
   int out_f32;
   int grid;
   int64_t N, K;
@@ -164,20 +166,13 @@ __device__ __forceinline__ uint64_t x_desc(uint32_t addr) {
          (1ull << 46);
 }
 
-// ------------------------------------------------------------------ activation conversion
-// One 128-thread block per activation row m < 8 * ceil(M / 8); rows m >= M are written as
-// zeros.  Small on purpose (<= 32 registers per thread): a block fits on an SM beside a block
-// of the main kernel, so converting the next call's activations never displaces one.  Pass 1
-// finds the row's largest magnitude, pass 2 (re-reading through L1) scales, converts, stores.
-// x16 layout: row group g = m / 8 owns bytes [g * 16K, (g + 1) * 16K); inside it, k16 block
-// j at j * 256, k-half h at + h * 128, row m % 8 at + (m % 8) * 16, 8 fp16 per 16 bytes.
-constexpr int kPrepThreads = 128;
-
+// ------------------------------------------------------------------ activation conversion helpers
 __device__ __forceinline__ float bf16x2_absmax(uint32_t w, float a) {
   a = fmaxf(a, fabsf(__uint_as_float(w << 16)));
   return fmaxf(a, fabsf(__uint_as_float(w & 0xFFFF0000u)));
 }
 
+// 8 bf16 -> 8 fp16, each times f1 * f2 (two factors: 2^e can exceed the float range).
 __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, float f1, float f2) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   uint32_t r[4];
@@ -190,56 +185,44 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, float f1, float f2) {
   return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
-__global__ void __launch_bounds__(kPrepThreads, 16) x_prep_kernel(const uint16_t* __restrict__ x, int M, int64_t K,
-                                                                  uint8_t* __restrict__ x16, float* __restrict__ xs) {
-  ptx::grid_launch_dependents();
-  ptx::grid_dependency_wait();  // x is produced upstream; x16 / xs are read by the previous call
-  const int m = blockIdx.x;
-  const int64_t K8 = K / 8;
-  const uint4* xr = reinterpret_cast<const uint4*>(x + (int64_t)m * K);
-  __shared__ float red[kPrepThreads / 32];
-  float amax = 0.f;
-  if (m < M) {
-#pragma unroll 4
-    for (int64_t i = threadIdx.x; i < K8; i += kPrepThreads) {
-      const uint4 w = __ldg(xr + i);
-      amax = bf16x2_absmax(w.x, bf16x2_absmax(w.y, bf16x2_absmax(w.z, bf16x2_absmax(w.w, amax))));
-    }
-  }
+// acc[j] += (D_a[j] + D_b[j]) * xs[j] over the first 16 or all 32 columns of two accumulators,
+// 8 columns at a time (few registers held: the epilogue also keeps 64 accumulators).
+template <int C0, int NC>
+__device__ __forceinline__ void drain_cols8(float (&acc)[NC], uint32_t addr_a, uint32_t addr_b, const float* xs) {
+  uint32_t a[8], b[8];
+  ptx::tmem_ld8(addr_a + C0, a);
+  ptx::tmem_ld8(addr_b + C0, b);
+  ptx::tmem_wait_ld();
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
-  __syncthreads();
-  amax = red[0];
-#pragma unroll
-  for (int i = 1; i < kPrepThreads / 32; ++i) amax = fmaxf(amax, red[i]);
-  // amax = f * 2^E, f in [0.5, 1): e = 16 - E puts amax * 2^e in [2^15, 2^16).
-  int e = 0;
-  if (amax > 0.f && amax <= 3.4028234663852886e38f) {
-    int E;
-    (void)frexpf(amax, &E);
-    e = 16 - E;
+  for (int j = 0; j < 8; ++j)
+    acc[C0 + j] = __fmaf_rn(__fadd_rn(__uint_as_float(a[j]), __uint_as_float(b[j])), xs[C0 + j], acc[C0 + j]);
+}
+template <int NC>
+__device__ __forceinline__ void drain_tile(float (&acc)[NC], uint32_t addr_a, uint32_t addr_b, const float* xs) {
+  drain_cols8<0>(acc, addr_a, addr_b, xs);
+  drain_cols8<8>(acc, addr_a, addr_b, xs);
+  if constexpr (NC > 16) {
+    drain_cols8<16>(acc, addr_a, addr_b, xs);
+    drain_cols8<24>(acc, addr_a, addr_b, xs);
   }
-  const int e1 = e / 2, e2 = e - e1;
-  const float f1 = ldexpf(1.f, e1), f2 = ldexpf(1.f, e2);
-  uint8_t* grp = x16 + (int64_t)(m / 8) * 16 * K + (m % 8) * 16;
-#pragma unroll 4
-  for (int64_t i = threadIdx.x; i < K8; i += kPrepThreads) {
-    const uint4 w = m < M ? __ldg(xr + i) : make_uint4(0u, 0u, 0u, 0u);
-    *reinterpret_cast<uint4*>(grp + (i / 2) * 256 + (i % 2) * 128) = bf16x8_to_f16x8(w, f1, f2);
-  }
-  if (threadIdx.x == 0) xs[m] = (m < M) ? ldexpf(1.f, -e) : 1.f;
 }
 
 // ------------------------------------------------------------------ main kernel
+// NC = activation rows the epilogue reads back (16 for M <= 16, else 32).  The MMAs are the
+// same N = 32 instructions in both instantiations and every column's epilogue arithmetic is the
+// same sequence of correctly rounded operations, so a row's bits do not depend on NC either.
+template <int NC>
 __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_constant__ MainParams p) {
+  static_assert(NC == 16 || NC == 32, "epilogue width");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSmemBarOffset);
-  uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + kSmemMiscOffset);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemMiscOffset + 4);
-  volatile int* fix_flag = reinterpret_cast<volatile int*>(smem + kSmemMiscOffset + 8);
-  float* xs_smem = reinterpret_cast<float*>(smem + kSmemMiscOffset + 128);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSmemBar);
+  uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + kSmemMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemMisc + 4);
+  volatile int* fix_flag = reinterpret_cast<volatile int*>(smem + kSmemMisc + 8);
+  int* release_cnt = reinterpret_cast<int*>(smem + kSmemMisc + 16);  // [kStages]
+  float* xs_smem = reinterpret_cast<float*>(smem + kSmemMisc + 128);  // [kXBufs][32]
+  float* xf_smem = reinterpret_cast<float*>(smem + kSmemMisc + 384);  // [kXBufs][32][2]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = ptx::smem_addr(smem);
@@ -250,25 +233,46 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
   const int64_t u_begin = unit_begin(blockIdx.x, T, G), u_end = unit_begin(blockIdx.x + 1, T, G);
   const int n_local = (int)(u_end - u_begin);
 
-  // ---- set-up: barriers, x slots zeroed, tensor memory
+  // ---- set-up: barriers, activation operands zeroed (rows >= M stay zero), tensor memory
+  const uint64_t pol_w = ptx::policy_evict_first();
+  // unit i's weights -> stage i % kStages (full boxes are always delivered: rows past N are
+  // zero-filled); one thread issues
+  auto issue_weights = [&](int i) {
+    const int64_t u = u_begin + i, rb = u / S, s = u % S;
+    const int st = i % kStages;
+    const uint32_t stage = smem_base + (uint32_t)(st * kWStageBytes);
+    const uint32_t fb = bar(kBarFull + st);
+    ptx::mbar_arrive_expect_tx(fb, (uint32_t)kWStageBytes);
+    ptx::tma_load_2d(stage, &p.tm_codes, (int32_t)(s * kCodeRowBytes), (int32_t)(rb * kRowsPerBlock), fb, pol_w);
+    ptx::tma_load_2d(stage + kCodeStageBytes, &p.tm_scales, (int32_t)(s * kScaleRowBytes),
+                     (int32_t)(rb * kRowsPerBlock), fb, pol_w);
+  };
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(bar(kBarFull + s), 1);
-      ptx::mbar_init(bar(kBarEmpty + s), kDecodeWarps + kTiles);
+      release_cnt[s] = 0;
     }
-    for (int a = 0; a < kASlots * kTiles; ++a) ptx::mbar_init(bar(kBarAEmpty + a), 1);
-    for (int d = 0; d < 2; ++d) ptx::mbar_init(bar(kBarDFull + d), kTiles);
-    for (int t = 0; t < kTiles; ++t) ptx::mbar_init(bar(kBarFinal + t), 1);
+    for (int a = 0; a < kHalves * kTiles; ++a) ptx::mbar_init(bar(kBarAEmpty + a), 1);
+    for (int d = 0; d < kXBufs; ++d) {
+      ptx::mbar_init(bar(kBarUnit + d), kMmaWarps);
+      ptx::mbar_init(bar(kBarXRaw + d), 1);
+    }
+    for (int q = 0; q < kMmaWarps; ++q) ptx::mbar_init(bar(kBarFinal + q), 1);
     *abort_flag = 0;
     *fix_flag = 0;
     ptx::fence_mbar_init();
+    // The weights are read-only inputs that no kernel of this stream writes while calls are
+    // queued, so they are streamed before the dependency wait on the previous call.
+    ptx::prefetch_tensormap(&p.tm_codes);
+    ptx::prefetch_tensormap(&p.tm_scales);
+    for (int i = 0; i < kStages && i < n_local; ++i) issue_weights(i);
   }
-  for (int s = 0; s < kStages; ++s) {
-    uint4* xz = reinterpret_cast<uint4*>(smem + s * kStageBytes + kXStageOffset);
-    for (int i = threadIdx.x; i < kXStageBytes / 16; i += kThreads) xz[i] = make_uint4(0u, 0u, 0u, 0u);
+  {
+    uint4* xz = reinterpret_cast<uint4*>(smem + kSmemX16);
+    for (int i = threadIdx.x; i < kXBufs * kX16Bytes / 16; i += kThreads) xz[i] = make_uint4(0u, 0u, 0u, 0u);
   }
   ptx::fence_proxy_async_smem();
-  if (warp == kMmaWarp) {
+  if (warp == kEpiWarp0) {
     ptx::tmem_alloc(ptx::smem_addr(tmem_base_smem), kTmemCols);
     ptx::tmem_relinquish();
   }
@@ -279,68 +283,19 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
   const uint32_t tmem = *tmem_base_smem;
   const Abort ab{abort_flag, p.err};
 
-  if (warp == kProducerWarp) {
-    // ================================================================ producer
-    const uint64_t pol_w = ptx::policy_evict_first();
-    const uint64_t pol_x = ptx::policy_evict_last();
-    const int prologue = n_local < kStages ? n_local : kStages;
-    if (lane == 0) {
-      ptx::prefetch_tensormap(&p.tm_codes);
-      ptx::prefetch_tensormap(&p.tm_scales);
-    }
-    auto issue_weights = [&](int i) {
-      const int64_t u = u_begin + i, rb = u / S, s = u % S;
-      const int st = i % kStages;
-      const uint32_t stage = smem_base + (uint32_t)(st * kStageBytes);
-      const uint32_t fb = bar(kBarFull + st);
-      if (lane == 0) {
-        // full boxes are always delivered (rows past N are zero-filled)
-        ptx::mbar_arrive_expect_tx(fb, (uint32_t)(kCodeStageBytes + kScaleStageBytes + p.m_groups * kXGroupBytes));
-        ptx::tma_load_2d(stage, &p.tm_codes, (int32_t)(s * kCodeRowBytes), (int32_t)(rb * kRowsPerBlock), fb, pol_w);
-        ptx::tma_load_2d(stage + kCodeStageBytes, &p.tm_scales, (int32_t)(s * kScaleRowBytes),
-                         (int32_t)(rb * kRowsPerBlock), fb, pol_w);
-      }
-      __syncwarp();
-    };
-    auto issue_x = [&](int i) {
-      const int64_t s = (u_begin + i) % S;
-      const int st = i % kStages;
-      if (lane < p.m_groups)
-        ptx::bulk_g2s(smem_base + (uint32_t)(st * kStageBytes + kXStageOffset + lane * kXGroupBytes),
-                      p.x16 + (int64_t)lane * 16 * p.K + s * kXGroupBytes, kXGroupBytes, bar(kBarFull + st), pol_x);
-    };
-    // weights do not depend on earlier kernels: stream them before the dependency wait
-    for (int i = 0; i < prologue; ++i) issue_weights(i);
-    ptx::grid_dependency_wait();
-    for (int i = 0; i < prologue; ++i) issue_x(i);
-    bool ok = true;
-    for (int i = prologue; i < n_local && ok; ++i) {
-      const int st = i % kStages, round = i / kStages;
-      ok = wait_bar(bar(kBarEmpty + st), (uint32_t)((round & 1) ^ 1), ab);
-      if (!ok) break;
-      issue_weights(i);
-      issue_x(i);
-    }
-    // drain: the last fill of every stage must have landed before the block exits
-    for (int st = 0; st < kStages && st < n_local; ++st) {
-      const int last = st + ((n_local - 1 - st) / kStages) * kStages;
-      const int round = last / kStages;
-      wait_bar(bar(kBarFull + st), (uint32_t)(round & 1), ab);
-    }
-  } else if (warp < kDecodeWarps) {
+  if (warp < kDecodeWarps) {
     // ================================================================ decoders
     const int tile = warp >> 2, quad = warp & 3;
     const int row_in_block = tile * kTileRows + quad * 32 + lane;
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
-    int a_use = 0;
     bool ok = true;
-    // Every unit and sub-slot is walked even after an abort, so the A-full arrivals always
-    // pair with the issuer's syncs; after an abort the decoded data is simply not stored.
+    // Every unit and half is walked even after an abort, so the A-full arrivals always pair
+    // with the issuers' syncs; after an abort the decoded data is simply not stored.
     for (int i = 0; i < n_local; ++i) {
       const int st = i % kStages, round = i / kStages;
       if (ok) ok = wait_bar(bar(kBarFull + st), (uint32_t)(round & 1), ab);
       ok = __all_sync(0xffffffffu, ok);
-      const uint8_t* stage = smem + st * kStageBytes;
+      const uint8_t* stage = smem + st * kWStageBytes;
       // 128-byte swizzle: 16-byte chunk q of row r sits at chunk q ^ (r % 8) of the row
       const uint8_t* crow = stage + row_in_block * kCodeRowBytes;
       const int swz = row_in_block & 7;
@@ -350,23 +305,31 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
       for (int q = 0; q < 8; ++q) c[q] = ok ? *reinterpret_cast<const uint4*>(crow + ((q ^ swz) << 4)) : sc;
       if (ok) sc = *reinterpret_cast<const uint4*>(stage + kCodeStageBytes + row_in_block * kScaleRowBytes);
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(kBarEmpty + st));
+      if (lane == 0) {
+        // this warp's share of the stage is in registers; the last of the 8 warps refills it.
+        // The count only grows: a round's 8 increments all precede the refill that the next
+        // round's increments wait for, so the last of a round sees a count = 7 mod 8.
+        __threadfence_block();
+        if ((atomicAdd(release_cnt + st, 1) & (kDecodeWarps - 1)) == kDecodeWarps - 1) {
+          __threadfence_block();
+          if (i + kStages < n_local && !*abort_flag) issue_weights(i + kStages);
+        }
+      }
       const uint32_t sw4[4] = {sc.x, sc.y, sc.z, sc.w};
 #pragma unroll
-      for (int sub = 0; sub < kSubsPerStage; ++sub) {
-        const int slot = a_use % kASlots, around = a_use / kASlots;
-        // the slot's previous MMAs must have completed before it is overwritten (and before the
-        // next arrival on its named barrier): this wait ignores the abort flag
-        const bool freed = wait_bar(bar(kBarAEmpty + slot * kTiles + tile), (uint32_t)((around & 1) ^ 1), ab, false);
+      for (int h = 0; h < kHalves; ++h) {
+        // this half's A slot: its MMAs of the previous unit must have completed (and the issuer
+        // must have synced) before it is overwritten; the wait ignores the abort flag
+        const bool freed = wait_bar(bar(kBarAEmpty + h * kTiles + tile), (uint32_t)((i & 1) ^ 1), ab, false);
         const bool store = __all_sync(0xffffffffu, ok && freed);
         if (store) ptx::tc_fence_after();
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          // k [128 sub + 64 hh, +64): code words c[4 sub + 2 hh], c[4 sub + 2 hh + 1]; 4 scale blocks
-          const uint32_t sw = sw4[2 * sub + hh];
+          // k [128 h + 64 hh, +64): code words c[4 h + 2 hh], c[4 h + 2 hh + 1]; 4 scale blocks
+          const uint32_t sw = sw4[2 * h + hh];
           const uint32_t s0 = ptx::e4m3_pair(sw, 0), s1 = ptx::e4m3_pair(sw, 1);
           const uint32_t s2 = ptx::e4m3_pair(sw, 2), s3 = ptx::e4m3_pair(sw, 3);
-          const uint4 lo = c[4 * sub + 2 * hh], hi = c[4 * sub + 2 * hh + 1];
+          const uint4 lo = c[4 * h + 2 * hh], hi = c[4 * h + 2 * hh + 1];
           uint32_t o[32];
           ptx::e2m1x8_scaled(lo.x, s0, o[0], o[1], o[2], o[3]);
           ptx::e2m1x8_scaled(lo.y, s0, o[4], o[5], o[6], o[7]);
@@ -376,125 +339,169 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
           ptx::e2m1x8_scaled(hi.y, s2, o[20], o[21], o[22], o[23]);
           ptx::e2m1x8_scaled(hi.z, s3, o[24], o[25], o[26], o[27]);
           ptx::e2m1x8_scaled(hi.w, s3, o[28], o[29], o[30], o[31]);
-          if (store) ptx::tmem_st32(t_lane + kAColBase + (uint32_t)(slot * kASlotCols + tile * 64 + hh * 32), o);
+          if (store) ptx::tmem_st32(t_lane + a_col(h, tile) + (uint32_t)(hh * 32), o);
         }
         if (store) ptx::tmem_wait_st();
         ptx::tc_fence_before();
-        ptx::named_bar_arrive(nb_afull(slot, tile), kNbPairThreads);
-        ++a_use;
+        ptx::named_bar_arrive(nb_afull(h, tile), kNbAFullThreads);
       }
     }
-  } else if (warp == kMmaWarp || warp == kMmaWarp1) {
-    // ================================================================ MMA issuers (one per tile)
+  } else if (warp >= kMmaWarp0) {
+    // ================================================================ MMA issuers
     // The whole warp walks the schedule (named barriers are warp-wide); lane 0 issues.  No
-    // shared-memory reads here: A-full and D-free come from named barriers, completions go out
-    // through tcgen05.commit.  The issuer has no abort path: MMAs on stale data are harmless,
-    // and its commits keep every other role's waits completing.
-    const int t = warp == kMmaWarp ? 0 : 1;
-    int a_use = 0, dbuf = 0;
-    int d_use0 = 0, d_use1 = 0;
+    // shared-memory reads here: operand readiness comes from named barriers, completions go
+    // out through tcgen05.commit.  The issuer has no abort path: MMAs on stale data are
+    // harmless, and its commits keep every other role's waits completing.
+    const int q = warp - kMmaWarp0, t = q >> 1, h = q & 1;
     for (int i = 0; i < n_local; ++i) {
-      const int64_t u = u_begin + i, s = u % S;
-      const bool seg_start = (i == 0) || (s == 0);
-      const bool seg_end = (i == n_local - 1) || (s == S - 1);
-      const int st = i % kStages;
-      if (seg_start) {
-        if ((dbuf ? d_use1 : d_use0) > 0) ptx::named_bar_sync(nb_dempty(dbuf, t), kNbPairThreads);
-        ptx::tc_fence_after();
-      }
-      const uint32_t xstage = smem_base + (uint32_t)(st * kStageBytes + kXStageOffset);
-      const uint32_t d_tmem = tmem + kDColBase + (uint32_t)(dbuf * 64 + t * 32);
+      const int d = i & 1;
+      ptx::named_bar_sync(nb_ready(d), kNbReadyThreads);  // activations of unit i in place, D(d) drained
+      ptx::named_bar_sync(nb_afull(h, t), kNbAFullThreads);
+      ptx::tc_fence_after();
+      if (lane == 0) {
+        const uint32_t d_tmem = tmem + d_col(d, t, h);
+        const uint32_t a_tmem = tmem + a_col(h, t);
+        const uint32_t xb = smem_base + (uint32_t)(kSmemX16 + d * kX16Bytes + h * kK16PerHalf * 256);
 #pragma unroll
-      for (int sub = 0; sub < kSubsPerStage; ++sub) {
-        const int slot = a_use % kASlots;
-        ptx::named_bar_sync(nb_afull(slot, t), kNbPairThreads);
-        ptx::tc_fence_after();
-        if (lane == 0) {
-#pragma unroll
-          for (int kk = 0; kk < kK16PerSub; ++kk) {
-            const int j = sub * kK16PerSub + kk;
-            const uint32_t acc = (seg_start && sub == 0 && kk == 0) ? 0u : 1u;
-            ptx::mma_f16_ts(d_tmem, tmem + kAColBase + (uint32_t)(slot * kASlotCols + t * 64 + kk * 8),
-                            x_desc(xstage + (uint32_t)(j * 256)), kIdesc, acc);
-          }
-          ptx::mma_commit(bar(kBarAEmpty + slot * kTiles + t));
-        }
-        ++a_use;
+        for (int kk = 0; kk < kK16PerHalf; ++kk)
+          ptx::mma_f16_ts(d_tmem, a_tmem + (uint32_t)(kk * 8), x_desc(xb + (uint32_t)(kk * 256)), kIdesc,
+                          kk > 0 ? 1u : 0u);
+        ptx::mma_commit(bar(kBarAEmpty + h * kTiles + t));
+        ptx::mma_commit(bar(kBarUnit + d));
       }
-      if (lane == 0) ptx::mma_commit(bar(kBarEmpty + st));
-      if (seg_end) {
-        if (lane == 0) ptx::mma_commit(bar(kBarDFull + dbuf));
-        if (dbuf) ++d_use1; else ++d_use0;
-        dbuf ^= 1;
-      }
+      __syncwarp();
     }
     // drain every MMA issued before tensor memory is released
     if (lane == 0) {
-      ptx::mma_commit(bar(kBarFinal + t));
-      wait_bar(bar(kBarFinal + t), 0u, ab, false);
+      ptx::mma_commit(bar(kBarFinal + q));
+      wait_bar(bar(kBarFinal + q), 0u, ab, false);
     }
     __syncwarp();
   } else {
-    // ================================================================ epilogue
-    const int quad = warp & 3;
-    const int etid = (warp - kEpiWarp0) * 32 + lane;  // 0..127
-    ptx::grid_dependency_wait();  // xs, partials, counters and y belong to the previous call until here
-    if (etid < 32) xs_smem[etid] = p.xs[etid];
-    ptx::named_bar_sync(1, kEpiWarps * 32);
+    // ================================================================ activations + epilogue
+    const int ew = warp - kEpiWarp0, quad = warp & 3;
+    const int etid = ew * 32 + lane;  // 0..127
+    ptx::grid_dependency_wait();  // x is produced upstream; y, partials and counters belong to the previous call until here
     const int M = p.M;
     const float gs = p.gs;
-    int dbuf = 0;
-    int d_use[2] = {0, 0};
-    int n_seg = 0;
-    for (int i = 0; i < n_local; ++i)
-      if (i == n_local - 1 || (u_begin + i) % S == S - 1) ++n_seg;
-    int seg = 0;
+    const uint64_t pol_x = ptx::policy_evict_last();
+    const int64_t K = p.K;
+
+    // bf16 rows m < M of unit j's k-step -> raw buffer j % 2 (one 512-byte bulk copy per row)
+    auto issue_x = [&](int j) {
+      const int d = j & 1;
+      const int64_t s = (u_begin + j) % S;
+      const uint32_t xb = bar(kBarXRaw + d);
+      ptx::mbar_arrive_expect_tx(xb, (uint32_t)(M * kKStep * 2));
+      for (int m = 0; m < M; ++m)
+        ptx::bulk_g2s(smem_base + (uint32_t)(kSmemXRaw + d * kXRawBytes + m * kXRawPitch), p.x + m * K + s * kKStep,
+                      (uint32_t)(kKStep * 2), xb, pol_x);
+    };
+    // raw buffer j % 2 -> fp16 operand buffer j % 2, 2^-e -> xs; ends with a barrier of the 4 warps
+    auto convert = [&](int j) {
+      const int d = j & 1;
+      const bool xok = __all_sync(0xffffffffu, wait_bar(bar(kBarXRaw + d), (uint32_t)((j >> 1) & 1), ab));
+      const uint8_t* raw = smem + kSmemXRaw + d * kXRawBytes;
+      uint8_t* x16 = smem + kSmemX16 + d * kX16Bytes;
+      float* xs = xs_smem + d * kNmma;
+      float* xf = xf_smem + d * kNmma * 2;
+      // pass 1: one warp per row, e from the row's largest magnitude in this k-step
+      if (xok) {
+        for (int m = ew; m < M; m += kEpiWarps) {
+          const uint4 w = *reinterpret_cast<const uint4*>(raw + m * kXRawPitch + lane * 16);
+          float amax = bf16x2_absmax(w.x, bf16x2_absmax(w.y, bf16x2_absmax(w.z, bf16x2_absmax(w.w, 0.f))));
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+          if (lane == 0) {
+            // amax = f * 2^E, f in [0.5, 1): e = 16 - E puts amax * 2^e in [2^15, 2^16)
+            int e = 0;
+            if (amax > 0.f && amax <= 3.4028234663852886e38f) {
+              int E;
+              (void)frexpf(amax, &E);
+              e = 16 - E;
+            }
+            const int e1 = e / 2, e2 = e - e1;
+            xf[2 * m] = ldexpf(1.f, e1);
+            xf[2 * m + 1] = ldexpf(1.f, e2);
+            xs[m] = ldexpf(1.f, -e);
+          }
+        }
+      }
+      ptx::named_bar_sync(kNbEpi, kEpiWarps * 32);
+      // pass 2: lane = (row r = lane % 8, chunk c = 4 cb + lane / 8) of a row group; each warp
+      // writes 512 contiguous bytes of the operand layout
+      if (xok) {
+        const int items = ((M + 7) >> 3) * 8;
+        for (int it = ew; it < items; it += kEpiWarps) {
+          const int g = it >> 3, cb = it & 7;
+          const int m = g * 8 + (lane & 7), c = cb * 4 + (lane >> 3);
+          if (m < M) {
+            const uint4 w = *reinterpret_cast<const uint4*>(raw + m * kXRawPitch + c * 16);
+            *reinterpret_cast<uint4*>(x16 + g * kXGroupBytes + c * 128 + (m & 7) * 16) =
+                bf16x8_to_f16x8(w, xf[2 * m], xf[2 * m + 1]);
+          }
+        }
+      }
+      ptx::fence_proxy_async_smem();  // operand writes -> the tensor core's (async proxy) reads
+      ptx::named_bar_sync(kNbEpi, kEpiWarps * 32);
+    };
+
+    if (etid == 0)
+      for (int j = 0; j < kXBufs && j < n_local; ++j) issue_x(j);
+    for (int j = 0; j < kXBufs && j < n_local; ++j) {
+      convert(j);
+      if (etid == 0 && j + kXBufs < n_local) issue_x(j + kXBufs);
+      ptx::named_bar_arrive(nb_ready(j), kNbReadyThreads);
+    }
+
+    float acc0[NC], acc1[NC];  // rows r0 (tile 0) and r1 (tile 1) of the current row block
+#pragma unroll
+    for (int m = 0; m < NC; ++m) acc0[m] = acc1[m] = 0.f;
     bool ok = true;
     int64_t pend[2] = {0, 0};  // split row blocks of this block's range (its first and last)
     int n_pend = 0;
+    const int r0 = quad * 32 + lane, r1 = r0 + kTileRows;  // rows inside the row block
     for (int i = 0; i < n_local; ++i) {
+      const int d = i & 1;
       const int64_t u = u_begin + i, rb = u / S, s = u % S;
       const bool seg_end = (i == n_local - 1) || (s == S - 1);
-      if (!seg_end) continue;
-      // D must be complete before it is read and before the D-free arrival: ignores the abort flag
-      const bool full = wait_bar(bar(kBarDFull + dbuf), (uint32_t)(d_use[dbuf] & 1), ab, false);
-      ok = ok && full;
+      // unit i's MMAs complete: D(d) final and activation buffer d free; gates a ready arrival,
+      // so the wait ignores the abort flag
+      const bool full = wait_bar(bar(kBarUnit + d), (uint32_t)((i >> 1) & 1), ab, false);
+      ok = __all_sync(0xffffffffu, ok && full);
       ptx::tc_fence_after();
-      uint32_t v0[32], v1[32];
-      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + kDColBase + (uint32_t)(dbuf * 64);
-      ptx::tmem_ld32(taddr, v0);
-      ptx::tmem_ld32(taddr + 32, v1);
-      ptx::tmem_wait_ld();
+      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16);
+      const float* xs = xs_smem + d * kNmma;
+      drain_tile(acc0, taddr + d_col(d, 0, 0), taddr + d_col(d, 0, 1), xs);
+      drain_tile(acc1, taddr + d_col(d, 1, 0), taddr + d_col(d, 1, 1), xs);
       ptx::tc_fence_before();
-      // the issuers wait for this buffer again only if a later segment of this block uses it
-      if (seg + 2 < n_seg) {
-        ptx::named_bar_arrive(nb_dempty(dbuf, 0), kNbPairThreads);
-        ptx::named_bar_arrive(nb_dempty(dbuf, 1), kNbPairThreads);
+      ptx::named_bar_sync(kNbEpi, kEpiWarps * 32);  // D(d) and xs[d] read by every epilogue thread
+      if (i + kXBufs < n_local) {
+        convert(i + kXBufs);
+        if (etid == 0 && i + 2 * kXBufs < n_local) issue_x(i + 2 * kXBufs);
+        ptx::named_bar_arrive(nb_ready(d), kNbReadyThreads);
       }
-      ++d_use[dbuf];
-      dbuf ^= 1;
-      ++seg;
-      ok = __all_sync(0xffffffffu, ok);
+      if (!seg_end) continue;
+      ok = ok && !*abort_flag;  // an aborted call stores nothing more
 
-      const int r0 = quad * 32 + lane, r1 = r0 + kTileRows;  // rows inside the row block
       const int64_t n0 = rb * kRowsPerBlock + r0, n1 = rb * kRowsPerBlock + r1;
       const int64_t pf = block_of_unit(rb * S, T, G), pl = block_of_unit(rb * S + S - 1, T, G);
       if (pf == pl) {
-        if (!ok) continue;
         // the whole K of this row block was summed here
+        if (ok) {
 #pragma unroll
-        for (int m = 0; m < kNmma; ++m) {
-          if (m < M) {
-            const float a0 = __uint_as_float(v0[m]) * xs_smem[m] * gs;
-            const float a1 = __uint_as_float(v1[m]) * xs_smem[m] * gs;
-            if (p.out_f32) {
-              float* y = static_cast<float*>(p.y) + (int64_t)m * p.N;
-              if (n0 < p.N) y[n0] = a0;
-              if (n1 < p.N) y[n1] = a1;
-            } else {
-              uint16_t* y = static_cast<uint16_t*>(p.y) + (int64_t)m * p.N;
-              if (n0 < p.N) y[n0] = ptx::f32_to_bf16_rn(a0);
-              if (n1 < p.N) y[n1] = ptx::f32_to_bf16_rn(a1);
+          for (int m = 0; m < NC; ++m) {
+            if (m < M) {
+              const float a0 = acc0[m] * gs, a1 = acc1[m] * gs;
+              if (p.out_f32) {
+                float* y = static_cast<float*>(p.y) + (int64_t)m * p.N;
+                if (n0 < p.N) y[n0] = a0;
+                if (n1 < p.N) y[n1] = a1;
+              } else {
+                uint16_t* y = static_cast<uint16_t*>(p.y) + (int64_t)m * p.N;
+                if (n0 < p.N) y[n0] = ptx::f32_to_bf16_rn(a0);
+                if (n1 < p.N) y[n1] = ptx::f32_to_bf16_rn(a1);
+              }
             }
           }
         }
@@ -503,10 +510,10 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
         const int slot = partial_slot(blockIdx.x, rb, T, G, S);
         float* part = p.partials + (int64_t)slot * (kNmma * kRowsPerBlock);
 #pragma unroll
-        for (int m = 0; m < kNmma; ++m) {
+        for (int m = 0; m < NC; ++m) {
           if (ok && m < M) {
-            part[m * kRowsPerBlock + r0] = __uint_as_float(v0[m]) * xs_smem[m];
-            part[m * kRowsPerBlock + r1] = __uint_as_float(v1[m]) * xs_smem[m];
+            part[m * kRowsPerBlock + r0] = acc0[m];
+            part[m * kRowsPerBlock + r1] = acc1[m];
           }
         }
         __threadfence();
@@ -514,6 +521,8 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
         if (etid == 0 && ok) atomicAdd(p.counters + rb, 1);  // release: every thread fenced its stores
         if (n_pend < 2) pend[n_pend++] = rb;
       }
+#pragma unroll
+      for (int m = 0; m < NC; ++m) acc0[m] = acc1[m] = 0.f;
     }
     // Split row blocks: wait until every contributing block has published its part, then add
     // this block's slice of the rows (part q of the block order is always added q-th).  Every
@@ -594,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, kTmemCols);
+  if (warp == kEpiWarp0) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace nvfp4
