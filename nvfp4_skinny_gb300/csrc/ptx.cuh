@@ -66,6 +66,20 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
 }
+// 16-byte asynchronous copy global -> shared through the load/store path (not the tensor-copy
+// engine, so it does not queue behind bulk copies); L2 only, with a cache policy.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most n (0 or 1) of this thread's committed groups are still in flight.
+__device__ __forceinline__ void cp_async_wait(int n) {
+  if (n == 0)
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+  else
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
 // 2-D tiled tensor copy global -> shared (box and swizzle from the tensor map); x is the
 // inner (byte) coordinate and must be a multiple of 16.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int32_t x, int32_t y, uint32_t bar,

@@ -8,7 +8,9 @@
 //                2-D tensor copies (TMA) of a 256-row x 256-k block of codes (128-byte swizzle)
 //                and of its block scales into a 4-stage shared-memory ring; the last decoder
 //                warp to take a stage's bytes into registers issues the stage's next copy;
-//   warps 8-11   activations and epilogue: bulk copies of the unit's bf16 activation rows,
+//   warps 8-11   activations and epilogue: 16-byte asynchronous copies of the unit's bf16
+//                activation rows (through the load/store path: a copy queued behind the
+//                weight stream in the tensor-copy engine would arrive microseconds late),
 //                conversion to fp16 times 2^e with e chosen per (row, unit) from the largest
 //                magnitude (exact for every element within 2^-33 of it), and after each unit:
 //                tensor memory -> registers, the unit's sums times 2^-e added to an fp32
@@ -86,13 +88,15 @@ constexpr int kSmemBar = kSmemXRaw + kXBufs * kXRawBytes;   // 214016
 constexpr int kBarFull = 0;                                  // [kStages]  weight copies (tx) -> decoders
 constexpr int kBarAEmpty = kBarFull + kStages;               // [half][tile]  MMA commit -> decoders
 constexpr int kBarUnit = kBarAEmpty + kHalves * kTiles;      // [kXBufs]   4 MMA commits -> epilogue
-constexpr int kBarXRaw = kBarUnit + kXBufs;                  // [kXBufs]   activation copies (tx)
-constexpr int kBarFinal = kBarXRaw + kXBufs;                 // [issuer]   MMA drain at exit
+constexpr int kBarFinal = kBarUnit + kXBufs;                 // [issuer]   MMA drain at exit
 constexpr int kNumBars = kBarFinal + kMmaWarps;
 constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
 // misc: +0 tensor-memory base, +4 abort flag, +8 fix-up flag, +16 stage release counts
-// [kStages], +128 xs[kXBufs][32] (2^-e), +384 xf[kXBufs][32][2] (2^e as two factors)
-constexpr int kSmemBytes = kSmemMisc + 1024 + 1024;  // misc + alignment slack
+// [kStages], +128 xs[kXsBufs][32] (2^-e of unit j in buffer j % 4), +640 partial row maxima
+// [2][epilogue warp][32] (unit j in buffer j % 2)
+constexpr int kXsBufs = 4;
+constexpr int kMiscBytes = 640 + 2 * 4 * 32 * 4;
+constexpr int kSmemBytes = kSmemMisc + kMiscBytes + 1024;  // misc + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory per block");
 
 // hardware named barriers (0 is __syncthreads)
@@ -131,9 +135,6 @@ struct MainParams {
 // ------------------------------------------------------------------ work split
 __device__ __forceinline__ int64_t unit_begin(int64_t p, int64_t T, int64_t G) { return p * T / G; }
 __device__ __forceinline__ int64_t block_of_unit(int64_t u, int64_t T, int64_t G) { return ((u + 1) * G - 1) / T; }
-__device__ __forceinline__ int partial_slot(int64_t p, int64_t rb, int64_t T, int64_t G, int64_t S) {
-  return (int)(2 * p + (rb == unit_begin(p, T, G) / S ? 0 : 1));
-}
 
 // ------------------------------------------------------------------ bounded waits
 struct Abort {
@@ -172,6 +173,40 @@ __device__ __forceinline__ float bf16x2_absmax(uint32_t w, float a) {
   return fmaxf(a, fabsf(__uint_as_float(w & 0xFFFF0000u)));
 }
 
+// e with amax * 2^e in [2^15, 2^16) (amax = f * 2^E, f in [0.5, 1): e = 16 - E); 0 when amax
+// is zero, infinite or NaN.  Integer work on the bits: exact, and no library call.
+__device__ __forceinline__ int x_exponent(float amax) {
+  const uint32_t b = __float_as_uint(amax);  // amax >= 0
+  const int ef = (int)(b >> 23);
+  if (b == 0u || ef >= 0xFF) return 0;
+  const int E = ef != 0 ? ef - 126 : (32 - __clz((int)b)) - 149;  // subnormal: b * 2^-149
+  return 16 - E;
+}
+// 2^k for -126 <= k <= 127.
+__device__ __forceinline__ float pow2i(int k) { return __uint_as_float((uint32_t)(k + 127) << 23); }
+
+// Per-half max(|a|, |b|) of two bf16 pairs (the sign of the result is not used).
+__device__ __forceinline__ uint32_t bf16x2_absmax2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bf16x8_absmax2(uint4 w, uint32_t acc) {
+  return bf16x2_absmax2(acc, bf16x2_absmax2(bf16x2_absmax2(w.x, w.y), bf16x2_absmax2(w.z, w.w)));
+}
+
+// 8 bf16 -> 8 fp16, each times f (a power of two).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, float f) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t r[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float lo = __uint_as_float(w[q] << 16) * f;
+    const float hi = __uint_as_float(w[q] & 0xFFFF0000u) * f;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r[q]) : "f"(hi), "f"(lo));
+  }
+  return make_uint4(r[0], r[1], r[2], r[3]);
+}
 // 8 bf16 -> 8 fp16, each times f1 * f2 (two factors: 2^e can exceed the float range).
 __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, float f1, float f2) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -221,8 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemMisc + 4);
   volatile int* fix_flag = reinterpret_cast<volatile int*>(smem + kSmemMisc + 8);
   int* release_cnt = reinterpret_cast<int*>(smem + kSmemMisc + 16);  // [kStages]
-  float* xs_smem = reinterpret_cast<float*>(smem + kSmemMisc + 128);  // [kXBufs][32]
-  float* xf_smem = reinterpret_cast<float*>(smem + kSmemMisc + 384);  // [kXBufs][32][2]
+  float* xs_smem = reinterpret_cast<float*>(smem + kSmemMisc + 128);  // [kXsBufs][32]
+  float* pmax_smem = reinterpret_cast<float*>(smem + kSmemMisc + 640);  // [2][kEpiWarps][32]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = ptx::smem_addr(smem);
@@ -232,13 +267,27 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
   const int64_t T = p.units, G = p.grid, S = p.S;
   const int64_t u_begin = unit_begin(blockIdx.x, T, G), u_end = unit_begin(blockIdx.x + 1, T, G);
   const int n_local = (int)(u_end - u_begin);
+  // (row block, k-step) of local unit i with 32-bit arithmetic (K <= 2^24, so S < 2^16)
+  const int64_t rb0 = u_begin / S;
+  const uint32_t s0 = (uint32_t)(u_begin - rb0 * S), S32 = (uint32_t)S;
+  auto unit_rb = [&](int i, int& ks) -> int64_t {
+    const uint32_t t = s0 + (uint32_t)i, q = t / S32;
+    ks = (int)(t - q * S32);
+    return rb0 + q;
+  };
+  auto unit_kstep = [&](int i) {
+    int ks;
+    (void)unit_rb(i, ks);
+    return ks;
+  };
 
   // ---- set-up: barriers, activation operands zeroed (rows >= M stay zero), tensor memory
   const uint64_t pol_w = ptx::policy_evict_first();
   // unit i's weights -> stage i % kStages (full boxes are always delivered: rows past N are
   // zero-filled); one thread issues
   auto issue_weights = [&](int i) {
-    const int64_t u = u_begin + i, rb = u / S, s = u % S;
+    int s;
+    const int64_t rb = unit_rb(i, s);
     const int st = i % kStages;
     const uint32_t stage = smem_base + (uint32_t)(st * kWStageBytes);
     const uint32_t fb = bar(kBarFull + st);
@@ -255,7 +304,6 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
     for (int a = 0; a < kHalves * kTiles; ++a) ptx::mbar_init(bar(kBarAEmpty + a), 1);
     for (int d = 0; d < kXBufs; ++d) {
       ptx::mbar_init(bar(kBarUnit + d), kMmaWarps);
-      ptx::mbar_init(bar(kBarXRaw + d), 1);
     }
     for (int q = 0; q < kMmaWarps; ++q) ptx::mbar_init(bar(kBarFinal + q), 1);
     *abort_flag = 0;
@@ -387,70 +435,78 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
     const uint64_t pol_x = ptx::policy_evict_last();
     const int64_t K = p.K;
 
-    // bf16 rows m < M of unit j's k-step -> raw buffer j % 2 (one 512-byte bulk copy per row)
+    // Epilogue warp ew owns the 16-byte chunks 8 ew .. 8 ew + 7 (k 64 ew .. 64 ew + 63 of the
+    // k-step) of every activation row; lane (r8 = lane % 8, cc = lane / 8) owns, in each row
+    // group g, row 8 g + r8, chunks 8 ew + cc and 8 ew + cc + 4.  A lane copies its chunks,
+    // reads them back and writes their fp16 values, so no thread reads another thread's copies;
+    // the four warps' partial row maxima meet in shared memory behind one barrier per unit.
+    const int groups = (M + 7) >> 3;
+    const int r8 = lane & 7, cc = lane >> 3;
+    // unit j's k-step of the warp's chunks -> raw buffer j % 2; one commit group per unit
     auto issue_x = [&](int j) {
       const int d = j & 1;
-      const int64_t s = (u_begin + j) % S;
-      const uint32_t xb = bar(kBarXRaw + d);
-      ptx::mbar_arrive_expect_tx(xb, (uint32_t)(M * kKStep * 2));
-      for (int m = 0; m < M; ++m)
-        ptx::bulk_g2s(smem_base + (uint32_t)(kSmemXRaw + d * kXRawBytes + m * kXRawPitch), p.x + m * K + s * kKStep,
-                      (uint32_t)(kKStep * 2), xb, pol_x);
-    };
-    // raw buffer j % 2 -> fp16 operand buffer j % 2, 2^-e -> xs; ends with a barrier of the 4 warps
-    auto convert = [&](int j) {
-      const int d = j & 1;
-      const bool xok = __all_sync(0xffffffffu, wait_bar(bar(kBarXRaw + d), (uint32_t)((j >> 1) & 1), ab));
-      const uint8_t* raw = smem + kSmemXRaw + d * kXRawBytes;
-      uint8_t* x16 = smem + kSmemX16 + d * kX16Bytes;
-      float* xs = xs_smem + d * kNmma;
-      float* xf = xf_smem + d * kNmma * 2;
-      // pass 1: one warp per row, e from the row's largest magnitude in this k-step
-      if (xok) {
-        for (int m = ew; m < M; m += kEpiWarps) {
-          const uint4 w = *reinterpret_cast<const uint4*>(raw + m * kXRawPitch + lane * 16);
-          float amax = bf16x2_absmax(w.x, bf16x2_absmax(w.y, bf16x2_absmax(w.z, bf16x2_absmax(w.w, 0.f))));
+      const int s = unit_kstep(j);
+      const uint32_t raw = smem_base + (uint32_t)(kSmemXRaw + d * kXRawBytes);
+      for (int g = 0; g < groups; ++g) {
+        const int m = g * 8 + r8;
+        if (m < M) {
+          const uint16_t* src = p.x + m * K + (int64_t)s * kKStep;
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-          if (lane == 0) {
-            // amax = f * 2^E, f in [0.5, 1): e = 16 - E puts amax * 2^e in [2^15, 2^16)
-            int e = 0;
-            if (amax > 0.f && amax <= 3.4028234663852886e38f) {
-              int E;
-              (void)frexpf(amax, &E);
-              e = 16 - E;
-            }
-            const int e1 = e / 2, e2 = e - e1;
-            xf[2 * m] = ldexpf(1.f, e1);
-            xf[2 * m + 1] = ldexpf(1.f, e2);
-            xs[m] = ldexpf(1.f, -e);
+          for (int k = 0; k < 2; ++k) {
+            const int c = 8 * ew + cc + 4 * k;
+            ptx::cp_async16(raw + (uint32_t)(m * kXRawPitch + c * 16), src + c * 8, pol_x);
           }
         }
       }
+      ptx::cp_async_commit();
+    };
+    // raw buffer j % 2 -> fp16 operand buffer j % 2 and 2^-e -> xs buffer j % 4.  Groups are
+    // committed in unit order and unit j + 1's may be the only younger one.
+    auto convert = [&](int j) {
+      const int d = j & 1;
+      ptx::cp_async_wait(j + 1 < n_local ? 1 : 0);
+      const uint8_t* raw = smem + kSmemXRaw + d * kXRawBytes;
+      uint8_t* x16 = smem + kSmemX16 + d * kX16Bytes;
+      float* xs = xs_smem + (j & (kXsBufs - 1)) * kNmma;
+      float* pm = pmax_smem + d * (kEpiWarps * kNmma);
+      // pass 1: this warp's maximum magnitude of each row over its 8 chunks
+      for (int g = 0; g < groups; ++g) {
+        const int m = g * 8 + r8;
+        uint32_t a2 = 0u;
+        if (m < M) {
+#pragma unroll
+          for (int k = 0; k < 2; ++k)
+            a2 = bf16x8_absmax2(*reinterpret_cast<const uint4*>(raw + m * kXRawPitch + (8 * ew + cc + 4 * k) * 16), a2);
+        }
+        float a = fmaxf(fabsf(__uint_as_float(a2 << 16)), fabsf(__uint_as_float(a2 & 0xFFFF0000u)));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));  // the 4 lanes of row r8
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 16));
+        if (cc == 0 && m < M) pm[ew * kNmma + m] = a;
+      }
       ptx::named_bar_sync(kNbEpi, kEpiWarps * 32);
-      // pass 2: lane = (row r = lane % 8, chunk c = 4 cb + lane / 8) of a row group; each warp
-      // writes 512 contiguous bytes of the operand layout
-      if (xok) {
-        const int items = ((M + 7) >> 3) * 8;
-        for (int it = ew; it < items; it += kEpiWarps) {
-          const int g = it >> 3, cb = it & 7;
-          const int m = g * 8 + (lane & 7), c = cb * 4 + (lane >> 3);
-          if (m < M) {
+      // pass 2: the row's exponent from the 4 partial maxima, then this lane's chunks
+      for (int g = 0; g < groups; ++g) {
+        const int m = g * 8 + r8;
+        if (m < M) {
+          const float amax = fmaxf(fmaxf(pm[m], pm[kNmma + m]), fmaxf(pm[2 * kNmma + m], pm[3 * kNmma + m]));
+          const int e = x_exponent(amax);  // -112 <= e <= 148 for bf16 data
+          if (ew == 0 && cc == 0) xs[m] = pow2i(-(e / 2)) * pow2i(-(e - e / 2));  // 2^-e, exact
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int c = 8 * ew + cc + 4 * k;
             const uint4 w = *reinterpret_cast<const uint4*>(raw + m * kXRawPitch + c * 16);
-            *reinterpret_cast<uint4*>(x16 + g * kXGroupBytes + c * 128 + (m & 7) * 16) =
-                bf16x8_to_f16x8(w, xf[2 * m], xf[2 * m + 1]);
+            *reinterpret_cast<uint4*>(x16 + g * kXGroupBytes + c * 128 + r8 * 16) =
+                e <= 127 ? bf16x8_to_f16x8(w, pow2i(e)) : bf16x8_to_f16x8(w, pow2i(e / 2), pow2i(e - e / 2));
           }
         }
       }
       ptx::fence_proxy_async_smem();  // operand writes -> the tensor core's (async proxy) reads
-      ptx::named_bar_sync(kNbEpi, kEpiWarps * 32);
     };
 
-    if (etid == 0)
-      for (int j = 0; j < kXBufs && j < n_local; ++j) issue_x(j);
+    for (int j = 0; j < kXBufs && j < n_local; ++j) issue_x(j);
     for (int j = 0; j < kXBufs && j < n_local; ++j) {
       convert(j);
-      if (etid == 0 && j + kXBufs < n_local) issue_x(j + kXBufs);
+      if (j + kXBufs < n_local) issue_x(j + kXBufs);
       ptx::named_bar_arrive(nb_ready(j), kNbReadyThreads);
     }
 
@@ -463,22 +519,24 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
     const int r0 = quad * 32 + lane, r1 = r0 + kTileRows;  // rows inside the row block
     for (int i = 0; i < n_local; ++i) {
       const int d = i & 1;
-      const int64_t u = u_begin + i, rb = u / S, s = u % S;
-      const bool seg_end = (i == n_local - 1) || (s == S - 1);
+      int s;
+      const int64_t rb = unit_rb(i, s);
+      const bool seg_end = (i == n_local - 1) || (s == (int)S - 1);
       // unit i's MMAs complete: D(d) final and activation buffer d free; gates a ready arrival,
       // so the wait ignores the abort flag
       const bool full = wait_bar(bar(kBarUnit + d), (uint32_t)((i >> 1) & 1), ab, false);
       ok = __all_sync(0xffffffffu, ok && full);
       ptx::tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16);
-      const float* xs = xs_smem + d * kNmma;
+      const float* xs = xs_smem + (i & (kXsBufs - 1)) * kNmma;
       drain_tile(acc0, taddr + d_col(d, 0, 0), taddr + d_col(d, 0, 1), xs);
       drain_tile(acc1, taddr + d_col(d, 1, 0), taddr + d_col(d, 1, 1), xs);
       ptx::tc_fence_before();
-      ptx::named_bar_sync(kNbEpi, kEpiWarps * 32);  // D(d) and xs[d] read by every epilogue thread
+      // xs of unit i + 2 goes to another buffer than the one just read, and D(d) is rewritten only
+      // after every epilogue warp has arrived below: no barrier among the epilogue warps here
       if (i + kXBufs < n_local) {
         convert(i + kXBufs);
-        if (etid == 0 && i + 2 * kXBufs < n_local) issue_x(i + 2 * kXBufs);
+        if (i + 2 * kXBufs < n_local) issue_x(i + 2 * kXBufs);
         ptx::named_bar_arrive(nb_ready(d), kNbReadyThreads);
       }
       if (!seg_end) continue;
@@ -507,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
         }
       } else {
         // split row block: publish this part; the sums are formed after the main loop
-        const int slot = partial_slot(blockIdx.x, rb, T, G, S);
+        const int slot = (int)(2 * blockIdx.x) + (rb == rb0 ? 0 : 1);  // first or last row block of the range
         float* part = p.partials + (int64_t)slot * (kNmma * kRowsPerBlock);
 #pragma unroll
         for (int m = 0; m < NC; ++m) {
@@ -548,40 +606,54 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
       if (*fix_flag) {
         __threadfence();
         const int q = (int)(blockIdx.x - pf);
+        // part slot of block b: 2 b for every b > pf (rb is the first row block of its range);
+        // block pf used slot 2 pf + 1 if its range began in an earlier row block
+        const int pf_bit = unit_begin(pf, T, G) < rb * S ? 1 : 0;
         // this block's slice: whole groups of 4 rows (the 64 groups of the row block split over nseg)
         const int g_lo = q * (kRowsPerBlock / 4) / nseg, g_hi = (q + 1) * (kRowsPerBlock / 4) / nseg;
         const int groups = g_hi - g_lo;
-        for (int o = etid; o < groups * M; o += kEpiWarps * 32) {
-          const int r = 4 * (g_lo + o % groups), m = o / groups;
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          // up to 8 parts in flight at once, added strictly in block order
-          for (int64_t q0 = pf; q0 <= pl; q0 += 8) {
-            float4 t[8];
+        // The slice's items (4 rows x 1 activation row) are the thread's work list, item-major and
+        // part-minor: each item's parts are added strictly in block order.  16 loads are issued
+        // before any is used, whatever the mix of items and parts.
+        const int n_items = groups * M;
+        const int my_items = n_items > etid ? (n_items - etid + kEpiWarps * 32 - 1) / (kEpiWarps * 32) : 0;
+        const int n_work = my_items * nseg;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int w0 = 0; w0 < n_work; w0 += 16) {
+          float4 t[16];
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              if (q0 + j <= pl)
-                t[j] = __ldcg(reinterpret_cast<const float4*>(
-                    p.partials + (int64_t)partial_slot(q0 + j, rb, T, G, S) * (kNmma * kRowsPerBlock) +
-                    m * kRowsPerBlock + r));
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              if (q0 + j <= pl) {
-                acc.x += t[j].x;
-                acc.y += t[j].y;
-                acc.z += t[j].z;
-                acc.w += t[j].w;
-              }
+          for (int j = 0; j < 16; ++j) {
+            const int w = w0 + j;
+            if (w < n_work) {
+              const int o = etid + (w / nseg) * (kEpiWarps * 32), b = (int)pf + w % nseg;
+              const float* part = p.partials + (int64_t)(2 * b + (b == pf ? pf_bit : 0)) * (kNmma * kRowsPerBlock);
+              t[j] = __ldcg(reinterpret_cast<const float4*>(part + (o / groups) * kRowsPerBlock + 4 * (g_lo + o % groups)));
             }
           }
-          const float v[4] = {acc.x * gs, acc.y * gs, acc.z * gs, acc.w * gs};
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int64_t n = rb * kRowsPerBlock + r + c;
-            if (n < p.N) {
-              if (p.out_f32)
-                static_cast<float*>(p.y)[(int64_t)m * p.N + n] = v[c];
-              else
-                static_cast<uint16_t*>(p.y)[(int64_t)m * p.N + n] = ptx::f32_to_bf16_rn(v[c]);
+          for (int j = 0; j < 16; ++j) {
+            const int w = w0 + j;
+            if (w < n_work) {
+              acc.x += t[j].x;
+              acc.y += t[j].y;
+              acc.z += t[j].z;
+              acc.w += t[j].w;
+              if (w % nseg == nseg - 1) {  // the item's last part: store it
+                const int o = etid + (w / nseg) * (kEpiWarps * 32);
+                const int m = o / groups, r = 4 * (g_lo + o % groups);
+                const float v[4] = {acc.x * gs, acc.y * gs, acc.z * gs, acc.w * gs};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                  const int64_t n = rb * kRowsPerBlock + r + c;
+                  if (n < p.N) {
+                    if (p.out_f32)
+                      static_cast<float*>(p.y)[(int64_t)m * p.N + n] = v[c];
+                    else
+                      static_cast<uint16_t*>(p.y)[(int64_t)m * p.N + n] = ptx::f32_to_bf16_rn(v[c]);
+                  }
+                }
+                acc = make_float4(0.f, 0.f, 0.f, 0.f);
+              }
             }
           }
         }
