@@ -38,6 +38,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// One poll that may suspend the thread until the phase completes or about `hint_ns`
+// nanoseconds have passed, so a waiting warp does not take issue slots from the others.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // ---------------------------------------------------------------- fences / proxies
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -73,12 +85,17 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64
                : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// Wait until at most n (0 or 1) of this thread's committed groups are still in flight.
+// Wait until at most n (0..3; larger counts as 3) of this thread's committed groups are still
+// in flight.
 __device__ __forceinline__ void cp_async_wait(int n) {
-  if (n == 0)
+  if (n <= 0)
     asm volatile("cp.async.wait_group 0;" ::: "memory");
-  else
+  else if (n == 1)
     asm volatile("cp.async.wait_group 1;" ::: "memory");
+  else if (n == 2)
+    asm volatile("cp.async.wait_group 2;" ::: "memory");
+  else
+    asm volatile("cp.async.wait_group 3;" ::: "memory");
 }
 // 2-D tiled tensor copy global -> shared (box and swizzle from the tensor map); x is the
 // inner (byte) coordinate and must be a multiple of 16.
@@ -203,6 +220,11 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* ptr) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
   return v;
+}
+
+// Add to a global int with release semantics at GPU scope, without waiting for the result.
+__device__ __forceinline__ void red_release_gpu_add(int* ptr, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
 }
 
 // fp32 -> bfloat16 bits, round to nearest even.

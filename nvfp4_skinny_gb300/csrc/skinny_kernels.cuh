@@ -574,100 +574,105 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
             part[m * kRowsPerBlock + r1] = acc1[m];
           }
         }
-        __threadfence();
+        // the barrier orders every thread's stores before thread 0's release (cumulative)
         ptx::named_bar_sync(kNbEpi, kEpiWarps * 32);
-        if (etid == 0 && ok) atomicAdd(p.counters + rb, 1);  // release: every thread fenced its stores
+        if (etid == 0 && ok) ptx::red_release_gpu_add(p.counters + rb, 1);
         if (n_pend < 2) pend[n_pend++] = rb;
       }
 #pragma unroll
       for (int m = 0; m < NC; ++m) acc0[m] = acc1[m] = 0.f;
     }
-    // Split row blocks: wait until every contributing block has published its part, then add
-    // this block's slice of the rows (part q of the block order is always added q-th).  Every
-    // block publishes all of its parts before it waits here, so the waits end.
+    // Split row blocks: wait until every contributing block has published its parts of both
+    // pending row blocks at once, then add this block's slice of the rows (part q of the block
+    // order is always added q-th).  Every block publishes all of its parts before it waits
+    // here, so the waits end.  Once a block has seen all parts it counts itself done; the last
+    // block of a row block to do so clears its counters (no block polls them any more).
+    int64_t pfs[2] = {0, 0}, pls[2] = {0, 0};
     for (int k = 0; k < n_pend; ++k) {
-      const int64_t rb = pend[k];
-      const int64_t pf = block_of_unit(rb * S, T, G), pl = block_of_unit(rb * S + S - 1, T, G);
-      const int nseg = (int)(pl - pf + 1);
+      pfs[k] = block_of_unit(pend[k] * S, T, G);
+      pls[k] = block_of_unit(pend[k] * S + S - 1, T, G);
+    }
+    if (n_pend > 0) {
       if (etid == 0) {
-        bool arrived = ptx::ld_acquire_gpu(p.counters + rb) >= nseg;
+        bool arrived[2] = {n_pend < 1, n_pend < 2};
         const long long t0 = clock64();
-        while (!arrived && !*abort_flag) {
-          __nanosleep(64);
-          arrived = ptx::ld_acquire_gpu(p.counters + rb) >= nseg;
-          if (!arrived && clock64() - t0 > kWaitLimitCycles) {
+        while (!(arrived[0] && arrived[1]) && !*abort_flag) {
+          for (int k = 0; k < n_pend; ++k)
+            if (!arrived[k]) arrived[k] = ptx::ld_acquire_gpu(p.counters + pend[k]) >= (int)(pls[k] - pfs[k] + 1);
+          if (!(arrived[0] && arrived[1]) && clock64() - t0 > kWaitLimitCycles) {
             *abort_flag = 1;
             atomicOr(p.err, kErrTimeout);
           }
         }
-        *fix_flag = arrived ? 1 : 0;
-      }
-      ptx::named_bar_sync(kNbEpi, kEpiWarps * 32);
-      if (*fix_flag) {
-        __threadfence();
-        const int q = (int)(blockIdx.x - pf);
-        // part slot of block b: 2 b for every b > pf (rb is the first row block of its range);
-        // block pf used slot 2 pf + 1 if its range began in an earlier row block
-        const int pf_bit = unit_begin(pf, T, G) < rb * S ? 1 : 0;
-        // this block's slice: whole groups of 4 rows (the 64 groups of the row block split over nseg)
-        const int g_lo = q * (kRowsPerBlock / 4) / nseg, g_hi = (q + 1) * (kRowsPerBlock / 4) / nseg;
-        const int groups = g_hi - g_lo;
-        // The slice's items (4 rows x 1 activation row) are the thread's work list, item-major and
-        // part-minor: each item's parts are added strictly in block order.  16 loads are issued
-        // before any is used, whatever the mix of items and parts.
-        const int n_items = groups * M;
-        const int my_items = n_items > etid ? (n_items - etid + kEpiWarps * 32 - 1) / (kEpiWarps * 32) : 0;
-        const int n_work = my_items * nseg;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int w0 = 0; w0 < n_work; w0 += 16) {
-          float4 t[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int w = w0 + j;
-            if (w < n_work) {
-              const int o = etid + (w / nseg) * (kEpiWarps * 32), b = (int)pf + w % nseg;
-              const float* part = p.partials + (int64_t)(2 * b + (b == pf ? pf_bit : 0)) * (kNmma * kRowsPerBlock);
-              t[j] = __ldcg(reinterpret_cast<const float4*>(part + (o / groups) * kRowsPerBlock + 4 * (g_lo + o % groups)));
+        const bool all = arrived[0] && arrived[1];
+        *fix_flag = all ? 1 : 0;
+        if (all) {
+          for (int k = 0; k < n_pend; ++k) {
+            const int64_t rb = pend[k];
+            if (atomicAdd(p.counters + p.row_blocks + rb, 1) == (int)(pls[k] - pfs[k])) {
+              p.counters[rb] = 0;
+              p.counters[p.row_blocks + rb] = 0;
             }
           }
+        }
+      }
+      ptx::named_bar_sync(kNbEpi, kEpiWarps * 32);  // orders the acquire before every thread's loads
+    }
+    for (int k = 0; k < n_pend && *fix_flag; ++k) {
+      const int64_t rb = pend[k], pf = pfs[k], pl = pls[k];
+      const int nseg = (int)(pl - pf + 1);
+      const int q = (int)(blockIdx.x - pf);
+      // part slot of block b: 2 b for every b > pf (rb is the first row block of its range);
+      // block pf used slot 2 pf + 1 if its range began in an earlier row block
+      const int pf_bit = unit_begin(pf, T, G) < rb * S ? 1 : 0;
+      // this block's slice: whole groups of 4 rows (the 64 groups of the row block split over nseg)
+      const int g_lo = q * (kRowsPerBlock / 4) / nseg, g_hi = (q + 1) * (kRowsPerBlock / 4) / nseg;
+      const int groups = g_hi - g_lo;
+      // The slice's items (4 rows x 1 activation row) are the thread's work list, item-major and
+      // part-minor: each item's parts are added strictly in block order.  16 loads are issued
+      // before any is used, whatever the mix of items and parts.
+      const int n_items = groups * M;
+      const int my_items = n_items > etid ? (n_items - etid + kEpiWarps * 32 - 1) / (kEpiWarps * 32) : 0;
+      const int n_work = my_items * nseg;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int w0 = 0; w0 < n_work; w0 += 16) {
+        float4 t[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int w = w0 + j;
-            if (w < n_work) {
-              acc.x += t[j].x;
-              acc.y += t[j].y;
-              acc.z += t[j].z;
-              acc.w += t[j].w;
-              if (w % nseg == nseg - 1) {  // the item's last part: store it
-                const int o = etid + (w / nseg) * (kEpiWarps * 32);
-                const int m = o / groups, r = 4 * (g_lo + o % groups);
-                const float v[4] = {acc.x * gs, acc.y * gs, acc.z * gs, acc.w * gs};
+        for (int j = 0; j < 16; ++j) {
+          const int w = w0 + j;
+          if (w < n_work) {
+            const int o = etid + (w / nseg) * (kEpiWarps * 32), b = (int)pf + w % nseg;
+            const float* part = p.partials + (int64_t)(2 * b + (b == pf ? pf_bit : 0)) * (kNmma * kRowsPerBlock);
+            t[j] = __ldcg(reinterpret_cast<const float4*>(part + (o / groups) * kRowsPerBlock + 4 * (g_lo + o % groups)));
+          }
+        }
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                  const int64_t n = rb * kRowsPerBlock + r + c;
-                  if (n < p.N) {
-                    if (p.out_f32)
-                      static_cast<float*>(p.y)[(int64_t)m * p.N + n] = v[c];
-                    else
-                      static_cast<uint16_t*>(p.y)[(int64_t)m * p.N + n] = ptx::f32_to_bf16_rn(v[c]);
-                  }
+        for (int j = 0; j < 16; ++j) {
+          const int w = w0 + j;
+          if (w < n_work) {
+            acc.x += t[j].x;
+            acc.y += t[j].y;
+            acc.z += t[j].z;
+            acc.w += t[j].w;
+            if (w % nseg == nseg - 1) {  // the item's last part: store it
+              const int o = etid + (w / nseg) * (kEpiWarps * 32);
+              const int m = o / groups, r = 4 * (g_lo + o % groups);
+              const float v[4] = {acc.x * gs, acc.y * gs, acc.z * gs, acc.w * gs};
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                const int64_t n = rb * kRowsPerBlock + r + c;
+                if (n < p.N) {
+                  if (p.out_f32)
+                    static_cast<float*>(p.y)[(int64_t)m * p.N + n] = v[c];
+                  else
+                    static_cast<uint16_t*>(p.y)[(int64_t)m * p.N + n] = ptx::f32_to_bf16_rn(v[c]);
                 }
-                acc = make_float4(0.f, 0.f, 0.f, 0.f);
               }
+              acc = make_float4(0.f, 0.f, 0.f, 0.f);
             }
           }
         }
       }
-      ptx::named_bar_sync(kNbEpi, kEpiWarps * 32);
-      // the last block to finish this row block clears its counters for the next call
-      if (etid == 0 && *fix_flag) {
-        const int done = atomicAdd(p.counters + p.row_blocks + rb, 1);
-        if (done == nseg - 1) {
-          p.counters[rb] = 0;
-          p.counters[p.row_blocks + rb] = 0;
-        }
-      }
-      ptx::named_bar_sync(kNbEpi, kEpiWarps * 32);
     }
   }
 
