@@ -628,48 +628,53 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
       // this block's slice: whole groups of 4 rows (the 64 groups of the row block split over nseg)
       const int g_lo = q * (kRowsPerBlock / 4) / nseg, g_hi = (q + 1) * (kRowsPerBlock / 4) / nseg;
       const int groups = g_hi - g_lo;
-      // The slice's items (4 rows x 1 activation row) are the thread's work list, item-major and
-      // part-minor: each item's parts are added strictly in block order.  16 loads are issued
-      // before any is used, whatever the mix of items and parts.
+      // The slice's items (4 rows x 1 activation row): this thread takes items etid, etid + 128,
+      // ...; for each, the parts' loads (16 at a time) are all issued before any is used, and
+      // the parts are added strictly in block order.
       const int n_items = groups * M;
-      const int my_items = n_items > etid ? (n_items - etid + kEpiWarps * 32 - 1) / (kEpiWarps * 32) : 0;
-      const int n_work = my_items * nseg;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int w0 = 0; w0 < n_work; w0 += 16) {
-        float4 t[16];
+      for (int o = etid; o < n_items; o += kEpiWarps * 32) {
+        const int m = o / groups, r = 4 * (g_lo + o % groups);
+        const float* base = p.partials + m * kRowsPerBlock + r;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int b0 = 0; b0 < nseg; b0 += 16) {
+          float4 t[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int w = w0 + j;
-          if (w < n_work) {
-            const int o = etid + (w / nseg) * (kEpiWarps * 32), b = (int)pf + w % nseg;
-            const float* part = p.partials + (int64_t)(2 * b + (b == pf ? pf_bit : 0)) * (kNmma * kRowsPerBlock);
-            t[j] = __ldcg(reinterpret_cast<const float4*>(part + (o / groups) * kRowsPerBlock + 4 * (g_lo + o % groups)));
+          for (int j = 0; j < 16; ++j) {
+            if (b0 + j < nseg) {
+              const int64_t b = pf + b0 + j;
+              t[j] = __ldcg(reinterpret_cast<const float4*>(
+                  base + (2 * b + (b == pf ? pf_bit : 0)) * (int64_t)(kNmma * kRowsPerBlock)));
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (b0 + j < nseg) {
+              acc.x += t[j].x;
+              acc.y += t[j].y;
+              acc.z += t[j].z;
+              acc.w += t[j].w;
+            }
           }
         }
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int w = w0 + j;
-          if (w < n_work) {
-            acc.x += t[j].x;
-            acc.y += t[j].y;
-            acc.z += t[j].z;
-            acc.w += t[j].w;
-            if (w % nseg == nseg - 1) {  // the item's last part: store it
-              const int o = etid + (w / nseg) * (kEpiWarps * 32);
-              const int m = o / groups, r = 4 * (g_lo + o % groups);
-              const float v[4] = {acc.x * gs, acc.y * gs, acc.z * gs, acc.w * gs};
-#pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                const int64_t n = rb * kRowsPerBlock + r + c;
-                if (n < p.N) {
-                  if (p.out_f32)
-                    static_cast<float*>(p.y)[(int64_t)m * p.N + n] = v[c];
-                  else
-                    static_cast<uint16_t*>(p.y)[(int64_t)m * p.N + n] = ptx::f32_to_bf16_rn(v[c]);
-                }
-              }
-              acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+        const float v[4] = {acc.x * gs, acc.y * gs, acc.z * gs, acc.w * gs};
+        const int64_t n = rb * kRowsPerBlock + r;
+        if (p.out_f32) {
+          float* yrow = static_cast<float*>(p.y) + (int64_t)m * p.N;
+          if (n + 3 < p.N && (p.N & 3) == 0) {
+            *reinterpret_cast<float4*>(yrow + n) = make_float4(v[0], v[1], v[2], v[3]);
+          } else {
+            for (int c = 0; c < 4; ++c)
+              if (n + c < p.N) yrow[n + c] = v[c];
+          }
+        } else {
+          uint16_t* yrow = static_cast<uint16_t*>(p.y) + (int64_t)m * p.N;
+          if (n + 3 < p.N && (p.N & 3) == 0) {
+            const uint32_t lo = (uint32_t)ptx::f32_to_bf16_rn(v[0]) | ((uint32_t)ptx::f32_to_bf16_rn(v[1]) << 16);
+            const uint32_t hi = (uint32_t)ptx::f32_to_bf16_rn(v[2]) | ((uint32_t)ptx::f32_to_bf16_rn(v[3]) << 16);
+            *reinterpret_cast<uint2*>(yrow + n) = make_uint2(lo, hi);
+          } else {
+            for (int c = 0; c < 4; ++c)
+              if (n + c < p.N) yrow[n + c] = ptx::f32_to_bf16_rn(v[c]);
           }
         }
       }
