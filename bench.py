@@ -34,7 +34,7 @@ L2_BYTES = 129 * 1000 * 1000
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ("nvfp4_skinny_gb300/csrc/nvfp4_skinny.cu", "nvfp4_skinny_gb300/csrc/skinny_kernels.cuh",
                   "nvfp4_skinny_gb300/csrc/ptx.cuh")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "skinny_kernel_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "skinny_kernel_square5120_m16.md")
 
 
 def call_bytes(N, K, M, out_bytes=2):
@@ -59,18 +59,22 @@ def hbm_peak():
 
 
 def recorded_traffic(N, K, M):
-    """DRAM bytes per launch of the main kernel from a committed ncu summary, if it was
-    taken on the current kernel sources for this shape and M; else None."""
+    """DRAM bytes per launch of the main kernel from the committed ncu summary (its
+    `traffic-record:` line), if it was taken on the current kernel sources for this shape
+    and M; else None."""
     try:
         with open(TRAFFIC_FILE) as f:
-            rec = json.load(f)
+            lines = [ln for ln in f if ln.startswith("traffic-record:")]
     except Exception:
         return None
-    if rec.get("kernel_source_hash") != kernel_source_hash():
-        return None
-    for e in rec.get("launches", []):
-        if e.get("N") == N and e.get("K") == K and e.get("M") == M:
-            return e.get("dram_bytes_per_launch")
+    for ln in lines:
+        rec = dict(kv.split("=", 1) for kv in ln.split()[1:] if "=" in kv)
+        try:
+            if (rec.get("kernel_source_hash") == kernel_source_hash() and int(rec["N"]) == N
+                    and int(rec["K"]) == K and int(rec["M"]) == M):
+                return int(rec["dram_bytes_per_launch"])
+        except (KeyError, ValueError):
+            continue
     return None
 
 
@@ -225,11 +229,11 @@ def run_ours(args, rank, world):
     total_ms = max_over_ranks(total_ms, world)
     bytes_per_step = sum(step_bytes.values())
     value = bytes_per_step * args.steps * world / (total_ms * 1e-3) / 1e9
-    launches_per_step = 2 * copies * len(HEAD_MS)
+    launches_per_step = copies * len(HEAD_MS)  # one skinny_kernel launch per call
 
     per_m = {}
     for M in HEAD_MS:
-        t_call = per_m_ms[M] / (args.steps * copies)  # ms per call (both kernels)
+        t_call = per_m_ms[M] / (args.steps * copies)  # ms per call
         gbs = call_bytes(sq.N, sq.K, M) / (t_call * 1e-3) / 1e9
         per_m[str(M)] = {"us_per_call": round(t_call * 1e3, 3), "GBps": round(gbs, 1),
                          "frac_of_peak": round(gbs / peak, 4)}
@@ -241,6 +245,8 @@ def run_ours(args, rank, world):
     traffic = recorded_traffic(sq.N, sq.K, 16)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
+                "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one M=16 launch "
+                                  "(profiles/skinny_kernel_square5120_m16.md); null once the kernel sources change",
                 "algorithmic_bytes_per_launch": int(avg_bytes), "peak_source": peak_src,
                 "timing": "CUDA events on the launching stream over the timed region; a call is one "
                           "skinny_kernel launch (back-to-back launches overlap through PDL)"}
