@@ -221,8 +221,9 @@ def run_ours(args, rank, world):
     barrier(world)
     clk = clocks.stop()
     total_ms = t_start.elapsed_time(t_stop)
-    per_m_ms = {M: sum(events[k][j].elapsed_time(events[k][j + 1]) for k in range(args.steps))
-                for j, M in enumerate(HEAD_MS)}
+    step_m_ms = {M: [events[k][j].elapsed_time(events[k][j + 1]) for k in range(args.steps)]
+                 for j, M in enumerate(HEAD_MS)}
+    per_m_ms = {M: sum(v) for M, v in step_m_ms.items()}
     status = nb.nvfp4_plan_check(proj.plan, stream)
     if status != nb.NVFP4_OK:
         raise RuntimeError("kernel reported %s in the timed region" % nb.nvfp4_status_string(status))
@@ -235,8 +236,11 @@ def run_ours(args, rank, world):
     for M in HEAD_MS:
         t_call = per_m_ms[M] / (args.steps * copies)  # ms per call
         gbs = call_bytes(sq.N, sq.K, M) / (t_call * 1e-3) / 1e9
+        q = statistics.quantiles([v / copies * 1e3 for v in step_m_ms[M]], n=10) if args.steps > 1 else None
         per_m[str(M)] = {"us_per_call": round(t_call * 1e3, 3), "GBps": round(gbs, 1),
-                         "frac_of_peak": round(gbs / peak, 4)}
+                         "frac_of_peak": round(gbs / peak, 4),
+                         "us_per_call_p10_p50_p90_over_steps": [round(q[0], 3), round(q[4], 3), round(q[8], 3)] if q
+                         else None}
 
     # roofline of the dominant kernel: algorithmic bytes per call / average call time over the timed region
     avg_call_ms = total_ms / (args.steps * copies * len(HEAD_MS))

@@ -188,6 +188,32 @@ def test_back_to_back_different_plans():
         assert torch.equal(queued[i + len(shapes)], alone[i])
 
 
+# ------------------------------------------------------------------ N-sharding (replicas path)
+
+@pytest.mark.parametrize("cuts", [(2560,), (2000, 3100)])
+def test_n_shards_of_one_weight(cuts):
+    """The projection shards along N with no exchange: each shard is a plain call on a row
+    slice of the same weight (views into the packed arrays, no copies), and its output meets
+    the tolerance against the oracle on the whole slice.  Bitwise equality with the unsharded
+    call is not claimed: how K is split among blocks follows (N, K), so a shard of another N
+    may sum the same terms in another order."""
+    N, K, M = 5120, 5120, 16
+    case = Case(N, K, M, seed=12)
+    y_full = case.run(_plan(N, K))
+    bounds = (0,) + tuple(cuts) + (N,)
+    y_ref, absdot = case.oracle_full()
+    for n0, n1 in zip(bounds[:-1], bounds[1:]):
+        plan = _plan(n1 - n0, K)
+        y = torch.empty((M, n1 - n0), dtype=torch.bfloat16, device="cuda")
+        nb.nvfp4_skinny_linear(plan, case.d_x, M, case.d_codes[n0:n1], case.d_scales[n0:n1], case.gs, y)
+        torch.cuda.synchronize()
+        assert nb.nvfp4_plan_check(plan) == nb.NVFP4_OK
+        ok, ratio = within_tolerance(to_f64(y), y_ref[:, n0:n1], absdot[:, n0:n1])
+        assert ok, (n0, n1, ratio)
+    ok, ratio = within_tolerance(to_f64(y_full), y_ref, absdot)
+    assert ok, ratio
+
+
 # ------------------------------------------------------------------ full-size workloads, sampled
 
 def _sampled(case, plan, M, n_samples=384, seed=0):
