@@ -230,7 +230,7 @@ def run_ours(args, rank, world):
     total_ms = max_over_ranks(total_ms, world)
     bytes_per_step = sum(step_bytes.values())
     value = bytes_per_step * args.steps * world / (total_ms * 1e-3) / 1e9
-    launches_per_step = copies * len(HEAD_MS)  # one skinny_kernel launch per call
+    launches_per_step = copies * len(HEAD_MS) * nb.nvfp4_plan_get_info(proj.plan)["launches_per_call"]
 
     per_m = {}
     for M in HEAD_MS:
@@ -252,8 +252,9 @@ def run_ours(args, rank, world):
                 "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one M=16 launch "
                                   "(profiles/skinny_kernel_square5120_m16.md); null once the kernel sources change",
                 "algorithmic_bytes_per_launch": int(avg_bytes), "peak_source": peak_src,
-                "timing": "CUDA events on the launching stream over the timed region; a call is one "
-                          "skinny_kernel launch (back-to-back launches overlap through PDL)"}
+                "timing": "CUDA events on the launching stream over the timed region; a call is the "
+                          "plan's launches (one skinny_kernel for this shape; back-to-back calls overlap "
+                          "through programmatic dependent launch)"}
 
     # ---------------- e2e through the public call: pinned host x in, host y out, every call
     e2e = run_e2e(args, proj, x_all, stream, world)

@@ -31,15 +31,20 @@
  *
  * Ownership and concurrency
  *   The caller owns x, the weight buffers and y.  A plan owns host state and
- *   one device workspace (split-K partials, counters, an error word),
- *   allocated by nvfp4_plan_create* on the device that is
- *   current then; all later calls on the plan must run on that device.
- *   nvfp4_skinny_linear never allocates, never synchronizes and only
- *   enqueues one kernel on `stream`, so it can be captured in a CUDA graph.
- *   The kernel is launched with programmatic dependent launch: it starts
- *   reading the weights before the previous kernel on the stream has
- *   finished (x, y and the workspace are touched only after it has), so
- *   the weights must not be written by a kernel still running on `stream`.
+ *   one device workspace (split-K partials, counters, an error word, the
+ *   fp16 activation operand and its per-row scales), allocated by
+ *   nvfp4_plan_create* on the device that is current then; all later calls
+ *   on the plan must run on that device.  nvfp4_skinny_linear never
+ *   allocates, never synchronizes and only enqueues kernels on `stream`, so
+ *   it can be captured in a CUDA graph: one kernel when every block of the
+ *   work split has at most `stages` units (it then prepares its own
+ *   activations), else an activation-preparation kernel and then the
+ *   projection kernel (nvfp4_plan_info.launches_per_call says which).  The
+ *   kernels are launched with programmatic dependent launch: the projection
+ *   kernel starts reading the weights before the kernels before it on the
+ *   stream have finished (x, y and the workspace are touched only after they
+ *   have), so the weights must not be written by a kernel still running on
+ *   `stream`.
  *   Calls that share a plan must not run concurrently (the workspace is
  *   reused); calls on one stream are ordered and safe.
  *
@@ -51,14 +56,16 @@
  *   skips the remaining work and exits; nvfp4_plan_check reports it.
  *
  * Numerics
- *   For every 256-wide k-step, each activation row is converted to fp16 after
- *   multiplying it by a power of two chosen from its largest magnitude in
- *   that k-step (exact for every element within 2^-33 of that maximum);
- *   weights are decoded to fp16 (E2M1 x E4M3 is exact in fp16); products
- *   accumulate in fp32 on the tensor cores; each k-step's fp32 sum is
- *   multiplied back by the inverse power of two (exact) and added in a fixed
- *   order; w_global_scale multiplies the total, which is then rounded to
- *   nearest-even bfloat16 (or returned as fp32).
+ *   Each activation row is converted to fp16 after multiplying it by a power
+ *   of two chosen from its largest magnitude (over all of K, or, when one
+ *   launch does the call, over the k-steps of each block of the work split;
+ *   which applies depends on (N, K) and the SM count only), exact for every
+ *   element within 2^-32 of that maximum; weights are decoded to fp16
+ *   (E2M1 x E4M3 is exact in fp16); products accumulate in fp32 on the
+ *   tensor cores over a block's whole share of a row block's K; that sum is
+ *   multiplied back by the inverse power of two (exact); split shares are
+ *   added in a fixed order; w_global_scale multiplies the total, which is
+ *   then rounded to nearest-even bfloat16 (or returned as fp32).
  */
 #ifndef NVFP4_SKINNY_H
 #define NVFP4_SKINNY_H
@@ -135,6 +142,9 @@ typedef struct {
   int64_t units;            /* row_blocks * k_steps, split evenly over the grid */
   int64_t workspace_bytes;
   int64_t smem_bytes;       /* dynamic shared memory of the main kernel */
+  int32_t launches_per_call; /* 1: the projection kernel prepares its activations; 2: a
+                                preparation kernel runs before it */
+  int32_t reserved;
 } nvfp4_plan_info;
 
 nvfp4_status nvfp4_plan_get_info(nvfp4_plan_t plan, nvfp4_plan_info* info);
@@ -147,7 +157,8 @@ nvfp4_status nvfp4_plan_get_info(nvfp4_plan_t plan, nvfp4_plan_info* info);
  * allocates its workspace in nvfp4_plan_create*, so this entry point takes the shape directly.
  *
  * It computes the same y = x . dequant(W)^T with the same kernels, work split and numerics as
- * nvfp4_skinny_linear, but its scratch (split-K parts, split-K counters, an error word) lives
+ * nvfp4_skinny_linear, but its scratch (split-K parts, split-K counters, an error word, the
+ * activation operand and its scales) lives
  * in one fixed, statically sized device array inside the
  * library.  Every GPU that loads the library holds that array, NVFP4_NOALLOC_SCRATCH_BYTES
  * bytes, until the process exits.  Limits: K <= NVFP4_NOALLOC_MAX_K and
@@ -166,7 +177,7 @@ nvfp4_status nvfp4_plan_get_info(nvfp4_plan_t plan, nvfp4_plan_info* info);
  * ------------------------------------------------------------------------------------------- */
 #define NVFP4_NOALLOC_MAX_K 32768
 #define NVFP4_NOALLOC_MAX_N 4194304
-#define NVFP4_NOALLOC_SCRATCH_BYTES 10617088 /* about 10.1 MiB */
+#define NVFP4_NOALLOC_SCRATCH_BYTES 12714496 /* about 12.1 MiB */
 
 nvfp4_status nvfp4_skinny_linear_noalloc(int64_t N, int64_t K, nvfp4_out_dtype out_dtype, const void* x, int M,
                                          const uint8_t* w_codes, const uint8_t* w_block_scales, float w_global_scale,

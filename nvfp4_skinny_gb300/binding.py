@@ -52,7 +52,8 @@ class PlanInfo(ctypes.Structure):
                 ("rows_per_block", ctypes.c_int32), ("k_step", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("threads", ctypes.c_int32), ("grid", ctypes.c_int32), ("sm_count", ctypes.c_int32),
                 ("device", ctypes.c_int32), ("row_blocks", ctypes.c_int64), ("k_steps", ctypes.c_int64),
-                ("units", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64), ("smem_bytes", ctypes.c_int64)]
+                ("units", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64), ("smem_bytes", ctypes.c_int64),
+                ("launches_per_call", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 _cuda = None

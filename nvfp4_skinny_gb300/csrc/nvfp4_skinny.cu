@@ -1,7 +1,8 @@
 // C ABI of the skinny NVFP4 projection (declared and documented in include/nvfp4_skinny.h).
 // Host side: plan creation (work split from (N, K) and the SM count only), argument checks
-// before anything is enqueued, and the one launch of a call, with programmatic dependent
-// launch so that a call's weight stream starts while the previous call's kernel finishes.
+// before anything is enqueued, and the two launches of a call (activation preparation, then
+// the projection), with programmatic dependent launch so that a call's weight stream starts
+// while the kernels before it finish.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -16,12 +17,14 @@
 
 namespace {
 
-constexpr int kAbiVersion = 1;
+constexpr int kAbiVersion = 2;
 
 struct Workspace {
   float* partials = nullptr; // [2 * grid][32][256]
   int* counters = nullptr;   // [2][row_blocks]
   int* err = nullptr;        // [1]
+  uint8_t* x16 = nullptr;    // fp16 activation operand: [K / 256][32 rows x 256 k x 2 bytes]
+  float* xs = nullptr;       // [32] 2^-e per activation row
   void* base = nullptr;
   size_t bytes = 0;
 };
@@ -93,6 +96,14 @@ bool prepare_tensor_maps(nvfp4_plan* plan, const uint8_t* codes, const uint8_t* 
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+size_t x16_bytes(int64_t K) { return (size_t)(K / nvfp4::kKStep) * nvfp4::kXAreaBytes; }
+
+// One launch per call when every block of the split has at most kStages units: the projection
+// kernel then converts its own activations into its stages.  A function of (N, K, grid) only.
+int fused_mode(int64_t row_blocks, int64_t K, int grid) {
+  return (row_blocks * (K / nvfp4::kKStep) + grid - 1) / grid <= nvfp4::kStages ? 1 : 0;
+}
+
 cudaError_t set_smem_limits() {
   cudaError_t e = cudaFuncSetAttribute(nvfp4::skinny_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        nvfp4::kSmemBytes);
@@ -101,14 +112,36 @@ cudaError_t set_smem_limits() {
                               nvfp4::kSmemBytes);
 }
 
-// The one launch of a call (shared by the plan and allocation-free entry points).
+// The two launches of a call (shared by the plan and allocation-free entry points).
 nvfp4_status launch_main(const CUtensorMap& tm_codes, const CUtensorMap& tm_scales, const void* x, int M, float gs,
-                         void* y, float* partials, int* counters, int* err, int out_f32, int grid, int64_t N,
-                         int64_t K, int64_t row_blocks, cudaStream_t stream) {
+                         void* y, float* partials, int* counters, int* err, uint8_t* x16, float* xs, int out_f32,
+                         int grid, int64_t N, int64_t K, int64_t row_blocks, cudaStream_t stream) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+
+  const int nc = M <= 16 ? 16 : 32;
+  const int fused = fused_mode(row_blocks, K, grid);
+  if (!fused) {
+    cudaLaunchConfig_t pcfg = {};
+    pcfg.gridDim = dim3((unsigned)nc);
+    pcfg.blockDim = dim3(nvfp4::kPrepThreads);
+    pcfg.stream = stream;
+    pcfg.attrs = attr;
+    pcfg.numAttrs = 1;
+    const uint16_t* xb = static_cast<const uint16_t*>(x);
+    const cudaError_t pe = nc == 16 ? cudaLaunchKernelEx(&pcfg, nvfp4::x_prep_kernel<16>, xb, M, K, x16, xs)
+                                    : cudaLaunchKernelEx(&pcfg, nvfp4::x_prep_kernel<32>, xb, M, K, x16, xs);
+    if (pe != cudaSuccess) return NVFP4_ERR_CUDA;
+  }
+
   nvfp4::MainParams p;
   p.tm_codes = tm_codes;
   p.tm_scales = tm_scales;
   p.x = static_cast<const uint16_t*>(x);
+  p.x16 = x16;
+  p.xs = xs;
+  p.fused = fused;
   p.y = y;
   p.partials = partials;
   p.counters = counters;
@@ -123,9 +156,6 @@ nvfp4_status launch_main(const CUtensorMap& tm_codes, const CUtensorMap& tm_scal
   p.units = row_blocks * p.S;
   p.row_blocks = row_blocks;
 
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(nvfp4::kThreads);
@@ -133,7 +163,7 @@ nvfp4_status launch_main(const CUtensorMap& tm_codes, const CUtensorMap& tm_scal
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = M <= 16 ? cudaLaunchKernelEx(&cfg, nvfp4::skinny_kernel<16>, p)
+  const cudaError_t e = nc == 16 ? cudaLaunchKernelEx(&cfg, nvfp4::skinny_kernel<16>, p)
                                 : cudaLaunchKernelEx(&cfg, nvfp4::skinny_kernel<32>, p);
   return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
@@ -142,8 +172,8 @@ nvfp4_status launch_call(nvfp4_plan* plan, const void* x, int M, const uint8_t* 
                          float gs, void* y, cudaStream_t stream) {
   if (!prepare_tensor_maps(plan, codes, scales)) return NVFP4_ERR_CUDA;  // before anything is enqueued
   return launch_main(plan->tm_codes, plan->tm_scales, x, M, gs, y, plan->ws.partials, plan->ws.counters,
-                     plan->ws.err, plan->out == NVFP4_OUT_F32 ? 1 : 0, plan->grid, plan->N, plan->K,
-                     plan->row_blocks, stream);
+                     plan->ws.err, plan->ws.x16, plan->ws.xs, plan->out == NVFP4_OUT_F32 ? 1 : 0, plan->grid,
+                     plan->N, plan->K, plan->row_blocks, stream);
 }
 
 }  // namespace
@@ -202,7 +232,9 @@ nvfp4_status nvfp4_plan_create_ex(int64_t N, int64_t K, nvfp4_out_dtype out_dtyp
   const size_t part_bytes = round_up((size_t)2 * plan->grid * nvfp4::kNmma * nvfp4::kRowsPerBlock * 4, 256);
   const size_t cnt_bytes = round_up((size_t)plan->row_blocks * 2 * 4, 256);
   const size_t err_bytes = 256;
-  const size_t total = part_bytes + cnt_bytes + err_bytes;
+  const size_t xs_bytes = 256;
+  const size_t x16b = x16_bytes(K);
+  const size_t total = part_bytes + cnt_bytes + err_bytes + xs_bytes + x16b;
   void* base = nullptr;
   if (cudaMalloc(&base, total) != cudaSuccess) {
     delete plan;
@@ -214,6 +246,8 @@ nvfp4_status nvfp4_plan_create_ex(int64_t N, int64_t K, nvfp4_out_dtype out_dtyp
   plan->ws.partials = reinterpret_cast<float*>(b);
   plan->ws.counters = reinterpret_cast<int*>(b + part_bytes);
   plan->ws.err = reinterpret_cast<int*>(b + part_bytes + cnt_bytes);
+  plan->ws.xs = reinterpret_cast<float*>(b + part_bytes + cnt_bytes + err_bytes);
+  plan->ws.x16 = b + part_bytes + cnt_bytes + err_bytes + xs_bytes;
   if (cudaMemset(base, 0, total) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     cudaFree(base);
     delete plan;
@@ -282,6 +316,8 @@ nvfp4_status nvfp4_plan_get_info(nvfp4_plan_t plan, nvfp4_plan_info* info) {
   info->units = plan->units;
   info->workspace_bytes = (int64_t)plan->ws.bytes;
   info->smem_bytes = nvfp4::kSmemBytes;
+  info->launches_per_call = fused_mode(plan->row_blocks, plan->K, plan->grid) ? 1 : 2;
+  info->reserved = 0;
   return NVFP4_OK;
 }
 
@@ -290,7 +326,7 @@ nvfp4_status nvfp4_plan_get_info(nvfp4_plan_t plan, nvfp4_plan_info* info) {
 // ------------------------------------------------------------------------------------------------
 // Allocation-free entry point (declared in include/nvfp4_skinny.h).  Its scratch is one fixed
 // device array in this file, laid out like a plan's workspace for the largest problem it
-// accepts: error word, split-K counters, parts.
+// accepts: error word, split-K counters, parts, activation scales and operand.
 namespace {
 
 constexpr int64_t kNaMaxK = NVFP4_NOALLOC_MAX_K;
@@ -300,7 +336,9 @@ constexpr int kNaMaxGrid = 160;  // at most this many blocks (GB300 has 152 SMs)
 constexpr size_t kNaErrBytes = 256;
 constexpr size_t kNaCounterBytes = (size_t)kNaMaxRowBlocks * 2 * 4;
 constexpr size_t kNaPartBytes = (size_t)2 * kNaMaxGrid * nvfp4::kNmma * nvfp4::kRowsPerBlock * 4;
-constexpr size_t kNaScratchBytes = kNaErrBytes + kNaCounterBytes + kNaPartBytes;
+constexpr size_t kNaXsBytes = 256;
+constexpr size_t kNaX16Bytes = (size_t)(kNaMaxK / nvfp4::kKStep) * nvfp4::kXAreaBytes;
+constexpr size_t kNaScratchBytes = kNaErrBytes + kNaCounterBytes + kNaPartBytes + kNaXsBytes + kNaX16Bytes;
 static_assert(kNaScratchBytes == NVFP4_NOALLOC_SCRATCH_BYTES, "header states the scratch size");
 
 struct NoAllocDevice {
@@ -369,6 +407,8 @@ extern "C" nvfp4_status nvfp4_skinny_linear_noalloc(int64_t N, int64_t K, nvfp4_
   int* err = reinterpret_cast<int*>(base);
   int* counters = reinterpret_cast<int*>(base + kNaErrBytes);
   float* parts = reinterpret_cast<float*>(base + kNaErrBytes + kNaCounterBytes);
+  float* xs = reinterpret_cast<float*>(base + kNaErrBytes + kNaCounterBytes + kNaPartBytes);
+  uint8_t* x16 = base + kNaErrBytes + kNaCounterBytes + kNaPartBytes + kNaXsBytes;
 
   CUtensorMap tm_codes, tm_scales;
   if (!encode_u8_2d(&tm_codes, w_codes, (uint64_t)K / 2, (uint64_t)N, nvfp4::kCodeRowBytes, nvfp4::kRowsPerBlock,
@@ -383,6 +423,6 @@ extern "C" nvfp4_status nvfp4_skinny_linear_noalloc(int64_t N, int64_t K, nvfp4_
       cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess)
     return NVFP4_ERR_CUDA;
 
-  return launch_main(tm_codes, tm_scales, x, M, w_global_scale, y, parts, counters, err,
+  return launch_main(tm_codes, tm_scales, x, M, w_global_scale, y, parts, counters, err, x16, xs,
                      out_dtype == NVFP4_OUT_F32 ? 1 : 0, (int)grid, N, K, row_blocks, s);
 }

@@ -1,6 +1,17 @@
-// Device kernel of the skinny NVFP4 projection y = x . dequant(W)^T on sm_103a.
+// Device kernels of the skinny NVFP4 projection y = x . dequant(W)^T on sm_103a.
 //
-// One persistent, warp-specialised kernel per call, one block per SM, 16 warps (4 per SM
+// x_prep_kernel (one block per activation row): the row's largest magnitude over all of K
+// fixes a power of two 2^e (the maximum lands in [2^15, 2^16)); the row is written once, as
+// fp16 times 2^e, into an operand buffer laid out k-step by k-step exactly as the tensor core
+// reads it from shared memory, and 2^-e goes to a small table.  Exact for every element within
+// 2^-32 of the row's maximum.
+//
+// When every block of the work split has at most kStages units (fused mode), the call is one
+// launch of skinny_kernel: its epilogue and issuer warps copy the block's own activation rows
+// into the stages, take each row's largest magnitude over the block's k-steps and convert in
+// place.  Otherwise x_prep_kernel runs first.  The choice depends on (N, K, grid) only.
+//
+// skinny_kernel: persistent and warp-specialised, one block per SM, 16 warps (4 per SM
 // sub-partition, so each thread may hold 128 registers):
 //   warps 0-7    decoders: one weight row per thread; E2M1 x E4M3 -> fp16 with the hardware
 //                converters (exact: at most 6 significant bits), written to tensor memory as the
@@ -8,30 +19,26 @@
 //                2-D tensor copies (TMA) of a 256-row x 256-k block of codes (128-byte swizzle)
 //                and of its block scales into a 4-stage shared-memory ring; the last decoder
 //                warp to take a stage's bytes into registers issues the stage's next copy;
-//   warps 8-11   activations and epilogue: 16-byte asynchronous copies of the unit's bf16
-//                activation rows (through the load/store path: a copy queued behind the
-//                weight stream in the tensor-copy engine would arrive microseconds late),
-//                conversion to fp16 times 2^e with e chosen per (row, unit) from the largest
-//                magnitude (exact for every element within 2^-33 of it), and after each unit:
-//                tensor memory -> registers, the unit's sums times 2^-e added to an fp32
-//                accumulator.  At the end of a row block's k-range: times the per-tensor
-//                scale, rounded and stored; a row block split over several blocks is
-//                published and reduced at the end of the block's range;
-//   warps 12-15  MMA issuers, one per (128-row tile, k-half): tcgen05.mma M=128, N=32, K=16,
-//                fp32 accumulation in tensor memory, 8 per unit each.  Four issuers keep the
-//                tensor core fed at N=32 (one issuing thread sustains about one such MMA per
-//                44 cycles, four reach one per ~16 SM-wide).  An issuer never reads shared
-//                memory (a read waits for its MMAs in flight): it learns that operands are
-//                ready from hardware named barriers and reports completions through
-//                tcgen05.commit.
+//   warps 8-11   epilogue: one bulk copy per unit of the unit's fp16 activations into the
+//                stage (after the MMAs of the unit that last used it completed; fused mode:
+//                the activations are prepared once, before the first MMA); at the end of
+//                a row block's k-range: tensor memory -> registers, times 2^-e, times the
+//                per-tensor scale, rounded and stored, or published for the split-K reduction
+//                at the end of the block's range;
+//   warps 12-15  MMA issuers, one per (128-row tile, k-half): tcgen05.mma M=128, N=NC, K=16,
+//                fp32 accumulation in tensor memory over every unit of a row block's k-range,
+//                8 per unit each.  Four issuers keep the tensor core fed (one issuing thread
+//                sustains about one such MMA per 44 cycles, four reach one per ~16 SM-wide).
+//                An issuer never reads shared memory (a read waits for its MMAs in flight): it
+//                learns that operands are ready from hardware named barriers and reports
+//                completions through tcgen05.commit.
 //
 // Work split ("10 Kernels" 10.1 Row invariance): a unit is (row block of 256 weight rows,
 // k-step of 256).  The units, row-block-major, are split into `grid` contiguous, equal ranges;
 // grid = min(units, SMs).  Which block computes which part of a row's sum, the order of the
-// MMAs inside a unit, the order in which units and parts are added all depend on (N, K,
-// grid) only.  Activation row m is column m of every MMA, its exponent e depends on row m
-// alone, and nothing a column computes depends on another column, so a row's bits do not
-// depend on M.
+// MMAs and the order in which parts are added all depend on (N, K, grid) only.  Activation
+// row m is column m of every MMA, its exponent e depends on row m alone, and nothing a column
+// computes depends on another column, so a row's bits do not depend on M.
 #pragma once
 
 #include <cuda.h>
@@ -57,11 +64,10 @@ constexpr int kScaleRowBytes = kKStep / 16;         // 16 E4M3 scales per row pe
 constexpr int kCodeStageBytes = kRowsPerBlock * kCodeRowBytes;    // 32768, 128-byte swizzled rows
 constexpr int kScaleStageBytes = kRowsPerBlock * kScaleRowBytes;  // 4096
 constexpr int kWStageBytes = kCodeStageBytes + kScaleStageBytes;  // 36864
-constexpr int kXBufs = 2;                           // activation buffers (one per unit in flight)
-constexpr int kXGroupBytes = 8 * kKStep * 2;        // 8 activation rows x 256 k x fp16 = 4 KB
-constexpr int kX16Bytes = (kNmma / 8) * kXGroupBytes;             // 16384: operand layout
-constexpr int kXRawPitch = kKStep * 2 + 16;         // 528: bf16 row + 16 bytes (conflict-free reads)
-constexpr int kXRawBytes = kNmma * kXRawPitch;      // 16896
+constexpr int kXAreaBytes = kNmma * kKStep * 2;    // 16384: one unit's fp16 activations, up to 32 rows
+constexpr int kXOff = kWStageBytes;                 // activation area inside a stage (1 KB aligned)
+constexpr int kStageBytes = kWStageBytes + kXAreaBytes;           // 53248
+constexpr int kPrepThreads = 512;
 
 constexpr int kDecodeWarps = 8;
 constexpr int kEpiWarp0 = 8;  // also allocates and frees tensor memory
@@ -80,35 +86,37 @@ __device__ __forceinline__ uint32_t d_col(int d, int t, int h) {
   return 256u + (uint32_t)(d * 128 + (t * kHalves + h) * kNmma);
 }
 
-// shared memory
-constexpr int kSmemX16 = kStages * kWStageBytes;            // 147456
-constexpr int kSmemXRaw = kSmemX16 + kXBufs * kX16Bytes;    // 180224
-constexpr int kSmemBar = kSmemXRaw + kXBufs * kXRawBytes;   // 214016
+// shared memory: kStages stages of [codes | scales | activations], then barriers and misc
+constexpr int kSmemBar = kStages * kStageBytes;              // 212992
 // mbarrier indices
 constexpr int kBarFull = 0;                                  // [kStages]  weight copies (tx) -> decoders
-constexpr int kBarAEmpty = kBarFull + kStages;               // [half][tile]  MMA commit -> decoders
-constexpr int kBarUnit = kBarAEmpty + kHalves * kTiles;      // [kXBufs]   4 MMA commits -> epilogue
-constexpr int kBarFinal = kBarUnit + kXBufs;                 // [issuer]   MMA drain at exit
+constexpr int kBarXFull = kBarFull + kStages;                // [kStages]  activation copy (tx) -> decoders
+constexpr int kBarAEmpty = kBarXFull + kStages;              // [half][tile]  MMA commit -> decoders
+constexpr int kBarUnit = kBarAEmpty + kHalves * kTiles;      // [4]        4 MMA commits per unit -> epilogue
+constexpr int kUnitBars = 4;
+constexpr int kBarFinal = kBarUnit + kUnitBars;              // [issuer]   MMA drain at exit
 constexpr int kNumBars = kBarFinal + kMmaWarps;
 constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
 // misc: +0 tensor-memory base, +4 abort flag, +8 fix-up flag, +16 stage release counts
-// [kStages], +128 xs[kXsBufs][32] (2^-e of unit j in buffer j % 4), +640 partial row maxima
-// [2][epilogue warp][32] (unit j in buffer j % 2)
-constexpr int kXsBufs = 4;
-constexpr int kMiscBytes = 640 + 2 * 4 * 32 * 4;
+// [kStages], +128 xs[32] (2^-e of each activation row), +256 row maxima [32] (bf16 magnitude bits)
+constexpr int kMiscBytes = 256 + kNmma * 4;
+constexpr uint32_t kNbPrep = 8;                      // epilogue + issuer warps preparing activations
+constexpr uint32_t kNbPrepThreads = 8 * 32;
 constexpr int kSmemBytes = kSmemMisc + kMiscBytes + 1024;  // misc + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory per block");
 
 // hardware named barriers (0 is __syncthreads)
 constexpr uint32_t kNbEpi = 1;  // the 4 epilogue warps
 __device__ __forceinline__ uint32_t nb_afull(int h, int t) { return 2u + (uint32_t)(h * kTiles + t); }
-__device__ __forceinline__ uint32_t nb_ready(int d) { return 6u + (uint32_t)d; }
+__device__ __forceinline__ uint32_t nb_dfree(int d) { return 6u + (uint32_t)d; }
 constexpr uint32_t kNbAFullThreads = 4 * 32 + 32;    // 4 decoder warps + 1 issuer warp
-constexpr uint32_t kNbReadyThreads = 4 * 32 + 4 * 32;  // 4 epilogue warps + 4 issuer warps
+constexpr uint32_t kNbDFreeThreads = 4 * 32 + 4 * 32;  // 4 epilogue warps + 4 issuer warps
 
-// instruction descriptor: kind::f16, D = f32, A = B = f16, both K-major, N = 32, M = 128
-constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(kNmma >> 3) << 17) |
-                            ((uint32_t)(kTileRows >> 4) << 24);
+// instruction descriptor: kind::f16, D = f32, A = B = f16, both K-major, N = NC, M = 128
+template <int NC>
+__host__ __device__ constexpr uint32_t idesc() {
+  return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(NC >> 3) << 17) | ((uint32_t)(kTileRows >> 4) << 24);
+}
 
 constexpr long long kWaitLimitCycles = 4000000000LL;  // ~2 s at 2 GHz: a bounded wait
 
@@ -117,7 +125,10 @@ enum : int { kErrTimeout = 1 };
 struct MainParams {
   CUtensorMap tm_codes;   // uint8 [N rows, K/2 bytes], box 128 B x 256 rows, 128-byte swizzle
   CUtensorMap tm_scales;  // uint8 [N rows, K/16 bytes], box 16 B x 256 rows
-  const uint16_t* x;      // bf16 [M, K]
+  const uint16_t* x;      // bf16 [M, K] (read when `fused`)
+  const uint8_t* x16;     // fp16 activation operand, one NC-row block of 256 k per k-step (else)
+  const float* xs;        // [32] 2^-e per activation row (else)
+  int fused;              // every block has at most kStages units: it prepares its own activations
   void* y;                // [M, N] bf16 or f32
   float* partials;        // workspace [2*grid][32][256]
   int* counters;          // workspace [2][row_blocks]: parts published, blocks done; zero between calls
@@ -159,12 +170,20 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ab
   return true;
 }
 
-// UMMA shared-memory descriptor, K-major, no swizzle: core matrices of 8 rows x 16 bytes;
-// LBO = distance between the two k-halves of a k16 block, SBO = distance between 8-row groups.
+// UMMA shared-memory descriptor of the activation operand: K-major with the 128-byte swizzle.
+// Each 64-k block holds the NC rows as 128-byte lines (8-row groups 1024 bytes apart: SBO);
+// 16-byte chunk c of row m sits at chunk c ^ (m % 8) of its line.  A k16 block starts 32
+// bytes further along the line; the leading offset is unused with this swizzle.
 __device__ __forceinline__ uint64_t x_desc(uint32_t addr) {
-  constexpr uint64_t lbo = 128, sbo = kXGroupBytes;
+  constexpr uint64_t lbo = 16, sbo = 1024;
   return (uint64_t)((addr >> 4) & 0x3FFF) | (((lbo >> 4) & 0x3FFF) << 16) | (((sbo >> 4) & 0x3FFF) << 32) |
-         (1ull << 46);
+         (1ull << 46) | (2ull << 61);
+}
+// byte offset, inside one k-step's operand block, of activation row m's 16-byte chunk l
+// (k 8 l .. 8 l + 7 of the k-step)
+template <int NC>
+__device__ __forceinline__ uint32_t x_chunk_off(int m, int l) {
+  return (uint32_t)((l >> 3) * (NC * 128) + (m >> 3) * 1024 + (m & 7) * 128 + (((l & 7) ^ (m & 7)) << 4));
 }
 
 // ------------------------------------------------------------------ activation conversion helpers
@@ -220,32 +239,94 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, float f1, float f2) {
   return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
-// acc[j] += (D_a[j] + D_b[j]) * xs[j] over the first 16 or all 32 columns of two accumulators,
-// 8 columns at a time (few registers held: the epilogue also keeps 64 accumulators).
-template <int C0, int NC>
-__device__ __forceinline__ void drain_cols8(float (&acc)[NC], uint32_t addr_a, uint32_t addr_b, const float* xs) {
-  uint32_t a[8], b[8];
-  ptx::tmem_ld8(addr_a + C0, a);
-  ptx::tmem_ld8(addr_b + C0, b);
+// v0[j] = (D_a0[j] + D_b0[j]) * xs[j] and v1[j] likewise for the second tile, 16 columns: the
+// two k-half accumulators of each tile, all four loads in flight, one wait.
+__device__ __forceinline__ void drain16(float (&v0)[16], float (&v1)[16], uint32_t a0, uint32_t b0, uint32_t a1,
+                                        uint32_t b1, const float* xs) {
+  uint32_t ra0[16], rb0[16], ra1[16], rb1[16];
+  ptx::tmem_ld16(a0, ra0);
+  ptx::tmem_ld16(b0, rb0);
+  ptx::tmem_ld16(a1, ra1);
+  ptx::tmem_ld16(b1, rb1);
   ptx::tmem_wait_ld();
 #pragma unroll
-  for (int j = 0; j < 8; ++j)
-    acc[C0 + j] = __fmaf_rn(__fadd_rn(__uint_as_float(a[j]), __uint_as_float(b[j])), xs[C0 + j], acc[C0 + j]);
+  for (int j = 0; j < 16; ++j) {
+    v0[j] = __fmul_rn(__fadd_rn(__uint_as_float(ra0[j]), __uint_as_float(rb0[j])), xs[j]);
+    v1[j] = __fmul_rn(__fadd_rn(__uint_as_float(ra1[j]), __uint_as_float(rb1[j])), xs[j]);
+  }
 }
+
+// ------------------------------------------------------------------ activation preparation
+// largest magnitude of 8 bf16 as a bf16 bit pattern (a non-negative bf16 orders like its bits)
+__device__ __forceinline__ uint32_t bf16x8_maxmag(uint4 v) {
+  const uint32_t w[4] = {v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu, v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu};
+  uint32_t r = 0u;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) r = max(r, max(w[q] & 0xFFFFu, w[q] >> 16));
+  return r;
+}
+__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
+  uint32_t r;
+  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+  return r;
+}
+
+// One block per operand row m < NC; rows M..NC-1 are written as zeros (their MMA columns are
+// never read).  Magnitudes are compared as bf16 bit patterns (a non-negative bf16 orders like
+// its bits).  Each thread keeps its first kPrepHeld chunks in registers between the two passes
+// and reads any further ones again.
+constexpr int kPrepHeld = 8;
 template <int NC>
-__device__ __forceinline__ void drain_tile(float (&acc)[NC], uint32_t addr_a, uint32_t addr_b, const float* xs) {
-  drain_cols8<0>(acc, addr_a, addr_b, xs);
-  drain_cols8<8>(acc, addr_a, addr_b, xs);
-  if constexpr (NC > 16) {
-    drain_cols8<16>(acc, addr_a, addr_b, xs);
-    drain_cols8<24>(acc, addr_a, addr_b, xs);
+__global__ void __launch_bounds__(kPrepThreads) x_prep_kernel(const uint16_t* __restrict__ x, int M, int64_t K,
+                                                              uint8_t* __restrict__ x16, float* __restrict__ xs) {
+  ptx::grid_launch_dependents();  // the projection kernel may start streaming its weights
+  ptx::grid_dependency_wait();    // x is produced upstream; the operand buffer was read by the previous call
+  __shared__ uint32_t wmax[kPrepThreads / 32];
+  const int m = blockIdx.x, tid = threadIdx.x;
+  const int64_t chunks = K / 8;
+  const int64_t xbytes = (int64_t)NC * kKStep * 2;
+  auto dst = [&](int64_t c) {
+    return reinterpret_cast<uint4*>(x16 + (c >> 5) * xbytes + x_chunk_off<NC>(m, (int)(c & 31)));
+  };
+  if (m >= M) {
+    for (int64_t c = tid; c < chunks; c += kPrepThreads) *dst(c) = make_uint4(0u, 0u, 0u, 0u);
+    if (tid == 0) xs[m] = 0.f;
+    return;
+  }
+  const uint4* row = reinterpret_cast<const uint4*>(x + (int64_t)m * K);
+  uint4 held[kPrepHeld];
+  uint32_t mx = 0u;
+#pragma unroll
+  for (int k = 0; k < kPrepHeld; ++k) {
+    const int64_t c = tid + (int64_t)k * kPrepThreads;
+    held[k] = c < chunks ? __ldg(row + c) : make_uint4(0u, 0u, 0u, 0u);
+    mx = max(mx, bf16x8_maxmag(held[k]));
+  }
+  for (int64_t c = tid + (int64_t)kPrepHeld * kPrepThreads; c < chunks; c += kPrepThreads) mx = max(mx, bf16x8_maxmag(__ldg(row + c)));
+  const uint32_t wm = warp_max_u32(mx);
+  if ((tid & 31) == 0) wmax[tid >> 5] = wm;
+  __syncthreads();
+  uint32_t bm = 0u;
+#pragma unroll
+  for (int w = 0; w < kPrepThreads / 32; ++w) bm = max(bm, wmax[w]);
+  const int e = x_exponent(__uint_as_float(bm << 16));  // -112 <= e <= 148 for bf16 data
+  if (tid == 0) xs[m] = pow2i(-(e / 2)) * pow2i(-(e - e / 2));  // 2^-e, exact
+  const float f1 = pow2i(e <= 127 ? e : e / 2), f2 = pow2i(e <= 127 ? 0 : e - e / 2);
+#pragma unroll
+  for (int k = 0; k < kPrepHeld; ++k) {
+    const int64_t c = tid + (int64_t)k * kPrepThreads;
+    if (c < chunks) *dst(c) = e <= 127 ? bf16x8_to_f16x8(held[k], f1) : bf16x8_to_f16x8(held[k], f1, f2);
+  }
+  for (int64_t c = tid + (int64_t)kPrepHeld * kPrepThreads; c < chunks; c += kPrepThreads) {
+    const uint4 v = __ldg(row + c);
+    *dst(c) = e <= 127 ? bf16x8_to_f16x8(v, f1) : bf16x8_to_f16x8(v, f1, f2);
   }
 }
 
 // ------------------------------------------------------------------ main kernel
-// NC = activation rows the epilogue reads back (16 for M <= 16, else 32).  The MMAs are the
-// same N = 32 instructions in both instantiations and every column's epilogue arithmetic is the
-// same sequence of correctly rounded operations, so a row's bits do not depend on NC either.
+// NC = activation rows of the MMA (16 for M <= 16, else 32).  An N = 16 and an N = 32 MMA give
+// every column the same bits, and every column's epilogue arithmetic is the same sequence of
+// correctly rounded operations, so a row's bits do not depend on NC either.
 template <int NC>
 __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_constant__ MainParams p) {
   static_assert(NC == 16 || NC == 32, "epilogue width");
@@ -256,8 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemMisc + 4);
   volatile int* fix_flag = reinterpret_cast<volatile int*>(smem + kSmemMisc + 8);
   int* release_cnt = reinterpret_cast<int*>(smem + kSmemMisc + 16);  // [kStages]
-  float* xs_smem = reinterpret_cast<float*>(smem + kSmemMisc + 128);  // [kXsBufs][32]
-  float* pmax_smem = reinterpret_cast<float*>(smem + kSmemMisc + 640);  // [2][kEpiWarps][32]
+  float* xs_smem = reinterpret_cast<float*>(smem + kSmemMisc + 128);  // [32]
+  uint32_t* rowmax_smem = reinterpret_cast<uint32_t*>(smem + kSmemMisc + 256);  // [32]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = ptx::smem_addr(smem);
@@ -281,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
     return ks;
   };
 
-  // ---- set-up: barriers, activation operands zeroed (rows >= M stay zero), tensor memory
+  // ---- set-up: barriers, tensor memory
   const uint64_t pol_w = ptx::policy_evict_first();
   // unit i's weights -> stage i % kStages (full boxes are always delivered: rows past N are
   // zero-filled); one thread issues
@@ -289,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
     int s;
     const int64_t rb = unit_rb(i, s);
     const int st = i % kStages;
-    const uint32_t stage = smem_base + (uint32_t)(st * kWStageBytes);
+    const uint32_t stage = smem_base + (uint32_t)(st * kStageBytes);
     const uint32_t fb = bar(kBarFull + st);
     ptx::mbar_arrive_expect_tx(fb, (uint32_t)kWStageBytes);
     ptx::tma_load_2d(stage, &p.tm_codes, (int32_t)(s * kCodeRowBytes), (int32_t)(rb * kRowsPerBlock), fb, pol_w);
@@ -301,13 +382,13 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
       ptx::mbar_init(bar(kBarFull + s), 1);
       release_cnt[s] = 0;
     }
+    for (int s = 0; s < kStages; ++s) ptx::mbar_init(bar(kBarXFull + s), 1);
     for (int a = 0; a < kHalves * kTiles; ++a) ptx::mbar_init(bar(kBarAEmpty + a), 1);
-    for (int d = 0; d < kXBufs; ++d) {
-      ptx::mbar_init(bar(kBarUnit + d), kMmaWarps);
-    }
+    for (int u = 0; u < kUnitBars; ++u) ptx::mbar_init(bar(kBarUnit + u), kMmaWarps);
     for (int q = 0; q < kMmaWarps; ++q) ptx::mbar_init(bar(kBarFinal + q), 1);
     *abort_flag = 0;
     *fix_flag = 0;
+    for (int m = 0; m < kNmma; ++m) rowmax_smem[m] = 0u;
     ptx::fence_mbar_init();
     // The weights are read-only inputs that no kernel of this stream writes while calls are
     // queued, so they are streamed before the dependency wait on the previous call.
@@ -315,11 +396,6 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
     ptx::prefetch_tensormap(&p.tm_scales);
     for (int i = 0; i < kStages && i < n_local; ++i) issue_weights(i);
   }
-  {
-    uint4* xz = reinterpret_cast<uint4*>(smem + kSmemX16);
-    for (int i = threadIdx.x; i < kXBufs * kX16Bytes / 16; i += kThreads) xz[i] = make_uint4(0u, 0u, 0u, 0u);
-  }
-  ptx::fence_proxy_async_smem();
   if (warp == kEpiWarp0) {
     ptx::tmem_alloc(ptx::smem_addr(tmem_base_smem), kTmemCols);
     ptx::tmem_relinquish();
@@ -330,6 +406,55 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
   ptx::grid_launch_dependents();
   const uint32_t tmem = *tmem_base_smem;
   const Abort ab{abort_flag, p.err};
+
+  // Fused mode (every block has at most kStages units, one per stage): the 8 epilogue and
+  // issuer warps convert this block's activation rows straight into the stages.  Item (row m,
+  // unit q) is one 512-byte row slice, one warp-wide load, lane l taking 16-byte chunk l.  Row
+  // m's exponent comes from its largest magnitude over this block's k-steps.
+  auto prep_fused = [&](int pw) {
+    ptx::grid_dependency_wait();  // x is produced upstream
+    const int M = p.M;
+    const int n_items = M * n_local;  // at most 32 * kStages
+    const uint64_t pol = ptx::policy_evict_last();
+    // each lane copies its chunk of the warp's items to the chunk's final place in the stage
+    // (all copies in flight at once) and later rewrites the same 16 bytes as fp16: no thread
+    // touches another thread's chunk before the row maxima are combined
+#pragma unroll 1
+    for (int it = pw; it < n_items; it += 8) {
+      const int m = it / n_local, q = it - m * n_local;
+      ptx::cp_async16(smem_base + (uint32_t)(q * kStageBytes + kXOff) + x_chunk_off<NC>(m, lane),
+                      p.x + (int64_t)m * p.K + (int64_t)unit_kstep(q) * kKStep + lane * 8, pol);
+    }
+    ptx::cp_async_commit();
+    ptx::cp_async_wait(0);
+#pragma unroll 1
+    for (int it = pw; it < n_items; it += 8) {
+      const int m = it / n_local, q = it - m * n_local;
+      const uint4 v = *reinterpret_cast<const uint4*>(smem + q * kStageBytes + kXOff + x_chunk_off<NC>(m, lane));
+      const uint32_t wm = warp_max_u32(bf16x8_maxmag(v));
+      if (lane == 0) atomicMax(rowmax_smem + m, wm);
+    }
+    ptx::named_bar_sync(kNbPrep, kNbPrepThreads);  // every row's maximum is in
+#pragma unroll 1
+    for (int it = pw; it < NC * n_local; it += 8) {
+      const int m = it / n_local, q = it - m * n_local;
+      uint4* slot = reinterpret_cast<uint4*>(smem + q * kStageBytes + kXOff + x_chunk_off<NC>(m, lane));
+      uint4 o = make_uint4(0u, 0u, 0u, 0u);  // rows M .. NC-1 are zero (their MMA columns are never read)
+      if (m < M) {
+        const uint4 v = *slot;
+        const int e = x_exponent(__uint_as_float(rowmax_smem[m] << 16));  // -112 <= e <= 148
+        o = e <= 127 ? bf16x8_to_f16x8(v, pow2i(e)) : bf16x8_to_f16x8(v, pow2i(e / 2), pow2i(e - e / 2));
+      }
+      *slot = o;
+    }
+    const int t = pw * 32 + lane;
+    if (t < NC) {
+      const int e = x_exponent(__uint_as_float(rowmax_smem[t] << 16));
+      xs_smem[t] = t < M ? pow2i(-(e / 2)) * pow2i(-(e - e / 2)) : 0.f;  // 2^-e, exact
+    }
+    ptx::fence_proxy_async_smem();  // operand writes -> the tensor core's (async proxy) reads
+    ptx::named_bar_sync(kNbPrep, kNbPrepThreads);  // every operand row in place before any MMA
+  };
 
   if (warp < kDecodeWarps) {
     // ================================================================ decoders
@@ -343,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
       const int st = i % kStages, round = i / kStages;
       if (ok) ok = wait_bar(bar(kBarFull + st), (uint32_t)(round & 1), ab);
       ok = __all_sync(0xffffffffu, ok);
-      const uint8_t* stage = smem + st * kWStageBytes;
+      const uint8_t* stage = smem + st * kStageBytes;
       // 128-byte swizzle: 16-byte chunk q of row r sits at chunk q ^ (r % 8) of the row
       const uint8_t* crow = stage + row_in_block * kCodeRowBytes;
       const int swz = row_in_block & 7;
@@ -391,6 +516,10 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
         }
         if (store) ptx::tmem_wait_st();
         ptx::tc_fence_before();
+        // the unit's activations must be in the stage before its first MMAs are released (after
+        // an abort this wait returns at once: the arrivals still pair with the issuers' syncs).
+        // In fused mode the issuers wrote them themselves before their first sync.
+        if (h == 0 && !p.fused) (void)wait_bar(bar(kBarXFull + st), (uint32_t)(round & 1), ab);
         ptx::named_bar_arrive(nb_afull(h, tile), kNbAFullThreads);
       }
     }
@@ -400,22 +529,30 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
     // shared-memory reads here: operand readiness comes from named barriers, completions go
     // out through tcgen05.commit.  The issuer has no abort path: MMAs on stale data are
     // harmless, and its commits keep every other role's waits completing.
+    if (p.fused) prep_fused(warp - kEpiWarp0);
     const int q = warp - kMmaWarp0, t = q >> 1, h = q & 1;
+    int sg = -1;  // row-block segment of this block's range; D buffer sg % 2 accumulates it
     for (int i = 0; i < n_local; ++i) {
-      const int d = i & 1;
-      ptx::named_bar_sync(nb_ready(d), kNbReadyThreads);  // activations of unit i in place, D(d) drained
-      ptx::named_bar_sync(nb_afull(h, t), kNbAFullThreads);
+      const bool first = i == 0 || unit_kstep(i) == 0;
+      if (first) {
+        ++sg;
+        ptx::named_bar_sync(nb_dfree(sg & 1), kNbDFreeThreads);  // D buffer drained by the epilogue
+      }
+      ptx::named_bar_sync(nb_afull(h, t), kNbAFullThreads);  // A slot decoded, activations in the stage
       ptx::tc_fence_after();
       if (lane == 0) {
-        const uint32_t d_tmem = tmem + d_col(d, t, h);
+        const uint32_t d_tmem = tmem + d_col(sg & 1, t, h);
         const uint32_t a_tmem = tmem + a_col(h, t);
-        const uint32_t xb = smem_base + (uint32_t)(kSmemX16 + d * kX16Bytes + h * kK16PerHalf * 256);
+        const uint32_t xb = smem_base + (uint32_t)((i % kStages) * kStageBytes + kXOff);
 #pragma unroll
-        for (int kk = 0; kk < kK16PerHalf; ++kk)
-          ptx::mma_f16_ts(d_tmem, a_tmem + (uint32_t)(kk * 8), x_desc(xb + (uint32_t)(kk * 256)), kIdesc,
-                          kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < kK16PerHalf; ++kk) {
+          const int j = h * kK16PerHalf + kk;  // k16 block of the unit: 64-k block j / 4, 32 bytes each
+          ptx::mma_f16_ts(d_tmem, a_tmem + (uint32_t)(kk * 8),
+                          x_desc(xb + (uint32_t)((j >> 2) * (NC * 128) + (j & 3) * 32)), idesc<NC>(),
+                          (first && kk == 0) ? 0u : 1u);
+        }
         ptx::mma_commit(bar(kBarAEmpty + h * kTiles + t));
-        ptx::mma_commit(bar(kBarUnit + d));
+        ptx::mma_commit(bar(kBarUnit + (i % kUnitBars)));
       }
       __syncwarp();
     }
@@ -426,161 +563,104 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
     }
     __syncwarp();
   } else {
-    // ================================================================ activations + epilogue
+    // ================================================================ epilogue
     const int ew = warp - kEpiWarp0, quad = warp & 3;
     const int etid = ew * 32 + lane;  // 0..127
-    ptx::grid_dependency_wait();  // x is produced upstream; y, partials and counters belong to the previous call until here
+    ptx::grid_dependency_wait();  // the activation operand, y, partials and counters are ready / free
     const int M = p.M;
     const float gs = p.gs;
     const uint64_t pol_x = ptx::policy_evict_last();
-    const int64_t K = p.K;
-
-    // Epilogue warp ew owns the 16-byte chunks 8 ew .. 8 ew + 7 (k 64 ew .. 64 ew + 63 of the
-    // k-step) of every activation row; lane (r8 = lane % 8, cc = lane / 8) owns, in each row
-    // group g, row 8 g + r8, chunks 8 ew + cc and 8 ew + cc + 4.  A lane copies its chunks,
-    // reads them back and writes their fp16 values, so no thread reads another thread's copies;
-    // the four warps' partial row maxima meet in shared memory behind one barrier per unit.
-    const int groups = (M + 7) >> 3;
-    const int r8 = lane & 7, cc = lane >> 3;
-    // unit j's k-step of the warp's chunks -> raw buffer j % 2; one commit group per unit
+    constexpr uint32_t kXBytes = NC * kKStep * 2;  // one unit's activations
+    // unit j's activations -> the activation area of stage j % kStages (one thread)
     auto issue_x = [&](int j) {
-      const int d = j & 1;
-      const int s = unit_kstep(j);
-      const uint32_t raw = smem_base + (uint32_t)(kSmemXRaw + d * kXRawBytes);
-      for (int g = 0; g < groups; ++g) {
-        const int m = g * 8 + r8;
-        if (m < M) {
-          const uint16_t* src = p.x + m * K + (int64_t)s * kKStep;
-#pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            const int c = 8 * ew + cc + 4 * k;
-            ptx::cp_async16(raw + (uint32_t)(m * kXRawPitch + c * 16), src + c * 8, pol_x);
-          }
-        }
-      }
-      ptx::cp_async_commit();
+      const int st = j % kStages;
+      const uint32_t xb = bar(kBarXFull + st);
+      ptx::mbar_arrive_expect_tx(xb, kXBytes);
+      ptx::bulk_g2s(smem_base + (uint32_t)(st * kStageBytes + kXOff), p.x16 + (int64_t)unit_kstep(j) * kXBytes,
+                    kXBytes, xb, pol_x);
     };
-    // raw buffer j % 2 -> fp16 operand buffer j % 2 and 2^-e -> xs buffer j % 4.  Groups are
-    // committed in unit order and unit j + 1's may be the only younger one.
-    auto convert = [&](int j) {
-      const int d = j & 1;
-      ptx::cp_async_wait(j + 1 < n_local ? 1 : 0);
-      const uint8_t* raw = smem + kSmemXRaw + d * kXRawBytes;
-      uint8_t* x16 = smem + kSmemX16 + d * kX16Bytes;
-      float* xs = xs_smem + (j & (kXsBufs - 1)) * kNmma;
-      float* pm = pmax_smem + d * (kEpiWarps * kNmma);
-      // pass 1: this warp's maximum magnitude of each row over its 8 chunks
-      for (int g = 0; g < groups; ++g) {
-        const int m = g * 8 + r8;
-        uint32_t a2 = 0u;
-        if (m < M) {
-#pragma unroll
-          for (int k = 0; k < 2; ++k)
-            a2 = bf16x8_absmax2(*reinterpret_cast<const uint4*>(raw + m * kXRawPitch + (8 * ew + cc + 4 * k) * 16), a2);
-        }
-        float a = fmaxf(fabsf(__uint_as_float(a2 << 16)), fabsf(__uint_as_float(a2 & 0xFFFF0000u)));
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));  // the 4 lanes of row r8
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 16));
-        if (cc == 0 && m < M) pm[ew * kNmma + m] = a;
-      }
-      ptx::named_bar_sync(kNbEpi, kEpiWarps * 32);
-      // pass 2: the row's exponent from the 4 partial maxima, then this lane's chunks
-      for (int g = 0; g < groups; ++g) {
-        const int m = g * 8 + r8;
-        if (m < M) {
-          const float amax = fmaxf(fmaxf(pm[m], pm[kNmma + m]), fmaxf(pm[2 * kNmma + m], pm[3 * kNmma + m]));
-          const int e = x_exponent(amax);  // -112 <= e <= 148 for bf16 data
-          if (ew == 0 && cc == 0) xs[m] = pow2i(-(e / 2)) * pow2i(-(e - e / 2));  // 2^-e, exact
-#pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            const int c = 8 * ew + cc + 4 * k;
-            const uint4 w = *reinterpret_cast<const uint4*>(raw + m * kXRawPitch + c * 16);
-            *reinterpret_cast<uint4*>(x16 + g * kXGroupBytes + c * 128 + r8 * 16) =
-                e <= 127 ? bf16x8_to_f16x8(w, pow2i(e)) : bf16x8_to_f16x8(w, pow2i(e / 2), pow2i(e - e / 2));
-          }
-        }
-      }
-      ptx::fence_proxy_async_smem();  // operand writes -> the tensor core's (async proxy) reads
-    };
-
-    for (int j = 0; j < kXBufs && j < n_local; ++j) issue_x(j);
-    for (int j = 0; j < kXBufs && j < n_local; ++j) {
-      convert(j);
-      if (j + kXBufs < n_local) issue_x(j + kXBufs);
-      ptx::named_bar_arrive(nb_ready(j), kNbReadyThreads);
+    if (p.fused) {
+      prep_fused(warp - kEpiWarp0);
+    } else {
+      if (etid == 0)
+        for (int j = 0; j < kStages && j < n_local; ++j) issue_x(j);
+      if (etid < kNmma) xs_smem[etid] = etid < NC ? p.xs[etid] : 0.f;
     }
+    int ks_last;
+    const int n_seg = (int)(unit_rb(n_local - 1, ks_last) - rb0) + 1;  // row-block segments of the range
+    for (int j = 0; j < 2 && j < n_seg; ++j) ptx::named_bar_arrive(nb_dfree(j), kNbDFreeThreads);
+    ptx::named_bar_sync(kNbEpi, kEpiWarps * 32);  // xs in shared memory for every epilogue thread
 
-    float acc0[NC], acc1[NC];  // rows r0 (tile 0) and r1 (tile 1) of the current row block
-#pragma unroll
-    for (int m = 0; m < NC; ++m) acc0[m] = acc1[m] = 0.f;
     bool ok = true;
     int64_t pend[2] = {0, 0};  // split row blocks of this block's range (its first and last)
     int n_pend = 0;
     const int r0 = quad * 32 + lane, r1 = r0 + kTileRows;  // rows inside the row block
+    const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16);
+    int sg = -1;
     for (int i = 0; i < n_local; ++i) {
-      const int d = i & 1;
       int s;
       const int64_t rb = unit_rb(i, s);
+      if (i == 0 || s == 0) ++sg;
       const bool seg_end = (i == n_local - 1) || (s == (int)S - 1);
-      // unit i's MMAs complete: D(d) final and activation buffer d free; gates a ready arrival,
-      // so the wait ignores the abort flag
-      const bool full = wait_bar(bar(kBarUnit + d), (uint32_t)((i >> 1) & 1), ab, false);
+      // unit i's MMAs complete: its stage's activation area may be refilled, and at the end of
+      // a segment the accumulators are final.  Gates later copies and arrivals, so the wait
+      // ignores the abort flag.
+      const bool full = wait_bar(bar(kBarUnit + (i % kUnitBars)), (uint32_t)((i / kUnitBars) & 1), ab, false);
       ok = __all_sync(0xffffffffu, ok && full);
-      ptx::tc_fence_after();
-      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16);
-      const float* xs = xs_smem + (i & (kXsBufs - 1)) * kNmma;
-      drain_tile(acc0, taddr + d_col(d, 0, 0), taddr + d_col(d, 0, 1), xs);
-      drain_tile(acc1, taddr + d_col(d, 1, 0), taddr + d_col(d, 1, 1), xs);
-      ptx::tc_fence_before();
-      // xs of unit i + 2 goes to another buffer than the one just read, and D(d) is rewritten only
-      // after every epilogue warp has arrived below: no barrier among the epilogue warps here
-      if (i + kXBufs < n_local) {
-        convert(i + kXBufs);
-        if (i + 2 * kXBufs < n_local) issue_x(i + 2 * kXBufs);
-        ptx::named_bar_arrive(nb_ready(d), kNbReadyThreads);
-      }
+      if (etid == 0 && !p.fused && i + kStages < n_local) issue_x(i + kStages);
       if (!seg_end) continue;
       ok = ok && !*abort_flag;  // an aborted call stores nothing more
+      ptx::tc_fence_after();
+      const int d = sg & 1;
 
       const int64_t n0 = rb * kRowsPerBlock + r0, n1 = rb * kRowsPerBlock + r1;
       const int64_t pf = block_of_unit(rb * S, T, G), pl = block_of_unit(rb * S + S - 1, T, G);
-      if (pf == pl) {
-        // the whole K of this row block was summed here
-        if (ok) {
+      const bool whole = pf == pl;  // the whole K of this row block was summed here
+      const int slot = (int)(2 * blockIdx.x) + (rb == rb0 ? 0 : 1);  // first or last row block of the range
+      // float stores go to the part (unscaled) or to an fp32 y; bf16 y is the other case
+      const bool bf16_out = whole && !p.out_f32;
+      const float mul = whole ? gs : 1.f;
+      const int64_t fstride = whole ? p.N : kRowsPerBlock;
+      float* f0 = whole ? static_cast<float*>(p.y) + n0 : p.partials + (int64_t)slot * (kNmma * kRowsPerBlock) + r0;
+      float* f1 = whole ? static_cast<float*>(p.y) + n1 : p.partials + (int64_t)slot * (kNmma * kRowsPerBlock) + r1;
+      uint16_t* h0 = static_cast<uint16_t*>(p.y) + n0;
+      uint16_t* h1 = static_cast<uint16_t*>(p.y) + n1;
+      const bool in0 = !whole || n0 < p.N, in1 = !whole || n1 < p.N;
+#pragma unroll 1
+      for (int cb = 0; cb < NC / 16; ++cb) {
+        float v0[16], v1[16];
+        drain16(v0, v1, taddr + d_col(d, 0, 0) + 16 * cb, taddr + d_col(d, 0, 1) + 16 * cb,
+                taddr + d_col(d, 1, 0) + 16 * cb, taddr + d_col(d, 1, 1) + 16 * cb, xs_smem + 16 * cb);
+        if (!ok) continue;
+        if (bf16_out) {
 #pragma unroll
-          for (int m = 0; m < NC; ++m) {
+          for (int j = 0; j < 16; ++j) {
+            const int64_t m = 16 * cb + j;
             if (m < M) {
-              const float a0 = acc0[m] * gs, a1 = acc1[m] * gs;
-              if (p.out_f32) {
-                float* y = static_cast<float*>(p.y) + (int64_t)m * p.N;
-                if (n0 < p.N) y[n0] = a0;
-                if (n1 < p.N) y[n1] = a1;
-              } else {
-                uint16_t* y = static_cast<uint16_t*>(p.y) + (int64_t)m * p.N;
-                if (n0 < p.N) y[n0] = ptx::f32_to_bf16_rn(a0);
-                if (n1 < p.N) y[n1] = ptx::f32_to_bf16_rn(a1);
-              }
+              if (in0) h0[m * p.N] = ptx::f32_to_bf16_rn(__fmul_rn(v0[j], gs));
+              if (in1) h1[m * p.N] = ptx::f32_to_bf16_rn(__fmul_rn(v1[j], gs));
+            }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int64_t m = 16 * cb + j;
+            if (m < M) {
+              if (in0) f0[m * fstride] = __fmul_rn(v0[j], mul);
+              if (in1) f1[m * fstride] = __fmul_rn(v1[j], mul);
             }
           }
         }
-      } else {
-        // split row block: publish this part; the sums are formed after the main loop
-        const int slot = (int)(2 * blockIdx.x) + (rb == rb0 ? 0 : 1);  // first or last row block of the range
-        float* part = p.partials + (int64_t)slot * (kNmma * kRowsPerBlock);
-#pragma unroll
-        for (int m = 0; m < NC; ++m) {
-          if (ok && m < M) {
-            part[m * kRowsPerBlock + r0] = acc0[m];
-            part[m * kRowsPerBlock + r1] = acc1[m];
-          }
-        }
+      }
+      ptx::tc_fence_before();
+      // D(d) is free again for segment sg + 2
+      if (sg + 2 < n_seg) ptx::named_bar_arrive(nb_dfree(d), kNbDFreeThreads);
+      if (!whole) {
         // the barrier orders every thread's stores before thread 0's release (cumulative)
         ptx::named_bar_sync(kNbEpi, kEpiWarps * 32);
         if (etid == 0 && ok) ptx::red_release_gpu_add(p.counters + rb, 1);
         if (n_pend < 2) pend[n_pend++] = rb;
       }
-#pragma unroll
-      for (int m = 0; m < NC; ++m) acc0[m] = acc1[m] = 0.f;
     }
     // Split row blocks: wait until every contributing block has published its parts of both
     // pending row blocks at once, then add this block's slice of the rows (part q of the block
@@ -629,17 +709,17 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
       const int g_lo = q * (kRowsPerBlock / 4) / nseg, g_hi = (q + 1) * (kRowsPerBlock / 4) / nseg;
       const int groups = g_hi - g_lo;
       // The slice's items (4 rows x 1 activation row): this thread takes items etid, etid + 128,
-      // ...; for each, the parts' loads (16 at a time) are all issued before any is used, and
+      // ...; for each, the parts' loads (8 at a time) are all issued before any is used, and
       // the parts are added strictly in block order.
       const int n_items = groups * M;
       for (int o = etid; o < n_items; o += kEpiWarps * 32) {
         const int m = o / groups, r = 4 * (g_lo + o % groups);
         const float* base = p.partials + m * kRowsPerBlock + r;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int b0 = 0; b0 < nseg; b0 += 16) {
-          float4 t[16];
+        for (int b0 = 0; b0 < nseg; b0 += 8) {
+          float4 t[8];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
+          for (int j = 0; j < 8; ++j) {
             if (b0 + j < nseg) {
               const int64_t b = pf + b0 + j;
               t[j] = __ldcg(reinterpret_cast<const float4*>(
@@ -647,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
             }
           }
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
+          for (int j = 0; j < 8; ++j) {
             if (b0 + j < nseg) {
               acc.x += t[j].x;
               acc.y += t[j].y;
