@@ -227,6 +227,13 @@ __device__ __forceinline__ void red_release_gpu_add(int* ptr, int v) {
   asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
 }
 
+// Add to a global int with acquire-release semantics at GPU scope; returns the old value.
+__device__ __forceinline__ int atom_acq_rel_gpu_add(int* ptr, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
+  return old;
+}
+
 // fp32 -> bfloat16 bits, round to nearest even.
 __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
   uint16_t h;

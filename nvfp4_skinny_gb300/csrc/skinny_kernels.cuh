@@ -97,8 +97,9 @@ constexpr int kUnitBars = 4;
 constexpr int kBarFinal = kBarUnit + kUnitBars;              // [issuer]   MMA drain at exit
 constexpr int kNumBars = kBarFinal + kMmaWarps;
 constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
-// misc: +0 tensor-memory base, +4 abort flag, +8 fix-up flag, +16 stage release counts
-// [kStages], +128 xs[32] (2^-e of each activation row), +256 row maxima [32] (bf16 magnitude bits)
+// misc: +0 tensor-memory base, +4 abort flag, +12 reduce count, +16 stage release counts
+// [kStages], +32 row blocks this block reduces [2] (int64) and their count, +128 xs[32] (2^-e of
+// each activation row), +256 row maxima [32] (bf16 magnitude bits)
 constexpr int kMiscBytes = 256 + kNmma * 4;
 constexpr uint32_t kNbPrep = 8;                      // epilogue + issuer warps preparing activations
 constexpr uint32_t kNbPrepThreads = 8 * 32;
@@ -335,10 +336,11 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSmemBar);
   uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + kSmemMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemMisc + 4);
-  volatile int* fix_flag = reinterpret_cast<volatile int*>(smem + kSmemMisc + 8);
   int* release_cnt = reinterpret_cast<int*>(smem + kSmemMisc + 16);  // [kStages]
   float* xs_smem = reinterpret_cast<float*>(smem + kSmemMisc + 128);  // [32]
   uint32_t* rowmax_smem = reinterpret_cast<uint32_t*>(smem + kSmemMisc + 256);  // [32]
+  int64_t* red_rb = reinterpret_cast<int64_t*>(smem + kSmemMisc + 32);  // [2]
+  volatile int* n_red = reinterpret_cast<volatile int*>(smem + kSmemMisc + 12);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = ptx::smem_addr(smem);
@@ -387,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
     for (int u = 0; u < kUnitBars; ++u) ptx::mbar_init(bar(kBarUnit + u), kMmaWarps);
     for (int q = 0; q < kMmaWarps; ++q) ptx::mbar_init(bar(kBarFinal + q), 1);
     *abort_flag = 0;
-    *fix_flag = 0;
+    *n_red = 0;
     for (int m = 0; m < kNmma; ++m) rowmax_smem[m] = 0u;
     ptx::fence_mbar_init();
     // The weights are read-only inputs that no kernel of this stream writes while calls are
@@ -592,8 +594,6 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
     ptx::named_bar_sync(kNbEpi, kEpiWarps * 32);  // xs in shared memory for every epilogue thread
 
     bool ok = true;
-    int64_t pend[2] = {0, 0};  // split row blocks of this block's range (its first and last)
-    int n_pend = 0;
     const int r0 = quad * 32 + lane, r1 = r0 + kTileRows;  // rows inside the row block
     const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16);
     int sg = -1;
@@ -656,106 +656,84 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
       // D(d) is free again for segment sg + 2
       if (sg + 2 < n_seg) ptx::named_bar_arrive(nb_dfree(d), kNbDFreeThreads);
       if (!whole) {
-        // the barrier orders every thread's stores before thread 0's release (cumulative)
+        // The barrier orders every thread's stores before thread 0's release (cumulative).  The
+        // block that publishes a row block's last part adds all of its parts after the main
+        // loop; it also clears the counter for the next call (no other block reads it again).
         ptx::named_bar_sync(kNbEpi, kEpiWarps * 32);
-        if (etid == 0 && ok) ptx::red_release_gpu_add(p.counters + rb, 1);
-        if (n_pend < 2) pend[n_pend++] = rb;
-      }
-    }
-    // Split row blocks: wait until every contributing block has published its parts of both
-    // pending row blocks at once, then add this block's slice of the rows (part q of the block
-    // order is always added q-th).  Every block publishes all of its parts before it waits
-    // here, so the waits end.  Once a block has seen all parts it counts itself done; the last
-    // block of a row block to do so clears its counters (no block polls them any more).
-    int64_t pfs[2] = {0, 0}, pls[2] = {0, 0};
-    for (int k = 0; k < n_pend; ++k) {
-      pfs[k] = block_of_unit(pend[k] * S, T, G);
-      pls[k] = block_of_unit(pend[k] * S + S - 1, T, G);
-    }
-    if (n_pend > 0) {
-      if (etid == 0) {
-        bool arrived[2] = {n_pend < 1, n_pend < 2};
-        const long long t0 = clock64();
-        while (!(arrived[0] && arrived[1]) && !*abort_flag) {
-          for (int k = 0; k < n_pend; ++k)
-            if (!arrived[k]) arrived[k] = ptx::ld_acquire_gpu(p.counters + pend[k]) >= (int)(pls[k] - pfs[k] + 1);
-          if (!(arrived[0] && arrived[1]) && clock64() - t0 > kWaitLimitCycles) {
-            *abort_flag = 1;
-            atomicOr(p.err, kErrTimeout);
-          }
-        }
-        const bool all = arrived[0] && arrived[1];
-        *fix_flag = all ? 1 : 0;
-        if (all) {
-          for (int k = 0; k < n_pend; ++k) {
-            const int64_t rb = pend[k];
-            if (atomicAdd(p.counters + p.row_blocks + rb, 1) == (int)(pls[k] - pfs[k])) {
-              p.counters[rb] = 0;
-              p.counters[p.row_blocks + rb] = 0;
-            }
+        if (etid == 0 && ok) {
+          const int nseg = (int)(pl - pf + 1);
+          if (ptx::atom_acq_rel_gpu_add(p.counters + rb, 1) == nseg - 1) {
+            p.counters[rb] = 0;
+            red_rb[*n_red] = rb;
+            *n_red = *n_red + 1;
           }
         }
       }
-      ptx::named_bar_sync(kNbEpi, kEpiWarps * 32);  // orders the acquire before every thread's loads
     }
-    for (int k = 0; k < n_pend && *fix_flag; ++k) {
-      const int64_t rb = pend[k], pf = pfs[k], pl = pls[k];
-      const int nseg = (int)(pl - pf + 1);
-      const int q = (int)(blockIdx.x - pf);
-      // part slot of block b: 2 b for every b > pf (rb is the first row block of its range);
-      // block pf used slot 2 pf + 1 if its range began in an earlier row block
-      const int pf_bit = unit_begin(pf, T, G) < rb * S ? 1 : 0;
-      // this block's slice: whole groups of 4 rows (the 64 groups of the row block split over nseg)
-      const int g_lo = q * (kRowsPerBlock / 4) / nseg, g_hi = (q + 1) * (kRowsPerBlock / 4) / nseg;
-      const int groups = g_hi - g_lo;
-      // The slice's items (4 rows x 1 activation row): this thread takes items etid, etid + 128,
-      // ...; for each, the parts' loads (8 at a time) are all issued before any is used, and
-      // the parts are added strictly in block order.
-      const int n_items = groups * M;
-      for (int o = etid; o < n_items; o += kEpiWarps * 32) {
-        const int m = o / groups, r = 4 * (g_lo + o % groups);
-        const float* base = p.partials + m * kRowsPerBlock + r;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int b0 = 0; b0 < nseg; b0 += 8) {
-          float4 t[8];
+  }
+
+  // ---- split row blocks: the block that published a row block's last part adds all of them, in
+  // block order (part q of the row block's k-range is always added q-th), with all its threads.
+  // Blocks that reduce nothing finish here, so their SMs are free for the next kernel early.
+  ptx::tc_fence_before();
+  __syncthreads();  // the acquire of the last part's counter (thread 0 of the epilogue) comes first
+  ptx::tc_fence_after();
+  for (int k = 0; k < *n_red && !*abort_flag; ++k) {
+    const int64_t rb = red_rb[k];
+    const int64_t pf = block_of_unit(rb * S, T, G), pl = block_of_unit(rb * S + S - 1, T, G);
+    const int nseg = (int)(pl - pf + 1);
+    // part slot of block b: 2 b for every b > pf (rb is the first row block of its range);
+    // block pf used slot 2 pf + 1 if its range began in an earlier row block
+    const int pf_bit = unit_begin(pf, T, G) < rb * S ? 1 : 0;
+    const float gs = p.gs;
+    const int M = p.M;
+    // items of 4 rows x 1 activation row; each item's part loads (8 at a time) are issued
+    // before any is used, and the parts are added strictly in block order
+#pragma unroll 1
+    for (int o = threadIdx.x; o < (kRowsPerBlock / 4) * M; o += kThreads) {
+      const int m = o / (kRowsPerBlock / 4), r = 4 * (o % (kRowsPerBlock / 4));
+      const float* base = p.partials + m * kRowsPerBlock + r;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+      for (int b0 = 0; b0 < nseg; b0 += 8) {
+        float4 t[8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if (b0 + j < nseg) {
-              const int64_t b = pf + b0 + j;
-              t[j] = __ldcg(reinterpret_cast<const float4*>(
-                  base + (2 * b + (b == pf ? pf_bit : 0)) * (int64_t)(kNmma * kRowsPerBlock)));
-            }
-          }
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if (b0 + j < nseg) {
-              acc.x += t[j].x;
-              acc.y += t[j].y;
-              acc.z += t[j].z;
-              acc.w += t[j].w;
-            }
+        for (int j = 0; j < 8; ++j) {
+          if (b0 + j < nseg) {
+            const int64_t b = pf + b0 + j;
+            t[j] = __ldcg(reinterpret_cast<const float4*>(
+                base + (2 * b + (b == pf ? pf_bit : 0)) * (int64_t)(kNmma * kRowsPerBlock)));
           }
         }
-        const float v[4] = {acc.x * gs, acc.y * gs, acc.z * gs, acc.w * gs};
-        const int64_t n = rb * kRowsPerBlock + r;
-        if (p.out_f32) {
-          float* yrow = static_cast<float*>(p.y) + (int64_t)m * p.N;
-          if (n + 3 < p.N && (p.N & 3) == 0) {
-            *reinterpret_cast<float4*>(yrow + n) = make_float4(v[0], v[1], v[2], v[3]);
-          } else {
-            for (int c = 0; c < 4; ++c)
-              if (n + c < p.N) yrow[n + c] = v[c];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (b0 + j < nseg) {
+            acc.x += t[j].x;
+            acc.y += t[j].y;
+            acc.z += t[j].z;
+            acc.w += t[j].w;
           }
+        }
+      }
+      const float v[4] = {__fmul_rn(acc.x, gs), __fmul_rn(acc.y, gs), __fmul_rn(acc.z, gs), __fmul_rn(acc.w, gs)};
+      const int64_t n = rb * kRowsPerBlock + r;
+      if (p.out_f32) {
+        float* yrow = static_cast<float*>(p.y) + (int64_t)m * p.N;
+        if (n + 3 < p.N && (p.N & 3) == 0) {
+          *reinterpret_cast<float4*>(yrow + n) = make_float4(v[0], v[1], v[2], v[3]);
         } else {
-          uint16_t* yrow = static_cast<uint16_t*>(p.y) + (int64_t)m * p.N;
-          if (n + 3 < p.N && (p.N & 3) == 0) {
-            const uint32_t lo = (uint32_t)ptx::f32_to_bf16_rn(v[0]) | ((uint32_t)ptx::f32_to_bf16_rn(v[1]) << 16);
-            const uint32_t hi = (uint32_t)ptx::f32_to_bf16_rn(v[2]) | ((uint32_t)ptx::f32_to_bf16_rn(v[3]) << 16);
-            *reinterpret_cast<uint2*>(yrow + n) = make_uint2(lo, hi);
-          } else {
-            for (int c = 0; c < 4; ++c)
-              if (n + c < p.N) yrow[n + c] = ptx::f32_to_bf16_rn(v[c]);
-          }
+          for (int c = 0; c < 4; ++c)
+            if (n + c < p.N) yrow[n + c] = v[c];
+        }
+      } else {
+        uint16_t* yrow = static_cast<uint16_t*>(p.y) + (int64_t)m * p.N;
+        if (n + 3 < p.N && (p.N & 3) == 0) {
+          const uint32_t lo = (uint32_t)ptx::f32_to_bf16_rn(v[0]) | ((uint32_t)ptx::f32_to_bf16_rn(v[1]) << 16);
+          const uint32_t hi = (uint32_t)ptx::f32_to_bf16_rn(v[2]) | ((uint32_t)ptx::f32_to_bf16_rn(v[3]) << 16);
+          *reinterpret_cast<uint2*>(yrow + n) = make_uint2(lo, hi);
+        } else {
+          for (int c = 0; c < 4; ++c)
+            if (n + c < p.N) yrow[n + c] = ptx::f32_to_bf16_rn(v[c]);
         }
       }
     }
