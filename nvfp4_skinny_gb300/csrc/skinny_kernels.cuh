@@ -98,9 +98,9 @@ constexpr int kBarFinal = kBarUnit + kUnitBars;              // [issuer]   MMA d
 constexpr int kNumBars = kBarFinal + kMmaWarps;
 constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
 // misc: +0 tensor-memory base, +4 abort flag, +12 reduce count, +16 stage release counts
-// [kStages], +32 row blocks this block reduces [2] (int64) and their count, +128 xs[32] (2^-e of
-// each activation row), +256 row maxima [32] (bf16 magnitude bits)
-constexpr int kMiscBytes = 256 + kNmma * 4;
+// [kStages], +32 row blocks this block reduces [2] (int64), +128 xs[32] (2^-e of each activation
+// row)
+constexpr int kMiscBytes = 128 + kNmma * 4;
 constexpr uint32_t kNbPrep = 8;                      // epilogue + issuer warps preparing activations
 constexpr uint32_t kNbPrepThreads = 8 * 32;
 constexpr int kSmemBytes = kSmemMisc + kMiscBytes + 1024;  // misc + alignment slack
@@ -338,7 +338,6 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemMisc + 4);
   int* release_cnt = reinterpret_cast<int*>(smem + kSmemMisc + 16);  // [kStages]
   float* xs_smem = reinterpret_cast<float*>(smem + kSmemMisc + 128);  // [32]
-  uint32_t* rowmax_smem = reinterpret_cast<uint32_t*>(smem + kSmemMisc + 256);  // [32]
   int64_t* red_rb = reinterpret_cast<int64_t*>(smem + kSmemMisc + 32);  // [2]
   volatile int* n_red = reinterpret_cast<volatile int*>(smem + kSmemMisc + 12);
 
@@ -390,7 +389,6 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
     for (int q = 0; q < kMmaWarps; ++q) ptx::mbar_init(bar(kBarFinal + q), 1);
     *abort_flag = 0;
     *n_red = 0;
-    for (int m = 0; m < kNmma; ++m) rowmax_smem[m] = 0u;
     ptx::fence_mbar_init();
     // The weights are read-only inputs that no kernel of this stream writes while calls are
     // queued, so they are streamed before the dependency wait on the previous call.
@@ -416,43 +414,32 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
   auto prep_fused = [&](int pw) {
     ptx::grid_dependency_wait();  // x is produced upstream
     const int M = p.M;
-    const int n_items = M * n_local;  // at most 32 * kStages
     const uint64_t pol = ptx::policy_evict_last();
-    // each lane copies its chunk of the warp's items to the chunk's final place in the stage
-    // (all copies in flight at once) and later rewrites the same 16 bytes as fp16: no thread
-    // touches another thread's chunk before the row maxima are combined
-#pragma unroll 1
-    for (int it = pw; it < n_items; it += 8) {
-      const int m = it / n_local, q = it - m * n_local;
-      ptx::cp_async16(smem_base + (uint32_t)(q * kStageBytes + kXOff) + x_chunk_off<NC>(m, lane),
-                      p.x + (int64_t)m * p.K + (int64_t)unit_kstep(q) * kKStep + lane * 8, pol);
-    }
+    // Warp pw owns activation rows pw, pw + 8, ...; lane l owns chunk l (16 bytes) of each of
+    // the row's n_local k-slices.  Every chunk is copied straight to its final place in the
+    // stage (all copies in flight at once) and later rewritten there as fp16 by the same lane,
+    // so no thread touches another's chunk, and a row's maximum is a warp reduction.
+    for (int m = pw; m < M; m += 8)
+      for (int q = 0; q < n_local; ++q)
+        ptx::cp_async16(smem_base + (uint32_t)(q * kStageBytes + kXOff) + x_chunk_off<NC>(m, lane),
+                        p.x + (int64_t)m * p.K + (int64_t)unit_kstep(q) * kKStep + lane * 8, pol);
     ptx::cp_async_commit();
     ptx::cp_async_wait(0);
-#pragma unroll 1
-    for (int it = pw; it < n_items; it += 8) {
-      const int m = it / n_local, q = it - m * n_local;
-      const uint4 v = *reinterpret_cast<const uint4*>(smem + q * kStageBytes + kXOff + x_chunk_off<NC>(m, lane));
-      const uint32_t wm = warp_max_u32(bf16x8_maxmag(v));
-      if (lane == 0) atomicMax(rowmax_smem + m, wm);
-    }
-    ptx::named_bar_sync(kNbPrep, kNbPrepThreads);  // every row's maximum is in
-#pragma unroll 1
-    for (int it = pw; it < NC * n_local; it += 8) {
-      const int m = it / n_local, q = it - m * n_local;
-      uint4* slot = reinterpret_cast<uint4*>(smem + q * kStageBytes + kXOff + x_chunk_off<NC>(m, lane));
-      uint4 o = make_uint4(0u, 0u, 0u, 0u);  // rows M .. NC-1 are zero (their MMA columns are never read)
-      if (m < M) {
-        const uint4 v = *slot;
-        const int e = x_exponent(__uint_as_float(rowmax_smem[m] << 16));  // -112 <= e <= 148
-        o = e <= 127 ? bf16x8_to_f16x8(v, pow2i(e)) : bf16x8_to_f16x8(v, pow2i(e / 2), pow2i(e - e / 2));
+    for (int m = pw; m < NC; m += 8) {
+      uint32_t mx = 0u;
+      if (m < M)
+        for (int q = 0; q < n_local; ++q)
+          mx = max(mx, bf16x8_maxmag(*reinterpret_cast<const uint4*>(smem + q * kStageBytes + kXOff +
+                                                                     x_chunk_off<NC>(m, lane))));
+      const int e = x_exponent(__uint_as_float(warp_max_u32(mx) << 16));  // -112 <= e <= 148
+      const float f1 = pow2i(e <= 127 ? e : e / 2), f2 = pow2i(e <= 127 ? 0 : e - e / 2);
+      for (int q = 0; q < n_local; ++q) {
+        uint4* slot = reinterpret_cast<uint4*>(smem + q * kStageBytes + kXOff + x_chunk_off<NC>(m, lane));
+        // rows M .. NC-1 are zero (their MMA columns are never read)
+        *slot = m >= M ? make_uint4(0u, 0u, 0u, 0u)
+                       : (e <= 127 ? bf16x8_to_f16x8(*slot, f1) : bf16x8_to_f16x8(*slot, f1, f2));
       }
-      *slot = o;
-    }
-    const int t = pw * 32 + lane;
-    if (t < NC) {
-      const int e = x_exponent(__uint_as_float(rowmax_smem[t] << 16));
-      xs_smem[t] = t < M ? pow2i(-(e / 2)) * pow2i(-(e - e / 2)) : 0.f;  // 2^-e, exact
+      if (lane == 0) xs_smem[m] = m < M ? pow2i(-(e / 2)) * pow2i(-(e - e / 2)) : 0.f;  // 2^-e, exact
     }
     ptx::fence_proxy_async_smem();  // operand writes -> the tensor core's (async proxy) reads
     ptx::named_bar_sync(kNbPrep, kNbPrepThreads);  // every operand row in place before any MMA
@@ -687,34 +674,10 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
     const int pf_bit = unit_begin(pf, T, G) < rb * S ? 1 : 0;
     const float gs = p.gs;
     const int M = p.M;
-    // items of 4 rows x 1 activation row; each item's part loads (8 at a time) are issued
-    // before any is used, and the parts are added strictly in block order
-#pragma unroll 1
-    for (int o = threadIdx.x; o < (kRowsPerBlock / 4) * M; o += kThreads) {
-      const int m = o / (kRowsPerBlock / 4), r = 4 * (o % (kRowsPerBlock / 4));
-      const float* base = p.partials + m * kRowsPerBlock + r;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 1
-      for (int b0 = 0; b0 < nseg; b0 += 8) {
-        float4 t[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (b0 + j < nseg) {
-            const int64_t b = pf + b0 + j;
-            t[j] = __ldcg(reinterpret_cast<const float4*>(
-                base + (2 * b + (b == pf ? pf_bit : 0)) * (int64_t)(kNmma * kRowsPerBlock)));
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (b0 + j < nseg) {
-            acc.x += t[j].x;
-            acc.y += t[j].y;
-            acc.z += t[j].z;
-            acc.w += t[j].w;
-          }
-        }
-      }
+    // items of 4 rows x 1 activation row, two per thread and pass; the parts' loads of both
+    // items (up to 8 parts each) are issued before any is used, and the parts are added
+    // strictly in block order
+    auto store4 = [&](int m, int r, float4 acc) {
       const float v[4] = {__fmul_rn(acc.x, gs), __fmul_rn(acc.y, gs), __fmul_rn(acc.z, gs), __fmul_rn(acc.w, gs)};
       const int64_t n = rb * kRowsPerBlock + r;
       if (p.out_f32) {
@@ -736,6 +699,45 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
             if (n + c < p.N) yrow[n + c] = ptx::f32_to_bf16_rn(v[c]);
         }
       }
+    };
+    const int n_items = (kRowsPerBlock / 4) * M;
+#pragma unroll 1
+    for (int o = threadIdx.x; o < n_items; o += 2 * kThreads) {
+      const int o2 = o + kThreads;
+      const bool two = o2 < n_items;
+      const int m0 = o / (kRowsPerBlock / 4), r0 = 4 * (o % (kRowsPerBlock / 4));
+      const int m1 = two ? o2 / (kRowsPerBlock / 4) : m0, r1 = two ? 4 * (o2 % (kRowsPerBlock / 4)) : r0;
+      const float* base0 = p.partials + m0 * kRowsPerBlock + r0;
+      const float* base1 = p.partials + m1 * kRowsPerBlock + r1;
+      float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
+#pragma unroll 1
+      for (int b0 = 0; b0 < nseg; b0 += 8) {
+        float4 t0[8], t1[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (b0 + j < nseg) {
+            const int64_t b = pf + b0 + j;
+            const int64_t off = (2 * b + (b == pf ? pf_bit : 0)) * (int64_t)(kNmma * kRowsPerBlock);
+            t0[j] = __ldcg(reinterpret_cast<const float4*>(base0 + off));
+            if (two) t1[j] = __ldcg(reinterpret_cast<const float4*>(base1 + off));
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (b0 + j < nseg) {
+            acc0.x += t0[j].x;
+            acc0.y += t0[j].y;
+            acc0.z += t0[j].z;
+            acc0.w += t0[j].w;
+            acc1.x += t1[j].x;
+            acc1.y += t1[j].y;
+            acc1.z += t1[j].z;
+            acc1.w += t1[j].w;
+          }
+        }
+      }
+      store4(m0, r0, acc0);
+      if (two) store4(m1, r1, acc1);
     }
   }
 
