@@ -121,6 +121,18 @@ void nvfp4_plan_destroy(nvfp4_plan_t plan);
 nvfp4_status nvfp4_skinny_linear(nvfp4_plan_t plan, const void* x, int M, const uint8_t* w_codes,
                                  const uint8_t* w_block_scales, float w_global_scale, void* y, void* stream);
 
+/* Same, with row strides: row m of x starts lda elements after row m - 1 (lda >= K) and row m
+ * of y ldc elements after row m - 1 (ldc >= N), so x and y may be column slices of wider
+ * row-major buffers (for example one projection's share of a fused output).  lda and ldc must
+ * be multiples of 8 (16-byte row starts); elements between rows are neither read (x) nor
+ * written (y).  Same arithmetic and bits as nvfp4_skinny_linear for every row.  Refused with
+ * NVFP4_ERR_SHAPE (lda < K or ldc < N) or NVFP4_ERR_ALIGN before anything is enqueued.
+ * This is the "pitched lda/ldc" variant of the fused-projection extensions ("Module ops",
+ * w4a16 launchers taking leading dimensions). */
+nvfp4_status nvfp4_skinny_linear_strided(nvfp4_plan_t plan, const void* x, int64_t lda, int M, const uint8_t* w_codes,
+                                         const uint8_t* w_block_scales, float w_global_scale, void* y, int64_t ldc,
+                                         void* stream);
+
 /* Synchronize `stream`, then read and clear the plan's device error word.
  * Returns NVFP4_OK, NVFP4_ERR_TIMEOUT, or NVFP4_ERR_CUDA if the stream
  * reported an error. */

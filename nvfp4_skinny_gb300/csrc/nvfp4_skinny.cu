@@ -113,9 +113,10 @@ cudaError_t set_smem_limits() {
 }
 
 // The two launches of a call (shared by the plan and allocation-free entry points).
-nvfp4_status launch_main(const CUtensorMap& tm_codes, const CUtensorMap& tm_scales, const void* x, int M, float gs,
-                         void* y, float* partials, int* counters, int* err, uint8_t* x16, float* xs, int out_f32,
-                         int grid, int64_t N, int64_t K, int64_t row_blocks, cudaStream_t stream) {
+nvfp4_status launch_main(const CUtensorMap& tm_codes, const CUtensorMap& tm_scales, const void* x, int64_t lda, int M,
+                         float gs, void* y, int64_t ldc, float* partials, int* counters, int* err, uint8_t* x16,
+                         float* xs, int out_f32, int grid, int64_t N, int64_t K, int64_t row_blocks,
+                         cudaStream_t stream) {
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -130,8 +131,8 @@ nvfp4_status launch_main(const CUtensorMap& tm_codes, const CUtensorMap& tm_scal
     pcfg.attrs = attr;
     pcfg.numAttrs = 1;
     const uint16_t* xb = static_cast<const uint16_t*>(x);
-    const cudaError_t pe = nc == 16 ? cudaLaunchKernelEx(&pcfg, nvfp4::x_prep_kernel<16>, xb, M, K, x16, xs)
-                                    : cudaLaunchKernelEx(&pcfg, nvfp4::x_prep_kernel<32>, xb, M, K, x16, xs);
+    const cudaError_t pe = nc == 16 ? cudaLaunchKernelEx(&pcfg, nvfp4::x_prep_kernel<16>, xb, lda, M, K, x16, xs)
+                                    : cudaLaunchKernelEx(&pcfg, nvfp4::x_prep_kernel<32>, xb, lda, M, K, x16, xs);
     if (pe != cudaSuccess) return NVFP4_ERR_CUDA;
   }
 
@@ -139,6 +140,8 @@ nvfp4_status launch_main(const CUtensorMap& tm_codes, const CUtensorMap& tm_scal
   p.tm_codes = tm_codes;
   p.tm_scales = tm_scales;
   p.x = static_cast<const uint16_t*>(x);
+  p.lda = lda;
+  p.ldc = ldc;
   p.x16 = x16;
   p.xs = xs;
   p.fused = fused;
@@ -168,10 +171,10 @@ nvfp4_status launch_main(const CUtensorMap& tm_codes, const CUtensorMap& tm_scal
   return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
-nvfp4_status launch_call(nvfp4_plan* plan, const void* x, int M, const uint8_t* codes, const uint8_t* scales,
-                         float gs, void* y, cudaStream_t stream) {
+nvfp4_status launch_call(nvfp4_plan* plan, const void* x, int64_t lda, int M, const uint8_t* codes,
+                         const uint8_t* scales, float gs, void* y, int64_t ldc, cudaStream_t stream) {
   if (!prepare_tensor_maps(plan, codes, scales)) return NVFP4_ERR_CUDA;  // before anything is enqueued
-  return launch_main(plan->tm_codes, plan->tm_scales, x, M, gs, y, plan->ws.partials, plan->ws.counters,
+  return launch_main(plan->tm_codes, plan->tm_scales, x, lda, M, gs, y, ldc, plan->ws.partials, plan->ws.counters,
                      plan->ws.err, plan->ws.x16, plan->ws.xs, plan->out == NVFP4_OUT_F32 ? 1 : 0, plan->grid,
                      plan->N, plan->K, plan->row_blocks, stream);
 }
@@ -278,7 +281,21 @@ nvfp4_status nvfp4_skinny_linear(nvfp4_plan_t plan, const void* x, int M, const 
   if (!plan || !x || !w_codes || !w_block_scales || !y) return NVFP4_ERR_ARG;
   if (M < 1 || M > NVFP4_MAX_M) return NVFP4_ERR_M_RANGE;
   if (!aligned16(x) || !aligned16(y) || !aligned16(w_codes) || !aligned16(w_block_scales)) return NVFP4_ERR_ALIGN;
-  return launch_call(plan, x, M, w_codes, w_block_scales, w_global_scale, y, static_cast<cudaStream_t>(stream));
+  return launch_call(plan, x, plan->K, M, w_codes, w_block_scales, w_global_scale, y, plan->N,
+                     static_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_skinny_linear_strided(nvfp4_plan_t plan, const void* x, int64_t lda, int M, const uint8_t* w_codes,
+                                         const uint8_t* w_block_scales, float w_global_scale, void* y, int64_t ldc,
+                                         void* stream) {
+  if (!plan || !x || !w_codes || !w_block_scales || !y) return NVFP4_ERR_ARG;
+  if (M < 1 || M > NVFP4_MAX_M) return NVFP4_ERR_M_RANGE;
+  if (lda < plan->K || ldc < plan->N) return NVFP4_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(w_codes) || !aligned16(w_block_scales) || lda % 8 != 0 ||
+      ldc % 8 != 0)
+    return NVFP4_ERR_ALIGN;
+  return launch_call(plan, x, lda, M, w_codes, w_block_scales, w_global_scale, y, ldc,
+                     static_cast<cudaStream_t>(stream));
 }
 
 nvfp4_status nvfp4_plan_check(nvfp4_plan_t plan, void* stream) {
@@ -423,6 +440,6 @@ extern "C" nvfp4_status nvfp4_skinny_linear_noalloc(int64_t N, int64_t K, nvfp4_
       cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess)
     return NVFP4_ERR_CUDA;
 
-  return launch_main(tm_codes, tm_scales, x, M, w_global_scale, y, parts, counters, err, x16, xs,
+  return launch_main(tm_codes, tm_scales, x, K, M, w_global_scale, y, N, parts, counters, err, x16, xs,
                      out_dtype == NVFP4_OUT_F32 ? 1 : 0, (int)grid, N, K, row_blocks, s);
 }

@@ -126,7 +126,8 @@ enum : int { kErrTimeout = 1 };
 struct MainParams {
   CUtensorMap tm_codes;   // uint8 [N rows, K/2 bytes], box 128 B x 256 rows, 128-byte swizzle
   CUtensorMap tm_scales;  // uint8 [N rows, K/16 bytes], box 16 B x 256 rows
-  const uint16_t* x;      // bf16 [M, K] (read when `fused`)
+  const uint16_t* x;      // bf16 [M, K], row stride lda elements (read when `fused`)
+  int64_t lda, ldc;       // row strides of x and y in elements (>= K and >= N)
   const uint8_t* x16;     // fp16 activation operand, one NC-row block of 256 k per k-step (else)
   const float* xs;        // [32] 2^-e per activation row (else)
   int fused;              // every block has at most kStages units: it prepares its own activations
@@ -278,7 +279,7 @@ __device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
 // and reads any further ones again.
 constexpr int kPrepHeld = 8;
 template <int NC>
-__global__ void __launch_bounds__(kPrepThreads) x_prep_kernel(const uint16_t* __restrict__ x, int M, int64_t K,
+__global__ void __launch_bounds__(kPrepThreads) x_prep_kernel(const uint16_t* __restrict__ x, int64_t lda, int M, int64_t K,
                                                               uint8_t* __restrict__ x16, float* __restrict__ xs) {
   ptx::grid_launch_dependents();  // the projection kernel may start streaming its weights
   ptx::grid_dependency_wait();    // x is produced upstream; the operand buffer was read by the previous call
@@ -294,7 +295,7 @@ __global__ void __launch_bounds__(kPrepThreads) x_prep_kernel(const uint16_t* __
     if (tid == 0) xs[m] = 0.f;
     return;
   }
-  const uint4* row = reinterpret_cast<const uint4*>(x + (int64_t)m * K);
+  const uint4* row = reinterpret_cast<const uint4*>(x + (int64_t)m * lda);
   uint4 held[kPrepHeld];
   uint32_t mx = 0u;
 #pragma unroll
@@ -422,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
     for (int m = pw; m < M; m += 8)
       for (int q = 0; q < n_local; ++q)
         ptx::cp_async16(smem_base + (uint32_t)(q * kStageBytes + kXOff) + x_chunk_off<NC>(m, lane),
-                        p.x + (int64_t)m * p.K + (int64_t)unit_kstep(q) * kKStep + lane * 8, pol);
+                        p.x + (int64_t)m * p.lda + (int64_t)unit_kstep(q) * kKStep + lane * 8, pol);
     ptx::cp_async_commit();
     ptx::cp_async_wait(0);
     for (int m = pw; m < NC; m += 8) {
@@ -607,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
       // float stores go to the part (unscaled) or to an fp32 y; bf16 y is the other case
       const bool bf16_out = whole && !p.out_f32;
       const float mul = whole ? gs : 1.f;
-      const int64_t fstride = whole ? p.N : kRowsPerBlock;
+      const int64_t fstride = whole ? p.ldc : kRowsPerBlock;
       float* f0 = whole ? static_cast<float*>(p.y) + n0 : p.partials + (int64_t)slot * (kNmma * kRowsPerBlock) + r0;
       float* f1 = whole ? static_cast<float*>(p.y) + n1 : p.partials + (int64_t)slot * (kNmma * kRowsPerBlock) + r1;
       uint16_t* h0 = static_cast<uint16_t*>(p.y) + n0;
@@ -624,8 +625,8 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
           for (int j = 0; j < 16; ++j) {
             const int64_t m = 16 * cb + j;
             if (m < M) {
-              if (in0) h0[m * p.N] = ptx::f32_to_bf16_rn(__fmul_rn(v0[j], gs));
-              if (in1) h1[m * p.N] = ptx::f32_to_bf16_rn(__fmul_rn(v1[j], gs));
+              if (in0) h0[m * p.ldc] = ptx::f32_to_bf16_rn(__fmul_rn(v0[j], gs));
+              if (in1) h1[m * p.ldc] = ptx::f32_to_bf16_rn(__fmul_rn(v1[j], gs));
             }
           }
         } else {
@@ -681,16 +682,16 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
       const float v[4] = {__fmul_rn(acc.x, gs), __fmul_rn(acc.y, gs), __fmul_rn(acc.z, gs), __fmul_rn(acc.w, gs)};
       const int64_t n = rb * kRowsPerBlock + r;
       if (p.out_f32) {
-        float* yrow = static_cast<float*>(p.y) + (int64_t)m * p.N;
-        if (n + 3 < p.N && (p.N & 3) == 0) {
+        float* yrow = static_cast<float*>(p.y) + (int64_t)m * p.ldc;
+        if (n + 3 < p.N && (p.ldc & 3) == 0) {
           *reinterpret_cast<float4*>(yrow + n) = make_float4(v[0], v[1], v[2], v[3]);
         } else {
           for (int c = 0; c < 4; ++c)
             if (n + c < p.N) yrow[n + c] = v[c];
         }
       } else {
-        uint16_t* yrow = static_cast<uint16_t*>(p.y) + (int64_t)m * p.N;
-        if (n + 3 < p.N && (p.N & 3) == 0) {
+        uint16_t* yrow = static_cast<uint16_t*>(p.y) + (int64_t)m * p.ldc;
+        if (n + 3 < p.N && (p.ldc & 3) == 0) {
           const uint32_t lo = (uint32_t)ptx::f32_to_bf16_rn(v[0]) | ((uint32_t)ptx::f32_to_bf16_rn(v[1]) << 16);
           const uint32_t hi = (uint32_t)ptx::f32_to_bf16_rn(v[2]) | ((uint32_t)ptx::f32_to_bf16_rn(v[3]) << 16);
           *reinterpret_cast<uint2*>(yrow + n) = make_uint2(lo, hi);

@@ -188,6 +188,43 @@ def test_back_to_back_different_plans():
         assert torch.equal(queued[i + len(shapes)], alone[i])
 
 
+# ------------------------------------------------------------------ row strides (pitched x and y)
+
+@pytest.mark.parametrize("N,K,M", [(5120, 5120, 3), (34816, 5120, 17), (300, 768, 32)])
+def test_strided_slices_match_contiguous_bitwise(N, K, M):
+    """x and y as column slices of wider row-major buffers: the same bits as the contiguous
+    call for every row, and nothing outside the slices is written."""
+    plan = _plan(N, K)
+    case = Case(N, K, M, seed=N + M)
+    y_ref = case.run(plan)
+    lda, ldc, x_off, y_off = K + 264, -(-N // 8) * 8 + 136, 8, 16  # row strides (lda + x_off, ldc + y_off) % 8 == 0
+    xw = torch.zeros((M, lda + x_off), dtype=torch.bfloat16, device="cuda")
+    xw[:, x_off:x_off + K] = case.d_x
+    sentinel = torch.tensor(-7.0, dtype=torch.bfloat16)
+    yw = torch.full((M, ldc + y_off), float(sentinel), dtype=torch.bfloat16, device="cuda")
+    row = lda + x_off
+    nb.nvfp4_skinny_linear_strided(plan, xw.view(-1)[x_off:], row, M, case.d_codes, case.d_scales, case.gs,
+                                   yw.view(-1)[y_off:], ldc + y_off)
+    torch.cuda.synchronize()
+    assert nb.nvfp4_plan_check(plan) == nb.NVFP4_OK
+    assert torch.equal(yw[:, y_off:y_off + N], y_ref)
+    assert bool((yw[:, :y_off] == sentinel).all()) and bool((yw[:, y_off + N:] == sentinel).all())
+
+
+def test_strided_argument_errors():
+    plan = _plan(256, 512)
+    case = Case(256, 512, 2, seed=3)
+    y = torch.empty((2, 512), dtype=torch.bfloat16, device="cuda")
+    xw = torch.zeros((2, 1024), dtype=torch.bfloat16, device="cuda")
+    call = lambda lda, ldc, xx=xw: nb.nvfp4_skinny_linear_strided(plan, xx, lda, 2, case.d_codes, case.d_scales,
+                                                                 case.gs, y, ldc, check=False)
+    assert call(256, 512) == nb.NVFP4_ERR_SHAPE        # lda < K
+    assert call(512, 128) == nb.NVFP4_ERR_SHAPE        # ldc < N
+    assert call(516, 512) == nb.NVFP4_ERR_ALIGN        # lda not a multiple of 8
+    assert call(512, 260) == nb.NVFP4_ERR_ALIGN        # ldc not a multiple of 8
+    assert call(1024, 512) == nb.NVFP4_OK
+
+
 # ------------------------------------------------------------------ N-sharding (replicas path)
 
 @pytest.mark.parametrize("cuts", [(2560,), (2000, 3100)])
