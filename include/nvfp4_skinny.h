@@ -133,6 +133,17 @@ nvfp4_status nvfp4_skinny_linear_strided(nvfp4_plan_t plan, const void* x, int64
                                          const uint8_t* w_block_scales, float w_global_scale, void* y, int64_t ldc,
                                          void* stream);
 
+/* The down projection of a gated MLP, with its activation formed on the fly: row m of
+ * gate_up is [gate (K elements) | up (K elements)] (row stride ld_gate_up >= 2 K, a multiple of
+ * 8), as written by a [gate | up] projection, and the projection's input is
+ *   x[m, k] = bfloat16( silu(gate[m, k]) * up[m, k] ),  silu(g) = g / (1 + e^-g),
+ * computed in fp32 and rounded to nearest-even bfloat16 ("Module ops": the SiLU-times-up input
+ * of the fused MLP launchers).  y as in nvfp4_skinny_linear_strided.  Always two launches
+ * (activation preparation, then the projection); rows are bit-identical across M. */
+nvfp4_status nvfp4_skinny_linear_silu_mul(nvfp4_plan_t plan, const void* gate_up, int64_t ld_gate_up, int M,
+                                          const uint8_t* w_codes, const uint8_t* w_block_scales, float w_global_scale,
+                                          void* y, int64_t ldc, void* stream);
+
 /* Synchronize `stream`, then read and clear the plan's device error word.
  * Returns NVFP4_OK, NVFP4_ERR_TIMEOUT, or NVFP4_ERR_CUDA if the stream
  * reported an error. */

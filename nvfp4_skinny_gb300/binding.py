@@ -35,7 +35,7 @@ NVFP4_PACK_ERR_VALUE = -2
 # every symbol the headers declare, per library
 CUDA_SYMBOLS = ("nvfp4_status_string", "nvfp4_abi_version", "nvfp4_plan_create", "nvfp4_plan_create_ex",
                 "nvfp4_plan_destroy", "nvfp4_skinny_linear", "nvfp4_plan_check", "nvfp4_plan_get_info",
-                "nvfp4_skinny_linear_noalloc", "nvfp4_skinny_linear_strided")
+                "nvfp4_skinny_linear_noalloc", "nvfp4_skinny_linear_strided", "nvfp4_skinny_linear_silu_mul")
 PACK_SYMBOLS = ("nvfp4_pack_codes", "nvfp4_unpack_codes", "nvfp4_e4m3_encode")
 
 
@@ -91,6 +91,8 @@ def cuda_lib():
         lib.nvfp4_plan_get_info.argtypes = [p, ctypes.POINTER(PlanInfo)]
         lib.nvfp4_skinny_linear_strided.restype = i32
         lib.nvfp4_skinny_linear_strided.argtypes = [p, p, i64, i32, p, p, ctypes.c_float, p, i64, p]
+        lib.nvfp4_skinny_linear_silu_mul.restype = i32
+        lib.nvfp4_skinny_linear_silu_mul.argtypes = [p, p, i64, i32, p, p, ctypes.c_float, p, i64, p]
         lib.nvfp4_skinny_linear_noalloc.restype = i32
         lib.nvfp4_skinny_linear_noalloc.argtypes = [i64, i64, i32, p, i32, p, p, ctypes.c_float, p, p]
         _cuda = lib
@@ -214,6 +216,18 @@ def nvfp4_skinny_linear_strided(plan, x, lda, M, w_codes, w_block_scales, w_glob
                                                 float(w_global_scale), _ptr(y), int(ldc), _stream(stream))
     if check:
         _check(st, "nvfp4_skinny_linear_strided")
+    return st
+
+
+def nvfp4_skinny_linear_silu_mul(plan, gate_up, ld_gate_up, M, w_codes, w_block_scales, w_global_scale, y, ldc,
+                                 stream=None, check=True):
+    """Down projection of a gated MLP: the input is bf16(silu(gate) * up) of a [gate | up] row."""
+    st = cuda_lib().nvfp4_skinny_linear_silu_mul(plan.as_parameter if isinstance(plan, Plan) else plan,
+                                                 _ptr(gate_up), int(ld_gate_up), int(M), _ptr(w_codes),
+                                                 _ptr(w_block_scales), float(w_global_scale), _ptr(y), int(ldc),
+                                                 _stream(stream))
+    if check:
+        _check(st, "nvfp4_skinny_linear_silu_mul")
     return st
 
 

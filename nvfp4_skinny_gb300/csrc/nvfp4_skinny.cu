@@ -116,13 +116,14 @@ cudaError_t set_smem_limits() {
 nvfp4_status launch_main(const CUtensorMap& tm_codes, const CUtensorMap& tm_scales, const void* x, int64_t lda, int M,
                          float gs, void* y, int64_t ldc, float* partials, int* counters, int* err, uint8_t* x16,
                          float* xs, int out_f32, int grid, int64_t N, int64_t K, int64_t row_blocks,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, int silu_mul = 0) {
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
 
   const int nc = M <= 16 ? 16 : 32;
-  const int fused = fused_mode(row_blocks, K, grid);
+  // the gated-activation input is always prepared by x_prep_kernel (one exponent per row over K)
+  const int fused = silu_mul ? 0 : fused_mode(row_blocks, K, grid);
   if (!fused) {
     cudaLaunchConfig_t pcfg = {};
     pcfg.gridDim = dim3((unsigned)nc);
@@ -131,8 +132,8 @@ nvfp4_status launch_main(const CUtensorMap& tm_codes, const CUtensorMap& tm_scal
     pcfg.attrs = attr;
     pcfg.numAttrs = 1;
     const uint16_t* xb = static_cast<const uint16_t*>(x);
-    const cudaError_t pe = nc == 16 ? cudaLaunchKernelEx(&pcfg, nvfp4::x_prep_kernel<16>, xb, lda, M, K, x16, xs)
-                                    : cudaLaunchKernelEx(&pcfg, nvfp4::x_prep_kernel<32>, xb, lda, M, K, x16, xs);
+    const cudaError_t pe = nc == 16 ? cudaLaunchKernelEx(&pcfg, nvfp4::x_prep_kernel<16>, xb, lda, M, K, silu_mul, x16, xs)
+                                    : cudaLaunchKernelEx(&pcfg, nvfp4::x_prep_kernel<32>, xb, lda, M, K, silu_mul, x16, xs);
     if (pe != cudaSuccess) return NVFP4_ERR_CUDA;
   }
 
@@ -172,11 +173,12 @@ nvfp4_status launch_main(const CUtensorMap& tm_codes, const CUtensorMap& tm_scal
 }
 
 nvfp4_status launch_call(nvfp4_plan* plan, const void* x, int64_t lda, int M, const uint8_t* codes,
-                         const uint8_t* scales, float gs, void* y, int64_t ldc, cudaStream_t stream) {
+                         const uint8_t* scales, float gs, void* y, int64_t ldc, cudaStream_t stream,
+                         int silu_mul = 0) {
   if (!prepare_tensor_maps(plan, codes, scales)) return NVFP4_ERR_CUDA;  // before anything is enqueued
   return launch_main(plan->tm_codes, plan->tm_scales, x, lda, M, gs, y, ldc, plan->ws.partials, plan->ws.counters,
                      plan->ws.err, plan->ws.x16, plan->ws.xs, plan->out == NVFP4_OUT_F32 ? 1 : 0, plan->grid,
-                     plan->N, plan->K, plan->row_blocks, stream);
+                     plan->N, plan->K, plan->row_blocks, stream, silu_mul);
 }
 
 }  // namespace
@@ -296,6 +298,19 @@ nvfp4_status nvfp4_skinny_linear_strided(nvfp4_plan_t plan, const void* x, int64
     return NVFP4_ERR_ALIGN;
   return launch_call(plan, x, lda, M, w_codes, w_block_scales, w_global_scale, y, ldc,
                      static_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_skinny_linear_silu_mul(nvfp4_plan_t plan, const void* gate_up, int64_t ld_gate_up, int M,
+                                          const uint8_t* w_codes, const uint8_t* w_block_scales, float w_global_scale,
+                                          void* y, int64_t ldc, void* stream) {
+  if (!plan || !gate_up || !w_codes || !w_block_scales || !y) return NVFP4_ERR_ARG;
+  if (M < 1 || M > NVFP4_MAX_M) return NVFP4_ERR_M_RANGE;
+  if (ld_gate_up < 2 * plan->K || ldc < plan->N) return NVFP4_ERR_SHAPE;
+  if (!aligned16(gate_up) || !aligned16(y) || !aligned16(w_codes) || !aligned16(w_block_scales) ||
+      ld_gate_up % 8 != 0 || ldc % 8 != 0)
+    return NVFP4_ERR_ALIGN;
+  return launch_call(plan, gate_up, ld_gate_up, M, w_codes, w_block_scales, w_global_scale, y, ldc,
+                     static_cast<cudaStream_t>(stream), 1);
 }
 
 nvfp4_status nvfp4_plan_check(nvfp4_plan_t plan, void* stream) {

@@ -278,9 +278,26 @@ __device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
 // its bits).  Each thread keeps its first kPrepHeld chunks in registers between the two passes
 // and reads any further ones again.
 constexpr int kPrepHeld = 8;
+// x[m, k] = bf16(silu(g) * u) with g = in[m, k] and u = in[m, K + k], in fp32 (silu(g) = g / (1 + e^-g)),
+// for the activation of a gated MLP read straight from a [gate | up] projection output.
+__device__ __forceinline__ uint4 bf16x8_silu_mul(uint4 g, uint4 u) {
+  const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {u.x, u.y, u.z, u.w};
+  uint32_t r[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float g0 = __uint_as_float(gw[q] << 16), g1 = __uint_as_float(gw[q] & 0xFFFF0000u);
+    const float u0 = __uint_as_float(uw[q] << 16), u1 = __uint_as_float(uw[q] & 0xFFFF0000u);
+    const float x0 = __fmul_rn(__fdiv_rn(g0, __fadd_rn(1.f, expf(-g0))), u0);
+    const float x1 = __fmul_rn(__fdiv_rn(g1, __fadd_rn(1.f, expf(-g1))), u1);
+    r[q] = (uint32_t)ptx::f32_to_bf16_rn(x0) | ((uint32_t)ptx::f32_to_bf16_rn(x1) << 16);
+  }
+  return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
 template <int NC>
 __global__ void __launch_bounds__(kPrepThreads) x_prep_kernel(const uint16_t* __restrict__ x, int64_t lda, int M, int64_t K,
-                                                              uint8_t* __restrict__ x16, float* __restrict__ xs) {
+                                                              int silu_mul, uint8_t* __restrict__ x16,
+                                                              float* __restrict__ xs) {
   ptx::grid_launch_dependents();  // the projection kernel may start streaming its weights
   ptx::grid_dependency_wait();    // x is produced upstream; the operand buffer was read by the previous call
   __shared__ uint32_t wmax[kPrepThreads / 32];
@@ -296,15 +313,17 @@ __global__ void __launch_bounds__(kPrepThreads) x_prep_kernel(const uint16_t* __
     return;
   }
   const uint4* row = reinterpret_cast<const uint4*>(x + (int64_t)m * lda);
+  const uint4* urow = row + chunks;  // the up half of a [gate | up] row
+  auto load = [&](int64_t c) { return silu_mul ? bf16x8_silu_mul(__ldg(row + c), __ldg(urow + c)) : __ldg(row + c); };
   uint4 held[kPrepHeld];
   uint32_t mx = 0u;
 #pragma unroll
   for (int k = 0; k < kPrepHeld; ++k) {
     const int64_t c = tid + (int64_t)k * kPrepThreads;
-    held[k] = c < chunks ? __ldg(row + c) : make_uint4(0u, 0u, 0u, 0u);
+    held[k] = c < chunks ? load(c) : make_uint4(0u, 0u, 0u, 0u);
     mx = max(mx, bf16x8_maxmag(held[k]));
   }
-  for (int64_t c = tid + (int64_t)kPrepHeld * kPrepThreads; c < chunks; c += kPrepThreads) mx = max(mx, bf16x8_maxmag(__ldg(row + c)));
+  for (int64_t c = tid + (int64_t)kPrepHeld * kPrepThreads; c < chunks; c += kPrepThreads) mx = max(mx, bf16x8_maxmag(load(c)));
   const uint32_t wm = warp_max_u32(mx);
   if ((tid & 31) == 0) wmax[tid >> 5] = wm;
   __syncthreads();
@@ -320,7 +339,7 @@ __global__ void __launch_bounds__(kPrepThreads) x_prep_kernel(const uint16_t* __
     if (c < chunks) *dst(c) = e <= 127 ? bf16x8_to_f16x8(held[k], f1) : bf16x8_to_f16x8(held[k], f1, f2);
   }
   for (int64_t c = tid + (int64_t)kPrepHeld * kPrepThreads; c < chunks; c += kPrepThreads) {
-    const uint4 v = __ldg(row + c);
+    const uint4 v = load(c);
     *dst(c) = e <= 127 ? bf16x8_to_f16x8(v, f1) : bf16x8_to_f16x8(v, f1, f2);
   }
 }

@@ -172,4 +172,26 @@ def max_threads():
     return default().max_threads()
 
 
-__all__ = ["Oracle", "default", "e2m1", "e4m3", "bf16", "weight", "linear", "linear_at", "bf16_ulp", "tolerance", "max_threads"]
+def silu_mul_bf16(gate_up_bits, K: int) -> np.ndarray:
+    """Input of the gated-MLP down projection: x[m, k] = bf16(silu(g) * u) with g = row[k] and
+    u = row[K + k] of a [gate | up] bfloat16 row ("Module ops", the SiLU-times-up input of the
+    fused MLP launchers).  silu(g) = g / (1 + e^-g).
+
+    The bfloat16 rounding of x is a decision taken in the GPU path's precision (fp32 operations,
+    each rounded to nearest), so it is taken here in fp32 too; only the exponential may differ
+    from the GPU's by an ulp, which can move x by at most one bfloat16 ulp.
+
+    gate_up_bits: uint16 [M, >= 2K] (bfloat16 bits).  Returns uint16 [M, K] (bfloat16 bits)."""
+    gu = np.ascontiguousarray(gate_up_bits, dtype=np.uint16)
+    g = (gu[:, :K].astype(np.uint32) << 16).view(np.float32)
+    u = (gu[:, K:2 * K].astype(np.uint32) << 16).view(np.float32)
+    with np.errstate(over="ignore"):
+        den = np.float32(1.0) + np.exp(-g, dtype=np.float32)
+    x = (g / den).astype(np.float32) * u
+    bits = x.astype(np.float32).view(np.uint32)
+    rounded = (bits + np.uint32(0x7FFF) + ((bits >> 16) & np.uint32(1))) >> 16   # nearest-even (finite x)
+    return rounded.astype(np.uint16)
+
+
+__all__ = ["Oracle", "default", "e2m1", "e4m3", "bf16", "weight", "linear", "linear_at", "bf16_ulp", "tolerance",
+           "max_threads", "silu_mul_bf16"]

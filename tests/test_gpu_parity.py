@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_cases import Case, to_f64, within_tolerance
+from gpu_cases import Case, bf16_bits, to_f64, within_tolerance
 from nvfp4_skinny_gb300 import binding as nb
 from nvfp4_skinny_gb300 import synth
 
@@ -223,6 +223,57 @@ def test_strided_argument_errors():
     assert call(516, 512) == nb.NVFP4_ERR_ALIGN        # lda not a multiple of 8
     assert call(512, 260) == nb.NVFP4_ERR_ALIGN        # ldc not a multiple of 8
     assert call(1024, 512) == nb.NVFP4_OK
+
+
+# ------------------------------------------------------------------ gated-MLP input (silu(gate) * up)
+
+def _gate_up(M, K, seed):
+    gen = torch.Generator().manual_seed(seed)
+    return (torch.randn((M, 2 * K), generator=gen) * 2).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("N,K,M", [(256, 512, 5), (640, 1024, 17), (5120, 17408, 8)])
+def test_silu_mul_input(N, K, M):
+    """The down projection fed by a [gate | up] row: every sampled element within the
+    tolerance of the oracle applied to x = bf16(silu(gate) * up)."""
+    gu = _gate_up(M, K, seed=N + M)
+    x_bits = oracle.silu_mul_bf16(bf16_bits(gu), K)
+    x = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16)
+    case = Case(N, K, M, seed=N + K, x=x)
+    plan = _plan(N, K)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    nb.nvfp4_skinny_linear_silu_mul(plan, gu.cuda(), 2 * K, M, case.d_codes, case.d_scales, case.gs, y, N)
+    torch.cuda.synchronize()
+    assert nb.nvfp4_plan_check(plan) == nb.NVFP4_OK
+    if N * K <= 1 << 20:
+        y_ref, absdot = case.oracle_full()
+        ok, ratio = within_tolerance(to_f64(y), y_ref, absdot)
+    else:
+        rng = np.random.default_rng(M)
+        ms, ns = rng.integers(0, M, 256), rng.integers(0, N, 256)
+        y_ref, absdot = case.oracle_at(ms, ns)
+        ok, ratio = within_tolerance(to_f64(y)[ms, ns], y_ref, absdot)
+    assert ok, ratio
+
+
+def test_silu_mul_row_invariance_and_refusals():
+    N, K = 5120, 5120
+    plan = _plan(N, K)
+    case = Case(N, K, 1, seed=8)
+    gu = _gate_up(32, K, seed=9).cuda()
+    y32 = torch.empty((32, N), dtype=torch.bfloat16, device="cuda")
+    nb.nvfp4_skinny_linear_silu_mul(plan, gu, 2 * K, 32, case.d_codes, case.d_scales, case.gs, y32, N)
+    for r in (0, 7, 31):
+        y1 = torch.empty((1, N), dtype=torch.bfloat16, device="cuda")
+        nb.nvfp4_skinny_linear_silu_mul(plan, gu[r:r + 1].contiguous(), 2 * K, 1, case.d_codes, case.d_scales,
+                                        case.gs, y1, N)
+        torch.cuda.synchronize()
+        assert torch.equal(y1[0], y32[r])
+    call = lambda ld, ldc: nb.nvfp4_skinny_linear_silu_mul(plan, gu, ld, 2, case.d_codes, case.d_scales, case.gs,
+                                                           y32, ldc, check=False)
+    assert call(K, N) == nb.NVFP4_ERR_SHAPE           # the row holds gate and up: ld >= 2 K
+    assert call(2 * K + 4, N) == nb.NVFP4_ERR_ALIGN
+    assert nb.nvfp4_plan_check(plan) == nb.NVFP4_OK
 
 
 # ------------------------------------------------------------------ N-sharding (replicas path)
