@@ -93,7 +93,13 @@ constexpr int kBarFull = 0;                                  // [kStages]  weigh
 constexpr int kBarXFull = kBarFull + kStages;                // [kStages]  activation copy (tx) -> decoders
 constexpr int kBarAEmpty = kBarXFull + kStages;              // [half][tile]  MMA commit -> decoders
 constexpr int kBarUnit = kBarAEmpty + kHalves * kTiles;      // [4]        4 MMA commits per unit -> epilogue
+// The epilogue waits on unit i's barrier (i % 4) in unit order.  The MMAs can never run four
+// units ahead of those waits, so a barrier's parity cannot alias:
+// - with more than kStages units, unit i + 4's activation copy is issued only after the wait on
+//   unit i, and the decoders release unit i + 4's MMAs only once that copy has landed;
+// - in fused mode there are at most kStages (= 4) units.
 constexpr int kUnitBars = 4;
+static_assert(kUnitBars == kStages, "the Unit-barrier ring is as deep as the activation copies run ahead");
 constexpr int kBarFinal = kBarUnit + kUnitBars;              // [issuer]   MMA drain at exit
 constexpr int kNumBars = kBarFinal + kMmaWarps;
 constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
