@@ -144,6 +144,19 @@ nvfp4_status nvfp4_skinny_linear_silu_mul(nvfp4_plan_t plan, const void* gate_up
                                           const uint8_t* w_codes, const uint8_t* w_block_scales, float w_global_scale,
                                           void* y, int64_t ldc, void* stream);
 
+/* Quantize a bfloat16 weight w [rows, K] (row stride ldw >= K elements, a multiple of 8; w
+ * 16-byte aligned) to NVFP4 on `stream`: packed E2M1 codes w_codes [rows, K/2] (low nibble =
+ * even k; 8-byte aligned) and one E4M3 byte per 16 elements w_block_scales [rows, K/16], for
+ * the per-tensor scale w_global_scale (> 0; 1.0 is the pages' choice).  K must be a multiple of
+ * 16.  Per 16-element block, in fp32 operations rounded to nearest:
+ *   scale = E4M3(amax / 6 / w_global_scale)           nearest, ties to even, saturating at 448
+ *   code  = E2M1(x / (scale * w_global_scale))        nearest, ties to even, saturating at 6;
+ * a block whose scale is 0 gets codes 0, and a magnitude that rounds to 0 gets code 0 (+0)
+ * ("Module ops", quantize_bf16_to_nvfp4).  Asynchronous; no allocation.  Argument errors are
+ * refused before anything is enqueued. */
+nvfp4_status nvfp4_quantize_bf16(const void* w, int64_t rows, int64_t K, int64_t ldw, float w_global_scale,
+                                 uint8_t* w_codes, uint8_t* w_block_scales, void* stream);
+
 /* Synchronize `stream`, then read and clear the plan's device error word.
  * Returns NVFP4_OK, NVFP4_ERR_TIMEOUT, or NVFP4_ERR_CUDA if the stream
  * reported an error. */

@@ -35,7 +35,8 @@ NVFP4_PACK_ERR_VALUE = -2
 # every symbol the headers declare, per library
 CUDA_SYMBOLS = ("nvfp4_status_string", "nvfp4_abi_version", "nvfp4_plan_create", "nvfp4_plan_create_ex",
                 "nvfp4_plan_destroy", "nvfp4_skinny_linear", "nvfp4_plan_check", "nvfp4_plan_get_info",
-                "nvfp4_skinny_linear_noalloc", "nvfp4_skinny_linear_strided", "nvfp4_skinny_linear_silu_mul")
+                "nvfp4_skinny_linear_noalloc", "nvfp4_skinny_linear_strided", "nvfp4_skinny_linear_silu_mul",
+                "nvfp4_quantize_bf16")
 PACK_SYMBOLS = ("nvfp4_pack_codes", "nvfp4_unpack_codes", "nvfp4_e4m3_encode")
 
 
@@ -93,6 +94,8 @@ def cuda_lib():
         lib.nvfp4_skinny_linear_strided.argtypes = [p, p, i64, i32, p, p, ctypes.c_float, p, i64, p]
         lib.nvfp4_skinny_linear_silu_mul.restype = i32
         lib.nvfp4_skinny_linear_silu_mul.argtypes = [p, p, i64, i32, p, p, ctypes.c_float, p, i64, p]
+        lib.nvfp4_quantize_bf16.restype = i32
+        lib.nvfp4_quantize_bf16.argtypes = [p, i64, i64, i64, ctypes.c_float, p, p, p]
         lib.nvfp4_skinny_linear_noalloc.restype = i32
         lib.nvfp4_skinny_linear_noalloc.argtypes = [i64, i64, i32, p, i32, p, p, ctypes.c_float, p, p]
         _cuda = lib
@@ -227,7 +230,17 @@ def nvfp4_skinny_linear_silu_mul(plan, gate_up, ld_gate_up, M, w_codes, w_block_
                                                  _ptr(w_block_scales), float(w_global_scale), _ptr(y), int(ldc),
                                                  _stream(stream))
     if check:
-        _check(st, "nvfp4_skinny_linear_silu_mul")
+        _check(st, "nvfp4_skinny_linear_silu_mul",
+                "nvfp4_quantize_bf16")
+    return st
+
+
+def nvfp4_quantize_bf16(w, rows, K, ldw, w_global_scale, w_codes, w_block_scales, stream=None, check=True):
+    """Quantize a bfloat16 [rows, K] weight (row stride ldw) to NVFP4 codes and block scales."""
+    st = cuda_lib().nvfp4_quantize_bf16(_ptr(w), int(rows), int(K), int(ldw), float(w_global_scale), _ptr(w_codes),
+                                        _ptr(w_block_scales), _stream(stream))
+    if check:
+        _check(st, "nvfp4_quantize_bf16")
     return st
 
 

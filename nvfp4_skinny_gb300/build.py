@@ -17,8 +17,8 @@ OUT = os.path.join(HERE, "_build")
 CUDA_LIB = os.path.join(OUT, "libnvfp4skinny.so")
 PACK_LIB = os.path.join(OUT, "libnvfp4pack.so")
 
-CUDA_SOURCES = ["nvfp4_skinny.cu"]
-CUDA_DEPS = ["nvfp4_skinny.cu", "skinny_kernels.cuh", "ptx.cuh"]
+CUDA_SOURCES = ["nvfp4_skinny.cu", "quantize.cu"]
+CUDA_DEPS = ["nvfp4_skinny.cu", "quantize.cu", "skinny_kernels.cuh", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -193,5 +193,52 @@ def silu_mul_bf16(gate_up_bits, K: int) -> np.ndarray:
     return rounded.astype(np.uint16)
 
 
+def _nearest_even(values_sorted, codes_sorted, v):
+    """Index into codes_sorted of the value nearest to each v (v within [min, max] of the table);
+    ties go to the even code.  Distances are compared in binary64, exact for these operands."""
+    v = np.asarray(v, np.float64)
+    hi = np.clip(np.searchsorted(values_sorted, v, side="left"), 0, len(values_sorted) - 1)
+    lo = np.clip(hi - 1, 0, len(values_sorted) - 1)
+    dl = np.abs(v - values_sorted[lo])
+    dh = np.abs(values_sorted[hi] - v)
+    pick_hi = (dh < dl) | ((dh == dl) & (codes_sorted[hi] % 2 == 0) & (codes_sorted[lo] % 2 == 1))
+    return np.where(pick_hi, codes_sorted[hi], codes_sorted[lo])
+
+
+def quantize_nvfp4(w_bits, gs: float):
+    """BF16 weight -> NVFP4 ("Module ops", quantize_bf16_to_nvfp4), the plainest reading of the
+    unprinted rules: per 16-element block, scale = E4M3(amax / 6 / gs) and code = E2M1(x /
+    (scale * gs)), each the nearest representable value with ties to the even code, saturating
+    at 448 and 6; a zero scale gives codes 0; a code whose magnitude is 0 is +0.  The divisions
+    and the product are fp32 operations rounded to nearest, the precision in which the GPU path
+    takes the same rounding decisions; the nearest-value searches run over the formats' value
+    tables, decoded by this oracle.
+
+    w_bits: uint16 [rows, K] (bfloat16 bits), K a multiple of 16.  Returns (codes uint8
+    [rows, K/2] with the low nibble the even k, scales uint8 [rows, K/16])."""
+    w_bits = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    rows, K = w_bits.shape
+    assert K % 16 == 0
+    x = (w_bits.astype(np.uint32) << 16).view(np.float32).reshape(rows, K // 16, 16)
+    gs32 = np.float32(gs)
+    amax = np.abs(x).max(axis=2)
+    s = (amax / np.float32(6.0)).astype(np.float32) / gs32
+    # E4M3 table of the finite non-negative bytes 0x00..0x7E, in increasing order
+    e4_codes = np.arange(0x7F)
+    e4_vals = np.array([e4m3(int(c)) for c in e4_codes], np.float64)
+    s64 = np.minimum(s.astype(np.float64), 448.0)
+    sc = _nearest_even(e4_vals, e4_codes, s64).astype(np.uint8)
+    d = (e4_vals[sc].astype(np.float32) * gs32).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = (x / d[:, :, None]).astype(np.float32)
+    e2_codes = np.arange(8)
+    e2_vals = np.array([e2m1(int(c)) for c in e2_codes], np.float64)
+    mag = _nearest_even(e2_vals, e2_codes, np.minimum(np.abs(q.astype(np.float64)), 6.0))
+    code = np.where((mag != 0) & (q < 0), mag | 8, mag)
+    code = np.where(d[:, :, None] > 0, code, 0).astype(np.uint8).reshape(rows, K)
+    packed = (code[:, 0::2] | (code[:, 1::2] << 4)).astype(np.uint8)
+    return packed, sc
+
+
 __all__ = ["Oracle", "default", "e2m1", "e4m3", "bf16", "weight", "linear", "linear_at", "bf16_ulp", "tolerance",
-           "max_threads", "silu_mul_bf16"]
+           "max_threads", "silu_mul_bf16", "quantize_nvfp4"]

@@ -48,3 +48,68 @@ def test_silu_mul_odd_part_identity():
     fn = (neg.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     err = np.abs((fp - fn) - g.astype(np.float64))
     assert np.all(err <= 2.0 ** -8 * (np.abs(fp) + np.abs(fn)) + 1e-30)
+
+
+# ------------------------------------------------------------------ BF16 -> NVFP4 quantizer
+
+def _to_bf16_bits(a):
+    return (np.asarray(a, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def test_quantizer_e2m1_rounding_brute_force():
+    """Every E2M1 rounding decision against exact rationals: the nearest of the eight
+    magnitudes, ties to the even code, saturation above 6 (one element per block, so the
+    block scale is fixed by a second element of magnitude 6)."""
+    from fractions import Fraction
+    vals = [Fraction(v) for v in (0, 0.5, 1, 1.5, 2, 3, 4, 6)]
+    probes = sorted({Fraction(i, 16) for i in range(0, 97)})  # 0 .. 6 in steps of 1/16: every tie
+    x = np.zeros((len(probes), 16), np.float32)
+    x[:, 0] = [float(p) for p in probes]
+    x[:, 1] = 6.0  # amax = 6 -> scale 1 with gs = 1
+    codes, scales = oracle.quantize_nvfp4(_to_bf16_bits(x), 1.0)
+    assert np.all(scales == 0x38)  # E4M3 1.0
+    got = codes[:, 0] & 0xF
+    for p, c in zip(probes, got):
+        best = min(range(8), key=lambda i: (abs(vals[i] - p), i % 2))
+        assert c == best, (p, c, best)
+    # the same magnitudes negated carry the sign bit, except those that round to 0
+    codes_n, _ = oracle.quantize_nvfp4(_to_bf16_bits(-x), 1.0)
+    for c, cn in zip(got, codes_n[:, 0] & 0xF):
+        assert cn == (c | 8 if c else 0)
+
+
+def test_quantizer_round_trip_of_representable_blocks():
+    """Blocks built as code x E4M3 scale x gs with a +-6 in every block (so the block's amax
+    fixes the same scale) quantize back to the same codes and scales."""
+    rng = np.random.default_rng(21)
+    rows, K = 6, 64
+    for gs in (1.0, 0.25):
+        sc = rng.integers(0x20, 0x60, (rows, K // 16)).astype(np.uint8)
+        code = rng.integers(0, 16, (rows, K)).astype(np.uint8)
+        code[code == 8] = 0                                  # -0 comes back as +0
+        code[:, ::16] = np.where(rng.random((rows, K // 16)) < 0.5, 7, 15)  # a +-6 per block
+        sv = np.array([oracle.e4m3(int(b)) for b in sc.ravel()]).reshape(sc.shape)
+        cv = np.array([oracle.e2m1(int(c)) for c in code.ravel()]).reshape(code.shape)
+        w = (cv.reshape(rows, K // 16, 16) * sv[:, :, None] * gs).reshape(rows, K).astype(np.float32)
+        packed, scales = oracle.quantize_nvfp4(_to_bf16_bits(w), gs)
+        assert np.array_equal(scales, sc)
+        unpacked = np.empty((rows, K), np.uint8)
+        unpacked[:, 0::2] = packed & 0xF
+        unpacked[:, 1::2] = packed >> 4
+        assert np.array_equal(unpacked, code)
+
+
+def test_quantizer_special_blocks():
+    """An all-zero block: scale 0 and codes 0.  A block far above the E4M3 range saturates
+    its scale at 448.  Error bound: every element is within one scale step (the largest gap
+    of the E2M1 grid is 2) of its dequantized value when the scale does not saturate."""
+    x = np.zeros((3, 32), np.float32)
+    x[1, :16] = 1e30
+    x[2, 16:] = np.linspace(-3, 5, 16)
+    codes, scales = oracle.quantize_nvfp4(_to_bf16_bits(x), 1.0)
+    assert scales[0, 0] == 0 and not codes[0].any()
+    assert scales[1, 0] == 0x7E and np.all(codes[1, :8] == 0x77)  # saturated scale and codes
+    sv = oracle.e4m3(int(scales[2, 1]))
+    deq = np.array([oracle.e2m1(int((codes[2, 8 + i // 2] >> (4 * (i % 2))) & 0xF)) for i in range(16)]) * sv
+    xb = (_to_bf16_bits(x[2, 16:]).astype(np.uint32) << 16).view(np.float32)
+    assert np.all(np.abs(deq - xb) <= sv * 1.0 + 1e-12)
