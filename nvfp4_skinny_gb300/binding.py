@@ -230,8 +230,7 @@ def nvfp4_skinny_linear_silu_mul(plan, gate_up, ld_gate_up, M, w_codes, w_block_
                                                  _ptr(w_block_scales), float(w_global_scale), _ptr(y), int(ldc),
                                                  _stream(stream))
     if check:
-        _check(st, "nvfp4_skinny_linear_silu_mul",
-                "nvfp4_quantize_bf16")
+        _check(st, "nvfp4_skinny_linear_silu_mul")
     return st
 
 
