@@ -157,6 +157,27 @@ nvfp4_status nvfp4_skinny_linear_silu_mul(nvfp4_plan_t plan, const void* gate_up
 nvfp4_status nvfp4_quantize_bf16(const void* w, int64_t rows, int64_t K, int64_t ldw, float w_global_scale,
                                  uint8_t* w_codes, uint8_t* w_block_scales, void* stream);
 
+/* One expert's share of a grouped call: its activation rows, weight and output. */
+typedef struct {
+  const void* x;                  /* bfloat16 [M, K], device, 16-byte aligned */
+  int32_t M;                      /* 1..32 rows routed to this expert */
+  int32_t reserved;
+  const uint8_t* w_codes;         /* [N, K/2] */
+  const uint8_t* w_block_scales;  /* [N, K/16] */
+  float w_global_scale;
+  float reserved2;
+  void* y;                        /* [M, N], the plan's output type */
+} nvfp4_group_item;
+
+/* Grouped expert projections ("Module ops": the grouped NVFP4 expert GEMVs over pointer tables
+ * with per-expert global scales): y_e = x_e . dequant(W_e)^T for every item e of the host table
+ * `items` (count >= 1), all with the plan's (N, K) and output type.  Every item is checked
+ * before anything is enqueued (one bad item refuses the whole call with its status); the items
+ * are then enqueued in order on `stream`, one projection each, back to back (their launches
+ * overlap through programmatic dependent launch).  Each item's bits equal those of
+ * nvfp4_skinny_linear on the same arguments. */
+nvfp4_status nvfp4_skinny_linear_grouped(nvfp4_plan_t plan, const nvfp4_group_item* items, int count, void* stream);
+
 /* Synchronize `stream`, then read and clear the plan's device error word.
  * Returns NVFP4_OK, NVFP4_ERR_TIMEOUT, or NVFP4_ERR_CUDA if the stream
  * reported an error. */

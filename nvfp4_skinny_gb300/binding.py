@@ -36,8 +36,14 @@ NVFP4_PACK_ERR_VALUE = -2
 CUDA_SYMBOLS = ("nvfp4_status_string", "nvfp4_abi_version", "nvfp4_plan_create", "nvfp4_plan_create_ex",
                 "nvfp4_plan_destroy", "nvfp4_skinny_linear", "nvfp4_plan_check", "nvfp4_plan_get_info",
                 "nvfp4_skinny_linear_noalloc", "nvfp4_skinny_linear_strided", "nvfp4_skinny_linear_silu_mul",
-                "nvfp4_quantize_bf16")
+                "nvfp4_quantize_bf16", "nvfp4_skinny_linear_grouped")
 PACK_SYMBOLS = ("nvfp4_pack_codes", "nvfp4_unpack_codes", "nvfp4_e4m3_encode")
+
+
+class GroupItem(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("M", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("w_codes", ctypes.c_void_p), ("w_block_scales", ctypes.c_void_p), ("w_global_scale", ctypes.c_float),
+                ("reserved2", ctypes.c_float), ("y", ctypes.c_void_p)]
 
 
 class Nvfp4Error(RuntimeError):
@@ -94,6 +100,8 @@ def cuda_lib():
         lib.nvfp4_skinny_linear_strided.argtypes = [p, p, i64, i32, p, p, ctypes.c_float, p, i64, p]
         lib.nvfp4_skinny_linear_silu_mul.restype = i32
         lib.nvfp4_skinny_linear_silu_mul.argtypes = [p, p, i64, i32, p, p, ctypes.c_float, p, i64, p]
+        lib.nvfp4_skinny_linear_grouped.restype = i32
+        lib.nvfp4_skinny_linear_grouped.argtypes = [p, ctypes.POINTER(GroupItem), i32, p]
         lib.nvfp4_quantize_bf16.restype = i32
         lib.nvfp4_quantize_bf16.argtypes = [p, i64, i64, i64, ctypes.c_float, p, p, p]
         lib.nvfp4_skinny_linear_noalloc.restype = i32
@@ -231,6 +239,19 @@ def nvfp4_skinny_linear_silu_mul(plan, gate_up, ld_gate_up, M, w_codes, w_block_
                                                  _stream(stream))
     if check:
         _check(st, "nvfp4_skinny_linear_silu_mul")
+    return st
+
+
+def nvfp4_skinny_linear_grouped(plan, items, stream=None, check=True):
+    """Grouped expert projections: items is a sequence of (x, M, w_codes, w_block_scales,
+    w_global_scale, y), all for the plan's (N, K)."""
+    arr = (GroupItem * len(items))()
+    for i, (x, M, codes, scales, gs, y) in enumerate(items):
+        arr[i] = GroupItem(_ptr(x), int(M), 0, _ptr(codes), _ptr(scales), float(gs), 0.0, _ptr(y))
+    st = cuda_lib().nvfp4_skinny_linear_grouped(plan.as_parameter if isinstance(plan, Plan) else plan, arr,
+                                                len(items), _stream(stream))
+    if check:
+        _check(st, "nvfp4_skinny_linear_grouped")
     return st
 
 

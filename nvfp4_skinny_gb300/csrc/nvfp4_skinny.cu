@@ -300,6 +300,24 @@ nvfp4_status nvfp4_skinny_linear_strided(nvfp4_plan_t plan, const void* x, int64
                      static_cast<cudaStream_t>(stream));
 }
 
+nvfp4_status nvfp4_skinny_linear_grouped(nvfp4_plan_t plan, const nvfp4_group_item* items, int count, void* stream) {
+  if (!plan || !items || count < 1) return NVFP4_ERR_ARG;
+  for (int e = 0; e < count; ++e) {
+    const nvfp4_group_item& it = items[e];
+    if (!it.x || !it.w_codes || !it.w_block_scales || !it.y) return NVFP4_ERR_ARG;
+    if (it.M < 1 || it.M > NVFP4_MAX_M) return NVFP4_ERR_M_RANGE;
+    if (!aligned16(it.x) || !aligned16(it.y) || !aligned16(it.w_codes) || !aligned16(it.w_block_scales))
+      return NVFP4_ERR_ALIGN;
+  }
+  for (int e = 0; e < count; ++e) {
+    const nvfp4_group_item& it = items[e];
+    const nvfp4_status st = launch_call(plan, it.x, plan->K, it.M, it.w_codes, it.w_block_scales, it.w_global_scale,
+                                        it.y, plan->N, static_cast<cudaStream_t>(stream));
+    if (st != NVFP4_OK) return st;
+  }
+  return NVFP4_OK;
+}
+
 nvfp4_status nvfp4_skinny_linear_silu_mul(nvfp4_plan_t plan, const void* gate_up, int64_t ld_gate_up, int M,
                                           const uint8_t* w_codes, const uint8_t* w_block_scales, float w_global_scale,
                                           void* y, int64_t ldc, void* stream) {

@@ -276,6 +276,31 @@ def test_silu_mul_row_invariance_and_refusals():
     assert nb.nvfp4_plan_check(plan) == nb.NVFP4_OK
 
 
+# ------------------------------------------------------------------ grouped expert projections
+
+def test_grouped_experts_match_single_calls_and_oracle():
+    """Eight experts of one (N, K) with their own weights, global scales and row counts: each
+    item's bits equal a single call's, and sampled elements meet the oracle's tolerance."""
+    N, K = 2048, 1024
+    plan = _plan(N, K)
+    cases = [Case(N, K, M, seed=70 + e, gs=0.01 * (e + 1)) for e, M in enumerate((1, 3, 8, 16, 17, 24, 32, 2))]
+    ys = [torch.empty((c.M, N), dtype=torch.bfloat16, device="cuda") for c in cases]
+    nb.nvfp4_skinny_linear_grouped(plan, [(c.d_x, c.M, c.d_codes, c.d_scales, c.gs, y) for c, y in zip(cases, ys)])
+    torch.cuda.synchronize()
+    assert nb.nvfp4_plan_check(plan) == nb.NVFP4_OK
+    for c, y in zip(cases, ys):
+        assert torch.equal(y, c.run(plan))
+        rng = np.random.default_rng(c.M)
+        ms, ns = rng.integers(0, c.M, 128), rng.integers(0, N, 128)
+        y_ref, absdot = c.oracle_at(ms, ns)
+        ok, ratio = within_tolerance(to_f64(y)[ms, ns], y_ref, absdot)
+        assert ok, ratio
+    torch.cuda.synchronize()
+    bad = [(c.d_x, c.M, c.d_codes, c.d_scales, c.gs, y) for c, y in zip(cases, ys)]
+    bad[5] = (cases[5].d_x, 33, cases[5].d_codes, cases[5].d_scales, cases[5].gs, ys[5])
+    assert nb.nvfp4_skinny_linear_grouped(plan, bad, check=False) == nb.NVFP4_ERR_M_RANGE
+
+
 # ------------------------------------------------------------------ N-sharding (replicas path)
 
 @pytest.mark.parametrize("cuts", [(2560,), (2000, 3100)])
