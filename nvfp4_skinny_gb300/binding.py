@@ -1,4 +1,5 @@
-"""Thin ctypes binding over the C ABI in include/nvfp4_skinny.h and include/nvfp4_pack.h.
+"""Thin ctypes binding over the C ABI in include/nvfp4_skinny.h, include/nvfp4_prefill.h and
+include/nvfp4_pack.h.
 
 Argument marshalling only: every step of the projection runs in the CUDA library
 (nvfp4_skinny_gb300/_build/libnvfp4skinny.so).  If that library is missing the
@@ -37,7 +38,10 @@ CUDA_SYMBOLS = ("nvfp4_status_string", "nvfp4_abi_version", "nvfp4_plan_create",
                 "nvfp4_plan_destroy", "nvfp4_skinny_linear", "nvfp4_plan_check", "nvfp4_plan_get_info",
                 "nvfp4_skinny_linear_noalloc", "nvfp4_skinny_linear_strided", "nvfp4_skinny_linear_silu_mul",
                 "nvfp4_quantize_bf16", "nvfp4_skinny_linear_grouped")
+PREFILL_SYMBOLS = ("nvfp4_prefill_geometry", "nvfp4_prefill_plan_create", "nvfp4_prefill_plan_destroy",
+                   "nvfp4_prefill_linear", "nvfp4_prefill_plan_check", "nvfp4_prefill_plan_get_info")
 PACK_SYMBOLS = ("nvfp4_pack_codes", "nvfp4_unpack_codes", "nvfp4_e4m3_encode")
+NVFP4_PREFILL_MAX_ROWS = 65536
 
 
 class GroupItem(ctypes.Structure):
@@ -61,6 +65,14 @@ class PlanInfo(ctypes.Structure):
                 ("device", ctypes.c_int32), ("row_blocks", ctypes.c_int64), ("k_steps", ctypes.c_int64),
                 ("units", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64), ("smem_bytes", ctypes.c_int64),
                 ("launches_per_call", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class PrefillInfo(ctypes.Structure):
+    _fields_ = [("N", ctypes.c_int64), ("K", ctypes.c_int64), ("M", ctypes.c_int32), ("bm", ctypes.c_int32),
+                ("m_tiles", ctypes.c_int32), ("n_tiles", ctypes.c_int32), ("splits", ctypes.c_int32),
+                ("grid", ctypes.c_int32), ("threads", ctypes.c_int32), ("launches_per_call", ctypes.c_int32),
+                ("sm_count", ctypes.c_int32), ("max_M", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
+                ("smem_bytes", ctypes.c_int64)]
 
 
 _cuda = None
@@ -106,6 +118,18 @@ def cuda_lib():
         lib.nvfp4_quantize_bf16.argtypes = [p, i64, i64, i64, ctypes.c_float, p, p, p]
         lib.nvfp4_skinny_linear_noalloc.restype = i32
         lib.nvfp4_skinny_linear_noalloc.argtypes = [i64, i64, i32, p, i32, p, p, ctypes.c_float, p, p]
+        lib.nvfp4_prefill_geometry.restype = i32
+        lib.nvfp4_prefill_geometry.argtypes = [i64, i64, i32, i32, ctypes.POINTER(PrefillInfo)]
+        lib.nvfp4_prefill_plan_create.restype = i32
+        lib.nvfp4_prefill_plan_create.argtypes = [i64, i64, i32, ctypes.POINTER(p)]
+        lib.nvfp4_prefill_plan_destroy.restype = None
+        lib.nvfp4_prefill_plan_destroy.argtypes = [p]
+        lib.nvfp4_prefill_linear.restype = i32
+        lib.nvfp4_prefill_linear.argtypes = [p, p, i32, p, p, ctypes.c_float, p, p]
+        lib.nvfp4_prefill_plan_check.restype = i32
+        lib.nvfp4_prefill_plan_check.argtypes = [p, p]
+        lib.nvfp4_prefill_plan_get_info.restype = i32
+        lib.nvfp4_prefill_plan_get_info.argtypes = [p, i32, ctypes.POINTER(PrefillInfo)]
         _cuda = lib
     return _cuda
 
@@ -286,6 +310,79 @@ def nvfp4_plan_get_info(plan):
     info = PlanInfo()
     _check(cuda_lib().nvfp4_plan_get_info(plan.as_parameter, ctypes.byref(info)), "nvfp4_plan_get_info")
     return {f: getattr(info, f) for f, _ in PlanInfo._fields_}
+
+
+# --------------------------------------------------------------------------- prefill
+
+class PrefillPlan:
+    """Owns an nvfp4_prefill_plan_t; destroyed with the object (or by destroy())."""
+
+    def __init__(self, handle, N, K, max_M):
+        self.handle = handle
+        self.N, self.K, self.max_M = int(N), int(K), int(max_M)
+
+    def destroy(self):
+        if self.handle is not None:
+            cuda_lib().nvfp4_prefill_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+    @property
+    def as_parameter(self):
+        if self.handle is None:
+            raise ValueError("plan was destroyed")
+        return self.handle
+
+
+def _info_dict(info):
+    return {f: getattr(info, f) for f, _ in PrefillInfo._fields_}
+
+
+def nvfp4_prefill_geometry(N, K, M, sm_count):
+    """The launch geometry of a prefill call (host-only: no GPU needed)."""
+    info = PrefillInfo()
+    _check(cuda_lib().nvfp4_prefill_geometry(int(N), int(K), int(M), int(sm_count), ctypes.byref(info)),
+           "nvfp4_prefill_geometry")
+    return _info_dict(info)
+
+
+def nvfp4_prefill_plan_create(N, K, max_M):
+    """Plan for an [N, K] NVFP4 weight and calls of up to max_M activation rows."""
+    h = ctypes.c_void_p()
+    _check(cuda_lib().nvfp4_prefill_plan_create(int(N), int(K), int(max_M), ctypes.byref(h)),
+           "nvfp4_prefill_plan_create")
+    return PrefillPlan(h.value, N, K, max_M)
+
+
+def nvfp4_prefill_plan_destroy(plan):
+    plan.destroy()
+
+
+def nvfp4_prefill_linear(plan, x, M, w_codes, w_block_scales, w_global_scale, y, stream=None, check=True):
+    """Enqueue the prefill projection y = x . dequant(W)^T (M up to the plan's max_M)."""
+    st = cuda_lib().nvfp4_prefill_linear(plan.as_parameter if isinstance(plan, PrefillPlan) else plan, _ptr(x),
+                                         int(M), _ptr(w_codes), _ptr(w_block_scales), float(w_global_scale), _ptr(y),
+                                         _stream(stream))
+    if check:
+        _check(st, "nvfp4_prefill_linear")
+    return st
+
+
+def nvfp4_prefill_plan_check(plan, stream=None):
+    """Synchronise the stream and return the plan's device error status (and clear it)."""
+    return int(cuda_lib().nvfp4_prefill_plan_check(plan.as_parameter, _stream(stream)))
+
+
+def nvfp4_prefill_plan_get_info(plan, M):
+    info = PrefillInfo()
+    _check(cuda_lib().nvfp4_prefill_plan_get_info(plan.as_parameter, int(M), ctypes.byref(info)),
+           "nvfp4_prefill_plan_get_info")
+    return _info_dict(info)
 
 
 # --------------------------------------------------------------------------- packer

@@ -17,8 +17,8 @@ OUT = os.path.join(HERE, "_build")
 CUDA_LIB = os.path.join(OUT, "libnvfp4skinny.so")
 PACK_LIB = os.path.join(OUT, "libnvfp4pack.so")
 
-CUDA_SOURCES = ["nvfp4_skinny.cu", "quantize.cu"]
-CUDA_DEPS = ["nvfp4_skinny.cu", "quantize.cu", "skinny_kernels.cuh", "ptx.cuh"]
+CUDA_SOURCES = ["nvfp4_skinny.cu", "quantize.cu", "prefill.cu"]
+CUDA_DEPS = ["nvfp4_skinny.cu", "quantize.cu", "prefill.cu", "skinny_kernels.cuh", "prefill_kernels.cuh", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -36,7 +36,7 @@ def _stale(out, deps):
 
 
 def build_cuda(force=False, verbose=False):
-    deps = [os.path.join(CSRC, f) for f in CUDA_DEPS] + [os.path.join(INCLUDE, "nvfp4_skinny.h")]
+    deps = [os.path.join(CSRC, f) for f in CUDA_DEPS] + [os.path.join(INCLUDE, h) for h in ("nvfp4_skinny.h", "nvfp4_prefill.h")]
     if not force and not _stale(CUDA_LIB, deps):
         return CUDA_LIB
     os.makedirs(OUT, exist_ok=True)

@@ -1,0 +1,376 @@
+// Device kernels of the NVFP4 prefill projection y = x . dequant(W)^T for activation row counts
+// above the skinny band ("10.2 NVFP4 matrix products": a second kernel over the same stored format
+// serves prefill chunks of 33 to about 1,024 rows), on sm_103a.
+//
+// prefill_x_prep_kernel (one block per activation row): as in the skinny path, the row's largest
+// magnitude fixes a power of two 2^e (the maximum lands in [2^15, 2^16)); the row is written as
+// fp16 times 2^e into a plain row-major [M, K] operand, and 2^-e goes to xs[m].
+//
+// prefill_kernel: one block per (256 weight rows, BM activation rows, k-split) tile, 10 warps:
+//   warps 0-7  decoders: one weight row per thread.  Per k-step of 64 they read the row's 32 bytes
+//              of E2M1 codes and 4 E4M3 scales from shared memory, decode with the hardware
+//              converters (exact in fp16) and write the 64 fp16 weights into the stage's A operand
+//              in the 128-byte-swizzled K-major layout the tensor core reads.  After the k-loop
+//              they are the epilogue: tensor memory -> registers, times 2^-e and the per-tensor
+//              scale, rounded to bf16 (one k-split) or stored as fp32 parts;
+//   warp 8     producer (one lane): 2-D tensor copies of the codes (32 B x 256 rows per k-step),
+//              the scales (16 B x 256 rows per 256 k) and the fp16 activations (64 k x BM rows,
+//              128-byte swizzle) into a 3-stage ring; it also owns the tensor-memory allocation;
+//   warp 9     MMA issuer (one lane): per k-step, for each 128-row half of the weight tile, four
+//              tcgen05.mma kind::f16 (M = 128, N = BM, K = 16) with both operands in shared memory,
+//              fp32 accumulation in tensor memory (columns [256 t, 256 t + BM) for half t).
+// The weights are the MMA's A operand (M = weight rows) and the activations its B operand
+// (N = activation rows), so one decoded weight tile serves every activation row of the tile.
+//
+// prefill_reduce_kernel (only when the k-range is split): adds the parts in split order, then
+// multiplies by 2^-e and the per-tensor scale and rounds to bf16.  The tile shape and the split
+// are functions of (N, K, M, SM count), so a call is deterministic; unlike the skinny path, a row's
+// bits may change with M (the split count depends on M).
+#pragma once
+
+#include <cuda.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+#include "skinny_kernels.cuh"
+
+namespace nvfp4 {
+namespace prefill {
+
+constexpr int kBN = 256;                 // weight rows per tile (two MMA tiles of 128)
+constexpr int kMmaM = 128;
+constexpr int kBMMax = 256;              // activation rows per tile (MMA N): a multiple of 16
+constexpr int kKS = 64;                  // k per pipeline step: one 128-byte line of fp16
+constexpr int kStepsPerUnit = 4;         // one scale copy covers 256 k
+constexpr int kP = 3;                    // pipeline depth in k-steps
+constexpr int kATileBytes = kMmaM * kKS * 2;         // 16384: decoded weights of one MMA tile
+constexpr int kABytes = 2 * kATileBytes;             // 32768
+constexpr int kBOff = kABytes;                       // activations: BM x 128 bytes (<= 32 KB)
+constexpr int kCOff = kBOff + kBMMax * kKS * 2;      // codes: 256 rows x 32 bytes
+constexpr int kCBytes = kBN * kKS / 2;               // 8192
+constexpr int kStageBytes = kCOff + kCBytes;         // 73728 (a multiple of 1024)
+constexpr int kSBytes = kBN * 16;                    // 4096: scales of 256 k, 16 bytes per row
+constexpr int kSStages = 2;
+constexpr int kSmemScales = kP * kStageBytes;        // 221184
+constexpr int kSmemBar = kSmemScales + kSStages * kSBytes;
+// mbarriers
+constexpr int kBarCFull = 0;                 // [kP] codes copied (tx)      -> decoders
+constexpr int kBarBFull = kBarCFull + kP;    // [kP] activations copied (tx) -> issuer
+constexpr int kBarAFull = kBarBFull + kP;    // [kP] 256 decoder arrivals   -> issuer
+constexpr int kBarEmpty = kBarAFull + kP;    // [kP] MMA commit             -> producer
+constexpr int kBarSFull = kBarEmpty + kP;    // [2]  scales copied (tx)     -> decoders
+constexpr int kBarSEmpty = kBarSFull + kSStages;  // [2] 256 decoder arrivals -> producer
+constexpr int kBarDFull = kBarSEmpty + kSStages;  // accumulators final      -> epilogue
+constexpr int kNumBars = kBarDFull + 1;
+constexpr int kSmemMisc = kSmemBar + kNumBars * 8;  // +0 tensor-memory base, +4 abort flag
+constexpr int kSmemBytes = kSmemMisc + 16 + 1024;   // misc + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory per block");
+static_assert(kStageBytes % 1024 == 0 && kATileBytes % 1024 == 0 && kBOff % 1024 == 0, "swizzle atoms");
+
+constexpr int kDecodeWarps = 8;
+constexpr int kProducerWarp = 8;
+constexpr int kIssuerWarp = 9;
+constexpr int kThreads = 10 * 32;
+constexpr uint32_t kTmemCols = 512;  // half t accumulates in columns [256 t, 256 t + BM); one block per SM
+constexpr int kPrepThreads = 256;
+
+// instruction descriptor: kind::f16, D = f32, A = B = f16, both K-major, N = bm, M = 128
+__host__ __device__ constexpr uint32_t idesc_bm(int bm) {
+  return (1u << 4) | ((uint32_t)(bm >> 3) << 17) | ((uint32_t)(kMmaM >> 4) << 24);
+}
+
+struct PrefillParams {
+  CUtensorMap tm_codes;   // uint8 [N rows, K/2 bytes], box 32 B x 256 rows
+  CUtensorMap tm_scales;  // uint8 [N rows, K/16 bytes], box 16 B x 256 rows
+  CUtensorMap tm_x;       // fp16 [M rows, K], box 64 x BM rows, 128-byte swizzle
+  const float* xs;        // [M] 2^-e per activation row
+  uint16_t* y;            // bf16 [M, N] (one k-split)
+  float* parts;           // fp32 [splits][M][N] (several)
+  int* err;               // error word
+  float gs;
+  int M, bm, m_tiles, n_tiles, splits;
+  int64_t N, K;
+};
+
+// ------------------------------------------------------------------ activation preparation
+// One block per activation row: pass 1 takes the row's largest magnitude, pass 2 converts
+// (re-reading the row, which is in L2).
+__global__ void __launch_bounds__(kPrepThreads) prefill_x_prep_kernel(const uint16_t* __restrict__ x, int M, int64_t K,
+                                                                      uint16_t* __restrict__ x16,
+                                                                      float* __restrict__ xs) {
+  ptx::grid_launch_dependents();
+  ptx::grid_dependency_wait();  // x is produced upstream; x16 and xs were read by the previous call
+  __shared__ uint32_t wmax[kPrepThreads / 32];
+  const int m = blockIdx.x, tid = threadIdx.x;
+  if (m >= M) return;
+  const int64_t chunks = K / 8;
+  const uint4* row = reinterpret_cast<const uint4*>(x + (int64_t)m * K);
+  uint4* out = reinterpret_cast<uint4*>(x16 + (int64_t)m * K);
+  uint32_t mx = 0u;
+  for (int64_t c = tid; c < chunks; c += kPrepThreads) mx = max(mx, bf16x8_maxmag(__ldg(row + c)));
+  const uint32_t wm = warp_max_u32(mx);
+  if ((tid & 31) == 0) wmax[tid >> 5] = wm;
+  __syncthreads();
+  uint32_t bm = 0u;
+#pragma unroll
+  for (int w = 0; w < kPrepThreads / 32; ++w) bm = max(bm, wmax[w]);
+  const int e = x_exponent(__uint_as_float(bm << 16));  // -112 <= e <= 148 for bf16 data
+  if (tid == 0) xs[m] = pow2i(-(e / 2)) * pow2i(-(e - e / 2));  // 2^-e, exact
+  const float f1 = pow2i(e <= 127 ? e : e / 2), f2 = pow2i(e <= 127 ? 0 : e - e / 2);
+  for (int64_t c = tid; c < chunks; c += kPrepThreads) {
+    const uint4 v = __ldg(row + c);
+    out[c] = e <= 127 ? bf16x8_to_f16x8(v, f1) : bf16x8_to_f16x8(v, f1, f2);
+  }
+}
+
+// D[tmem] (+)= A[smem descriptor] * B[smem descriptor]; kind::f16, issued by one thread.
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t id,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(id), "r"(accumulate)
+      : "memory");
+}
+
+// ------------------------------------------------------------------ main kernel
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + kSmemMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemMisc + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t smem_base = ptx::smem_addr(smem);
+  const uint32_t bar_base = smem_base + (uint32_t)kSmemBar;
+  auto bar = [&](int i) { return bar_base + 8u * (uint32_t)i; };
+
+  // tile of this block: activation tiles fastest, so the blocks that share a weight tile run together
+  const int b = blockIdx.x;
+  const int mt = b % p.m_tiles, rest = b / p.m_tiles;
+  const int nt = rest % p.n_tiles, sp = rest / p.n_tiles;
+  const int BM = p.bm;
+  const int m0 = mt * BM;
+  const int n0 = nt * kBN;
+  const int64_t U = p.K / (kKS * kStepsPerUnit);
+  const int64_t u0 = sp * U / p.splits, u1 = (sp + 1) * U / p.splits;
+  const int nsteps = (int)(u1 - u0) * kStepsPerUnit;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kP; ++s) {
+      ptx::mbar_init(bar(kBarCFull + s), 1);
+      ptx::mbar_init(bar(kBarBFull + s), 1);
+      ptx::mbar_init(bar(kBarAFull + s), kDecodeWarps * 32);
+      ptx::mbar_init(bar(kBarEmpty + s), 1);
+    }
+    for (int s = 0; s < kSStages; ++s) {
+      ptx::mbar_init(bar(kBarSFull + s), 1);
+      ptx::mbar_init(bar(kBarSEmpty + s), kDecodeWarps * 32);
+    }
+    ptx::mbar_init(bar(kBarDFull), 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kProducerWarp) {
+    ptx::tmem_alloc(ptx::smem_addr(tmem_base_smem), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_base_smem;
+  const Abort ab{abort_flag, p.err};
+  ptx::grid_dependency_wait();  // the activation operand is ready; y and the parts are free
+  ptx::grid_launch_dependents();
+
+  if (warp < kDecodeWarps) {
+    // ================================================================ decoders, then epilogue
+    const int r = warp * 32 + lane;  // weight row of the tile
+    const int t = r >> 7, rr = r & (kMmaM - 1);
+    const int swz = rr & 7;
+    const uint32_t a_off = (uint32_t)(t * kATileBytes + (rr >> 3) * 1024 + (rr & 7) * 128);
+    bool ok = true;
+    for (int j = 0; j < nsteps; ++j) {
+      const int st = j % kP;
+      const uint32_t ph = (uint32_t)((j / kP) & 1);
+      const int u = j >> 2, q = j & 3, ss = u & 1;
+      if (q == 0 && ok) ok = wait_bar(bar(kBarSFull + ss), (uint32_t)((u >> 1) & 1), ab);
+      if (ok) ok = wait_bar(bar(kBarCFull + st), ph, ab);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      uint8_t* stage = smem + st * kStageBytes;
+      const uint4 c0 = *reinterpret_cast<const uint4*>(stage + kCOff + r * 32);
+      const uint4 c1 = *reinterpret_cast<const uint4*>(stage + kCOff + r * 32 + 16);
+      const uint32_t sw = *reinterpret_cast<const uint32_t*>(smem + kSmemScales + ss * kSBytes + r * 16 + q * 4);
+      if (q == kStepsPerUnit - 1) ptx::mbar_arrive(bar(kBarSEmpty + ss));  // this unit's scales are read
+      const uint32_t s0 = ptx::e4m3_pair(sw, 0), s1 = ptx::e4m3_pair(sw, 1);
+      const uint32_t s2 = ptx::e4m3_pair(sw, 2), s3 = ptx::e4m3_pair(sw, 3);
+      uint32_t o[32];
+      ptx::e2m1x8_scaled(c0.x, s0, o[0], o[1], o[2], o[3]);
+      ptx::e2m1x8_scaled(c0.y, s0, o[4], o[5], o[6], o[7]);
+      ptx::e2m1x8_scaled(c0.z, s1, o[8], o[9], o[10], o[11]);
+      ptx::e2m1x8_scaled(c0.w, s1, o[12], o[13], o[14], o[15]);
+      ptx::e2m1x8_scaled(c1.x, s2, o[16], o[17], o[18], o[19]);
+      ptx::e2m1x8_scaled(c1.y, s2, o[20], o[21], o[22], o[23]);
+      ptx::e2m1x8_scaled(c1.z, s3, o[24], o[25], o[26], o[27]);
+      ptx::e2m1x8_scaled(c1.w, s3, o[28], o[29], o[30], o[31]);
+      // 16-byte chunk c (k 8c .. 8c + 7) of the row goes to chunk c ^ (row % 8) of its line; the
+      // stage's A area is free: its codes were copied only after the MMAs that last read it ended
+      uint8_t* arow = stage + a_off;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(arow + ((c ^ swz) << 4)) = make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+      ptx::fence_proxy_async_smem();  // generic-proxy writes -> the tensor core's reads
+      ptx::mbar_arrive(bar(kBarAFull + st));
+    }
+
+    // ---- epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. + 31 of half w / 4
+    if (ok) ok = wait_bar(bar(kBarDFull), 0u, ab);
+    ok = __all_sync(0xffffffffu, ok);
+    ptx::tc_fence_after();
+    if (ok) {
+      const int quad = warp & 3;
+      const int64_t n = n0 + r;  // r = t * 128 + quad * 32 + lane
+      const bool n_in = n < p.N;
+      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(t * kBMMax);
+      const int M = p.M;
+      const float gs = p.gs;
+      for (int c = 0; c < BM / 16; ++c) {
+        const int mb = m0 + 16 * c;
+        if (mb >= M) break;  // warp-uniform
+        uint32_t v[16];
+        __syncwarp();
+        ptx::tmem_ld16(taddr + (uint32_t)(16 * c), v);
+        ptx::tmem_wait_ld();
+        if (!n_in) {
+        } else if (p.splits == 1) {
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int m = mb + jj;
+            if (m < M)
+              p.y[(int64_t)m * p.N + n] = ptx::f32_to_bf16_rn(__fmul_rn(__fmul_rn(__uint_as_float(v[jj]), __ldg(p.xs + m)), gs));
+          }
+        } else {
+          float* part = p.parts + (int64_t)sp * M * p.N + n;
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int m = mb + jj;
+            if (m < M) part[(int64_t)m * p.N] = __uint_as_float(v[jj]);
+          }
+        }
+      }
+    }
+  } else if (warp == kProducerWarp) {
+    // ================================================================ producer
+    if (lane == 0) {
+      const uint64_t pol_w = ptx::policy_evict_first();
+      const uint64_t pol_x = ptx::policy_evict_last();
+      ptx::prefetch_tensormap(&p.tm_codes);
+      ptx::prefetch_tensormap(&p.tm_scales);
+      ptx::prefetch_tensormap(&p.tm_x);
+      const uint32_t xbytes = (uint32_t)BM * (uint32_t)(kKS * 2);
+      int issued = 0, units_issued = 0;
+      for (int j = 0; j < nsteps; ++j) {
+        const int u = j >> 2;
+        if ((j & 3) == 0) {
+          const int ss = u & 1;
+          if (!wait_bar(bar(kBarSEmpty + ss), (uint32_t)(((u >> 1) & 1) ^ 1), ab)) break;
+          ptx::mbar_arrive_expect_tx(bar(kBarSFull + ss), (uint32_t)kSBytes);
+          ptx::tma_load_2d(smem_base + (uint32_t)(kSmemScales + ss * kSBytes), &p.tm_scales, (int32_t)((u0 + u) * 16),
+                           n0, bar(kBarSFull + ss), pol_w);
+          units_issued = u + 1;
+        }
+        const int st = j % kP;
+        if (!wait_bar(bar(kBarEmpty + st), (uint32_t)(((j / kP) & 1) ^ 1), ab)) break;
+        const int64_t g = u0 * kStepsPerUnit + j;  // global k-step
+        const uint32_t stage = smem_base + (uint32_t)(st * kStageBytes);
+        ptx::mbar_arrive_expect_tx(bar(kBarCFull + st), (uint32_t)kCBytes);
+        ptx::tma_load_2d(stage + kCOff, &p.tm_codes, (int32_t)(g * (kKS / 2)), n0, bar(kBarCFull + st), pol_w);
+        ptx::mbar_arrive_expect_tx(bar(kBarBFull + st), xbytes);
+        ptx::tma_load_2d(stage + kBOff, &p.tm_x, (int32_t)(g * kKS), m0, bar(kBarBFull + st), pol_x);
+        issued = j + 1;
+      }
+      // every copy this thread started has landed before the block can exit (normally they were
+      // all consumed already; after an abort this bounded wait keeps shared memory owned)
+      for (int j = issued - kP < 0 ? 0 : issued - kP; j < issued; ++j) {
+        const uint32_t ph = (uint32_t)((j / kP) & 1);
+        (void)wait_bar(bar(kBarCFull + j % kP), ph, ab, false);
+        (void)wait_bar(bar(kBarBFull + j % kP), ph, ab, false);
+      }
+      for (int u = units_issued - kSStages < 0 ? 0 : units_issued - kSStages; u < units_issued; ++u)
+        (void)wait_bar(bar(kBarSFull + (u & 1)), (uint32_t)((u >> 1) & 1), ab, false);
+    }
+  } else {
+    // ================================================================ MMA issuer
+    if (lane == 0) {
+      const uint32_t id = idesc_bm(BM);
+      for (int j = 0; j < nsteps; ++j) {
+        const int st = j % kP;
+        const uint32_t ph = (uint32_t)((j / kP) & 1);
+        if (!wait_bar(bar(kBarAFull + st), ph, ab)) break;
+        if (!wait_bar(bar(kBarBFull + st), ph, ab)) break;
+        ptx::tc_fence_after();
+        const uint32_t stage = smem_base + (uint32_t)(st * kStageBytes);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+#pragma unroll
+          for (int kk = 0; kk < kKS / 16; ++kk)
+            mma_f16_ss(tmem + (uint32_t)(t * kBMMax), x_desc(stage + (uint32_t)(t * kATileBytes + kk * 32)),
+                       x_desc(stage + (uint32_t)(kBOff + kk * 32)), id, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        ptx::mma_commit(bar(kBarEmpty + st));
+      }
+      // every MMA issued so far completes before the accumulators are read or released
+      ptx::mma_commit(bar(kBarDFull));
+      (void)wait_bar(bar(kBarDFull), 0u, ab, false);
+    }
+  }
+
+  // ---- teardown: every tensor-memory operation has completed (waited above)
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == kProducerWarp) ptx::tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------------------------------ split-k reduction
+// y[m, n] = bf16((sum over splits s, in order, of parts[s][m][n]) * 2^-e[m] * gs); four outputs
+// per thread and pass when N is a multiple of 4, else one.
+__global__ void __launch_bounds__(256) prefill_reduce_kernel(const float* __restrict__ parts, const float* __restrict__ xs,
+                                                             uint16_t* __restrict__ y, int M, int64_t N, int splits,
+                                                             float gs) {
+  ptx::grid_dependency_wait();  // the parts of this call are complete
+  ptx::grid_launch_dependents();
+  const int64_t MN = (int64_t)M * N;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  if ((N & 3) == 0) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < MN / 4; i += stride) {
+      const int64_t o = 4 * i;
+      float4 acc = __ldcg(reinterpret_cast<const float4*>(parts + o));
+      for (int s = 1; s < splits; ++s) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(parts + (int64_t)s * MN + o));
+        acc.x = __fadd_rn(acc.x, v.x);
+        acc.y = __fadd_rn(acc.y, v.y);
+        acc.z = __fadd_rn(acc.z, v.z);
+        acc.w = __fadd_rn(acc.w, v.w);
+      }
+      const float f = __ldg(xs + o / N);
+      const uint32_t lo = (uint32_t)ptx::f32_to_bf16_rn(__fmul_rn(__fmul_rn(acc.x, f), gs)) |
+                          ((uint32_t)ptx::f32_to_bf16_rn(__fmul_rn(__fmul_rn(acc.y, f), gs)) << 16);
+      const uint32_t hi = (uint32_t)ptx::f32_to_bf16_rn(__fmul_rn(__fmul_rn(acc.z, f), gs)) |
+                          ((uint32_t)ptx::f32_to_bf16_rn(__fmul_rn(__fmul_rn(acc.w, f), gs)) << 16);
+      *reinterpret_cast<uint2*>(y + o) = make_uint2(lo, hi);
+    }
+  } else {
+    for (int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; o < MN; o += stride) {
+      float acc = __ldcg(parts + o);
+      for (int s = 1; s < splits; ++s) acc = __fadd_rn(acc, __ldcg(parts + (int64_t)s * MN + o));
+      y[o] = ptx::f32_to_bf16_rn(__fmul_rn(__fmul_rn(acc, __ldg(xs + o / N)), gs));
+    }
+  }
+}
+
+}  // namespace prefill
+}  // namespace nvfp4

@@ -29,6 +29,7 @@ def _declared_functions(header):
 @pytest.mark.parametrize("header,getter,listed", [
     ("nvfp4_skinny.h", nb.cuda_lib, nb.CUDA_SYMBOLS),
     ("nvfp4_pack.h", nb.pack_lib, nb.PACK_SYMBOLS),
+    ("nvfp4_prefill.h", nb.cuda_lib, nb.PREFILL_SYMBOLS),
 ])
 def test_every_declared_symbol_is_exported(header, getter, listed):
     names = _declared_functions(header)
@@ -162,3 +163,46 @@ def test_e4m3_encoder_saturates_and_refuses():
     for bad in (-1.0, -1.0e-30, np.nan, -np.inf):
         with pytest.raises(ValueError):
             nb.nvfp4_e4m3_encode(np.array([1.0, bad], np.float32))
+
+
+# ----------------------------------------------------------------------------- prefill geometry
+# nvfp4_prefill_geometry is host-only: the tiles must cover [M, N], the split must give every
+# block at least one 256-k unit, and the choice must be a function of (N, K, M, SMs) alone.
+
+@pytest.mark.parametrize("N,K", [(17, 256), (640, 512), (5120, 5120), (34816, 5120), (5120, 17408), (152064, 5120)])
+@pytest.mark.parametrize("sms", [1, 8, 152])
+def test_prefill_geometry_invariants(N, K, sms):
+    U = K // 256
+    for M in list(range(1, 70)) + [96, 100, 127, 128, 129, 255, 256, 257, 300, 511, 512, 1000, 1024, 4096]:
+        g = nb.nvfp4_prefill_geometry(N, K, M, sms)
+        assert g == nb.nvfp4_prefill_geometry(N, K, M, sms)
+        bm, mt = g["bm"], g["m_tiles"]
+        assert bm % 16 == 0 and 16 <= bm <= 256, g
+        assert mt * bm >= M and (mt - 1) * bm < M, g
+        assert g["n_tiles"] == -(-N // 256)
+        assert 1 <= g["splits"] <= min(U, 32)
+        assert g["grid"] == mt * g["n_tiles"] * g["splits"]
+        assert g["launches_per_call"] == (3 if g["splits"] > 1 else 2)
+        assert g["threads"] == 320 and g["sm_count"] == sms
+        assert 0 < g["smem_bytes"] <= 232448
+        assert g["M"] == M and g["N"] == N and g["K"] == K
+
+
+def test_prefill_geometry_refusals():
+    info = nb.PrefillInfo()
+    lib = nb.cuda_lib()
+    assert lib.nvfp4_prefill_geometry(512, 512, 8, 152, None) == nb.NVFP4_ERR_ARG
+    assert lib.nvfp4_prefill_geometry(512, 512, 8, 0, ctypes.byref(info)) == nb.NVFP4_ERR_ARG
+    for N, K in [(0, 512), (512, 0), (512, 300), (512, 128)]:
+        assert lib.nvfp4_prefill_geometry(N, K, 8, 152, ctypes.byref(info)) == nb.NVFP4_ERR_SHAPE
+    for M in (0, -3, nb.NVFP4_PREFILL_MAX_ROWS + 1):
+        assert lib.nvfp4_prefill_geometry(512, 512, M, 152, ctypes.byref(info)) == nb.NVFP4_ERR_M_RANGE
+    h = ctypes.c_void_p(5)
+    assert lib.nvfp4_prefill_plan_create(512, 300, 8, ctypes.byref(h)) == nb.NVFP4_ERR_SHAPE and h.value is None
+    assert lib.nvfp4_prefill_plan_create(512, 512, 8, None) == nb.NVFP4_ERR_ARG
+    buf = np.zeros(64, np.uint8)
+    p = buf.ctypes.data
+    assert lib.nvfp4_prefill_linear(None, p, 40, p, p, ctypes.c_float(1.0), p, None) == nb.NVFP4_ERR_ARG
+    assert lib.nvfp4_prefill_plan_check(None, None) == nb.NVFP4_ERR_ARG
+    assert lib.nvfp4_prefill_plan_get_info(None, 40, None) == nb.NVFP4_ERR_ARG
+    lib.nvfp4_prefill_plan_destroy(None)  # ignored
