@@ -39,7 +39,8 @@ CUDA_SYMBOLS = ("nvfp4_status_string", "nvfp4_abi_version", "nvfp4_plan_create",
                 "nvfp4_skinny_linear_noalloc", "nvfp4_skinny_linear_strided", "nvfp4_skinny_linear_silu_mul",
                 "nvfp4_quantize_bf16", "nvfp4_skinny_linear_grouped")
 PREFILL_SYMBOLS = ("nvfp4_prefill_geometry", "nvfp4_prefill_plan_create", "nvfp4_prefill_plan_destroy",
-                   "nvfp4_prefill_linear", "nvfp4_prefill_plan_check", "nvfp4_prefill_plan_get_info")
+                   "nvfp4_prefill_linear", "nvfp4_prefill_linear_ex", "nvfp4_prefill_plan_check",
+                   "nvfp4_prefill_plan_get_info")
 PACK_SYMBOLS = ("nvfp4_pack_codes", "nvfp4_unpack_codes", "nvfp4_e4m3_encode")
 NVFP4_PREFILL_MAX_ROWS = 65536
 
@@ -71,7 +72,8 @@ class PrefillInfo(ctypes.Structure):
     _fields_ = [("N", ctypes.c_int64), ("K", ctypes.c_int64), ("M", ctypes.c_int32), ("bm", ctypes.c_int32),
                 ("m_tiles", ctypes.c_int32), ("n_tiles", ctypes.c_int32), ("splits", ctypes.c_int32),
                 ("grid", ctypes.c_int32), ("threads", ctypes.c_int32), ("launches_per_call", ctypes.c_int32),
-                ("sm_count", ctypes.c_int32), ("max_M", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
+                ("sm_count", ctypes.c_int32), ("max_M", ctypes.c_int32), ("load_stages", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
                 ("smem_bytes", ctypes.c_int64)]
 
 
@@ -126,6 +128,8 @@ def cuda_lib():
         lib.nvfp4_prefill_plan_destroy.argtypes = [p]
         lib.nvfp4_prefill_linear.restype = i32
         lib.nvfp4_prefill_linear.argtypes = [p, p, i32, p, p, ctypes.c_float, p, p]
+        lib.nvfp4_prefill_linear_ex.restype = i32
+        lib.nvfp4_prefill_linear_ex.argtypes = [p, p, i32, p, p, ctypes.c_float, p, i32, i32, p]
         lib.nvfp4_prefill_plan_check.restype = i32
         lib.nvfp4_prefill_plan_check.argtypes = [p, p]
         lib.nvfp4_prefill_plan_get_info.restype = i32
@@ -370,6 +374,17 @@ def nvfp4_prefill_linear(plan, x, M, w_codes, w_block_scales, w_global_scale, y,
                                          _stream(stream))
     if check:
         _check(st, "nvfp4_prefill_linear")
+    return st
+
+
+def nvfp4_prefill_linear_ex(plan, x, M, w_codes, w_block_scales, w_global_scale, y, bm=0, splits=0, stream=None,
+                            check=True):
+    """nvfp4_prefill_linear with an explicit tile height bm and k-split (0 = automatic)."""
+    st = cuda_lib().nvfp4_prefill_linear_ex(plan.as_parameter if isinstance(plan, PrefillPlan) else plan, _ptr(x),
+                                            int(M), _ptr(w_codes), _ptr(w_block_scales), float(w_global_scale),
+                                            _ptr(y), int(bm), int(splits), _stream(stream))
+    if check:
+        _check(st, "nvfp4_prefill_linear_ex")
     return st
 
 

@@ -31,6 +31,7 @@ struct nvfp4_prefill_plan {
   uint16_t* x16 = nullptr;  // fp16 [max_M, K]
   float* xs = nullptr;      // [max_M]
   float* parts = nullptr;   // fp32 [splits][M][N], the largest over M <= max_M
+  size_t parts_bytes = 0;
   int* err = nullptr;
 };
 
@@ -44,7 +45,22 @@ bool shape_ok(int64_t N, int64_t K) {
   return N < (int64_t(1) << 31) && K <= (int64_t(1) << 24) && N <= (int64_t(1) << 40) / K;
 }
 
-// The geometry of a call: for every tile height bm (a multiple of 16, balanced over the m-tiles)
+void fill(int64_t N, int M, int bm, int splits, int sms, nvfp4_prefill_info* g) {
+  const int64_t n_tiles = (N + pf::kBN - 1) / pf::kBN, mt = (M + bm - 1) / bm;
+  g->M = M;
+  g->bm = bm;
+  g->m_tiles = (int32_t)mt;
+  g->n_tiles = (int32_t)n_tiles;
+  g->splits = splits;
+  g->grid = (int32_t)(n_tiles * mt * splits);
+  g->threads = pf::kThreads;
+  g->launches_per_call = splits > 1 ? 3 : 2;
+  g->sm_count = sms;
+  g->smem_bytes = pf::kSmemBytes;
+  g->load_stages = pf::load_stages(bm);
+}
+
+// The geometry of a call: for every tile height bm (a multiple of 32, balanced over the m-tiles)
 // and k-split s, the modelled time is the waves of blocks times a block's k-loop (a k-step costs
 // the larger of its 8 MMAs and the decode) plus a fixed cost per block, bounded below by the HBM
 // time of the call's bytes; a split adds the parts' write and read and one launch.  The smallest
@@ -54,13 +70,13 @@ bool geometry(int64_t N, int64_t K, int M, int sms, nvfp4_prefill_info* g) {
   const int64_t U = K / 256;
   const int64_t n_tiles = (N + pf::kBN - 1) / pf::kBN;
   double best = 1e300;
-  int best_bm = 16, best_s = 1;
+  int best_bm = 32, best_s = 1;
   int64_t best_mt = 0;
   const double clock_hz = 1.9e9, hbm_bps = 6.5e12;
   const double t_hbm = ((double)N * (double)K * 0.5625 + 2.0 * M * (double)K + 2.0 * M * (double)N) / hbm_bps;
-  for (int bm = 16; bm <= pf::kBMMax; bm += 16) {
+  for (int bm = 32; bm <= pf::kBMMax; bm += 32) {
     const int64_t mt = (M + bm - 1) / bm;
-    const int64_t bal = ((M + mt - 1) / mt + 15) / 16 * 16;  // the balanced height for mt tiles
+    const int64_t bal = ((M + mt - 1) / mt + 31) / 32 * 32;  // the balanced height for mt tiles
     if (bal != bm) continue;
     const int64_t max_s = U < 32 ? U : 32;
     for (int64_t s = 1; s <= max_s; ++s) {
@@ -82,16 +98,7 @@ bool geometry(int64_t N, int64_t K, int M, int sms, nvfp4_prefill_info* g) {
     }
   }
   if (best_mt == 0) return false;
-  g->M = M;
-  g->bm = best_bm;
-  g->m_tiles = (int32_t)best_mt;
-  g->n_tiles = (int32_t)n_tiles;
-  g->splits = best_s;
-  g->grid = (int32_t)(n_tiles * best_mt * best_s);
-  g->threads = pf::kThreads;
-  g->launches_per_call = best_s > 1 ? 3 : 2;
-  g->sm_count = sms;
-  g->smem_bytes = pf::kSmemBytes;
+  fill(N, M, best_bm, best_s, sms, g);
   return true;
 }
 
@@ -201,6 +208,7 @@ nvfp4_status nvfp4_prefill_plan_create(int64_t N, int64_t K, int max_M, nvfp4_pr
   plan->xs = reinterpret_cast<float*>(b + x16b);
   plan->err = reinterpret_cast<int*>(b + x16b + xsb);
   plan->parts = partb ? reinterpret_cast<float*>(b + x16b + xsb + errb) : nullptr;
+  plan->parts_bytes = pb;
   if (cudaMemset(plan->base, 0, total) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     cudaFree(plan->base);
     delete plan;
@@ -229,11 +237,26 @@ void nvfp4_prefill_plan_destroy(nvfp4_prefill_plan_t plan) {
 
 nvfp4_status nvfp4_prefill_linear(nvfp4_prefill_plan_t plan, const void* x, int M, const uint8_t* w_codes,
                                   const uint8_t* w_block_scales, float w_global_scale, void* y, void* stream) {
+  return nvfp4_prefill_linear_ex(plan, x, M, w_codes, w_block_scales, w_global_scale, y, 0, 0, stream);
+}
+
+nvfp4_status nvfp4_prefill_linear_ex(nvfp4_prefill_plan_t plan, const void* x, int M, const uint8_t* w_codes,
+                                     const uint8_t* w_block_scales, float w_global_scale, void* y, int bm,
+                                     int splits, void* stream) {
   if (!plan || !x || !w_codes || !w_block_scales || !y) return NVFP4_ERR_ARG;
   if (M < 1 || M > plan->max_M) return NVFP4_ERR_M_RANGE;
   if (!aligned16(x) || !aligned16(y) || !aligned16(w_codes) || !aligned16(w_block_scales)) return NVFP4_ERR_ALIGN;
   nvfp4_prefill_info g{};
   if (!geometry(plan->N, plan->K, M, plan->sm_count, &g)) return NVFP4_ERR_SHAPE;
+  if (bm != 0 || splits != 0) {
+    const int64_t U = plan->K / 256;
+    const int b = bm != 0 ? bm : g.bm, sp = splits != 0 ? splits : g.splits;
+    if (b < 32 || b > pf::kBMMax || b % 32 != 0 || sp < 1 || sp > U || sp > 32) return NVFP4_ERR_ARG;
+    const int64_t blocks = (int64_t)((plan->N + pf::kBN - 1) / pf::kBN) * ((M + b - 1) / b) * sp;
+    if (blocks > 0x7FFFFFFF) return NVFP4_ERR_SHAPE;
+    if (sp > 1 && (size_t)sp * (size_t)M * (size_t)plan->N * 4 > plan->parts_bytes) return NVFP4_ERR_SCRATCH_LIMIT;
+    fill(plan->N, M, b, sp, plan->sm_count, &g);
+  }
   if (!prepare_maps(plan, w_codes, w_block_scales, M, g.bm)) return NVFP4_ERR_CUDA;  // before anything is enqueued
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -265,6 +288,7 @@ nvfp4_status nvfp4_prefill_linear(nvfp4_prefill_plan_t plan, const void* x, int 
   p.m_tiles = g.m_tiles;
   p.n_tiles = g.n_tiles;
   p.splits = g.splits;
+  p.lp = g.load_stages;
   p.N = plan->N;
   p.K = plan->K;
   cudaLaunchConfig_t cfg = {};

@@ -6,19 +6,22 @@
 // magnitude fixes a power of two 2^e (the maximum lands in [2^15, 2^16)); the row is written as
 // fp16 times 2^e into a plain row-major [M, K] operand, and 2^-e goes to xs[m].
 //
-// prefill_kernel: one block per (256 weight rows, BM activation rows, k-split) tile, 10 warps:
+// prefill_kernel: one block per (256 weight rows, BM <= 192 activation rows, k-split) tile, 13 warps:
 //   warps 0-7  decoders: one weight row per thread.  Per k-step of 64 they read the row's 32 bytes
 //              of E2M1 codes and 4 E4M3 scales from shared memory, decode with the hardware
-//              converters (exact in fp16) and write the 64 fp16 weights into the stage's A operand
-//              in the 128-byte-swizzled K-major layout the tensor core reads.  After the k-loop
-//              they are the epilogue: tensor memory -> registers, times 2^-e and the per-tensor
-//              scale, rounded to bf16 (one k-split) or stored as fp32 parts;
-//   warp 8     producer (one lane): 2-D tensor copies of the codes (32 B x 256 rows per k-step),
-//              the scales (16 B x 256 rows per 256 k) and the fp16 activations (64 k x BM rows,
-//              128-byte swizzle) into a 3-stage ring; it also owns the tensor-memory allocation;
-//   warp 9     MMA issuer (one lane): per k-step, for each 128-row half of the weight tile, four
-//              tcgen05.mma kind::f16 (M = 128, N = BM, K = 16) with both operands in shared memory,
-//              fp32 accumulation in tensor memory (columns [256 t, 256 t + BM) for half t).
+//              converters (exact in fp16) and write the 64 fp16 weights into a tensor-memory A slot
+//              (tcgen05.st, the row's own lane), so the decoded weights never pass through shared
+//              memory.  After the k-loop they are the epilogue: tensor memory -> registers, times
+//              2^-e and the per-tensor scale, rounded to bf16 (one k-split) or stored as fp32 parts;
+//   warp 8     producer (one lane): 2-D tensor copies of the codes (32 B x 256 rows per k-step)
+//              and the fp16 activations (64 k x BM rows, 128-byte swizzle) into a load ring as
+//              deep as shared memory allows for BM (6 stages at BM = 192, up to 8), and of the
+//              scales (16 B x 256 rows per 256 k) into two stages; it also owns the tensor-memory
+//              allocation.  The decoded weights go to a separate 2-slot ring, so the copies run
+//              several k-steps ahead of the decode and the MMAs;
+//   warps 9-12 MMA issuers (one lane each), one per (128-row weight half, BM / 2 activation rows):
+//              per k-step four tcgen05.mma kind::f16 (M = 128, N = BM / 2, K = 16), A from tensor
+//              memory and B from shared memory, fp32 accumulation in tensor memory.
 // The weights are the MMA's A operand (M = weight rows) and the activations its B operand
 // (N = activation rows), so one decoded weight tile serves every activation row of the tile.
 //
@@ -40,39 +43,51 @@ namespace prefill {
 
 constexpr int kBN = 256;                 // weight rows per tile (two MMA tiles of 128)
 constexpr int kMmaM = 128;
-constexpr int kBMMax = 256;              // activation rows per tile (MMA N): a multiple of 16
+constexpr int kBMMax = 192;              // activation rows per tile: a multiple of 32 (two MMAs of N = BM / 2)
 constexpr int kKS = 64;                  // k per pipeline step: one 128-byte line of fp16
 constexpr int kStepsPerUnit = 4;         // one scale copy covers 256 k
-constexpr int kP = 3;                    // pipeline depth in k-steps
-constexpr int kATileBytes = kMmaM * kKS * 2;         // 16384: decoded weights of one MMA tile
-constexpr int kABytes = 2 * kATileBytes;             // 32768
-constexpr int kBOff = kABytes;                       // activations: BM x 128 bytes (<= 32 KB)
-constexpr int kCOff = kBOff + kBMMax * kKS * 2;      // codes: 256 rows x 32 bytes
-constexpr int kCBytes = kBN * kKS / 2;               // 8192
-constexpr int kStageBytes = kCOff + kCBytes;         // 73728 (a multiple of 1024)
-constexpr int kSBytes = kBN * 16;                    // 4096: scales of 256 k, 16 bytes per row
+constexpr int kASlots = 2;                    // decoded-weight ring (tensor memory)
+constexpr int kCBytes = kBN * kKS / 2;        // 8192: codes of a k-step, 32 bytes per row
+constexpr int kSBytes = kBN * 16;             // 4096: scales of 256 k, 16 bytes per row
 constexpr int kSStages = 2;
-constexpr int kSmemScales = kP * kStageBytes;        // 221184
-constexpr int kSmemBar = kSmemScales + kSStages * kSBytes;
+constexpr int kLPMax = 8;                     // load ring depth (codes + activations) at most
+// shared memory (offsets from the 1024-aligned base): barriers and misc in the first 1 KB, then
+// the scale stages and the load ring.  A load stage is [codes | activations]; its size (8 KB +
+// BM x 128 bytes, rounded up to 1 KB) and the ring depth lp depend on BM.
+constexpr int kSmemMisc = 768;                // +0 tensor-memory base, +4 abort flag
+constexpr int kSmemScales = 1024;
+constexpr int kSmemLoad = kSmemScales + kSStages * kSBytes;    // 9216
+constexpr int kSmemBytes = 232448;                             // the per-block maximum
+constexpr int kLoadBudget = kSmemBytes - 1024 - kSmemLoad;     // 1024: alignment slack
+// load stage bytes for a tile height bm, and the ring depth that fits
+__host__ __device__ constexpr int load_stage_bytes(int bm) { return (kCBytes + bm * kKS * 2 + 1023) / 1024 * 1024; }
+__host__ __device__ constexpr int load_stages(int bm) {
+  return kLoadBudget / load_stage_bytes(bm) < kLPMax ? kLoadBudget / load_stage_bytes(bm) : kLPMax;
+}
+static_assert(load_stages(kBMMax) >= 3, "ring depth at the tallest tile");
 // mbarriers
-constexpr int kBarCFull = 0;                 // [kP] codes copied (tx)      -> decoders
-constexpr int kBarBFull = kBarCFull + kP;    // [kP] activations copied (tx) -> issuer
-constexpr int kBarAFull = kBarBFull + kP;    // [kP] 256 decoder arrivals   -> issuer
-constexpr int kBarEmpty = kBarAFull + kP;    // [kP] MMA commit             -> producer
-constexpr int kBarSFull = kBarEmpty + kP;    // [2]  scales copied (tx)     -> decoders
-constexpr int kBarSEmpty = kBarSFull + kSStages;  // [2] 256 decoder arrivals -> producer
-constexpr int kBarDFull = kBarSEmpty + kSStages;  // accumulators final      -> epilogue
+constexpr int kBarCFull = 0;                        // [lp] codes copied (tx)        -> decoders
+constexpr int kBarBFull = kBarCFull + kLPMax;       // [lp] activations copied (tx)  -> issuer
+constexpr int kBarLEmpty = kBarBFull + kLPMax;      // [lp] 4 issuer commits: free   -> producer
+constexpr int kBarAFull = kBarLEmpty + kLPMax;      // [2]  8 decoder-warp arrivals  -> issuer
+constexpr int kBarAEmpty = kBarAFull + kASlots;     // [2]  4 issuer commits: free   -> decoders
+constexpr int kBarSFull = kBarAEmpty + kASlots;     // [2]  scales copied (tx)       -> decoders
+constexpr int kBarSEmpty = kBarSFull + kSStages;    // [2]  8 decoder-warp arrivals  -> producer
+constexpr int kBarDFull = kBarSEmpty + kSStages;    // 4 issuer commits: D final     -> epilogue
 constexpr int kNumBars = kBarDFull + 1;
-constexpr int kSmemMisc = kSmemBar + kNumBars * 8;  // +0 tensor-memory base, +4 abort flag
-constexpr int kSmemBytes = kSmemMisc + 16 + 1024;   // misc + alignment slack
-static_assert(kSmemBytes <= 232448, "shared memory per block");
-static_assert(kStageBytes % 1024 == 0 && kATileBytes % 1024 == 0 && kBOff % 1024 == 0, "swizzle atoms");
+static_assert(kNumBars * 8 <= kSmemMisc, "barriers before misc");
+static_assert(kSmemLoad % 1024 == 0, "swizzle atoms");
 
 constexpr int kDecodeWarps = 8;
 constexpr int kProducerWarp = 8;
-constexpr int kIssuerWarp = 9;
-constexpr int kThreads = 10 * 32;
-constexpr uint32_t kTmemCols = 512;  // half t accumulates in columns [256 t, 256 t + BM); one block per SM
+constexpr int kIssuerWarp0 = 9;  // issuer q: weight half q / 2, activation-row half q % 2
+constexpr int kIssuers = 4;
+constexpr int kThreads = (kIssuerWarp0 + kIssuers) * 32;  // 416
+// tensor memory: half t accumulates in columns [192 t, 192 t + BM); A slot s of half t (64 k of
+// fp16 pairs) is columns 384 + 64 s + 32 t; one block per SM
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kDCol = 192;
+__device__ __forceinline__ uint32_t a_col_pf(int s, int t) { return 384u + (uint32_t)(64 * s + 32 * t); }
 constexpr int kPrepThreads = 256;
 
 // instruction descriptor: kind::f16, D = f32, A = B = f16, both K-major, N = bm, M = 128
@@ -90,6 +105,7 @@ struct PrefillParams {
   int* err;               // error word
   float gs;
   int M, bm, m_tiles, n_tiles, splits;
+  int lp;                 // load ring depth: load_stages(bm)
   int64_t N, K;
 };
 
@@ -124,16 +140,6 @@ __global__ void __launch_bounds__(kPrepThreads) prefill_x_prep_kernel(const uint
   }
 }
 
-// D[tmem] (+)= A[smem descriptor] * B[smem descriptor]; kind::f16, issued by one thread.
-__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t id,
-                                           uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(id), "r"(accumulate)
-      : "memory");
-}
-
 // ------------------------------------------------------------------ main kernel
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -142,14 +148,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemMisc + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = ptx::smem_addr(smem);
-  const uint32_t bar_base = smem_base + (uint32_t)kSmemBar;
-  auto bar = [&](int i) { return bar_base + 8u * (uint32_t)i; };
+  auto bar = [&](int i) { return smem_base + 8u * (uint32_t)i; };
 
   // tile of this block: activation tiles fastest, so the blocks that share a weight tile run together
   const int b = blockIdx.x;
   const int mt = b % p.m_tiles, rest = b / p.m_tiles;
   const int nt = rest % p.n_tiles, sp = rest / p.n_tiles;
-  const int BM = p.bm;
+  const int BM = p.bm, LP = p.lp;
+  const int LS = load_stage_bytes(BM);
   const int m0 = mt * BM;
   const int n0 = nt * kBN;
   const int64_t U = p.K / (kKS * kStepsPerUnit);
@@ -157,17 +163,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const int nsteps = (int)(u1 - u0) * kStepsPerUnit;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kP; ++s) {
+    for (int s = 0; s < LP; ++s) {
       ptx::mbar_init(bar(kBarCFull + s), 1);
       ptx::mbar_init(bar(kBarBFull + s), 1);
-      ptx::mbar_init(bar(kBarAFull + s), kDecodeWarps * 32);
-      ptx::mbar_init(bar(kBarEmpty + s), 1);
+      ptx::mbar_init(bar(kBarLEmpty + s), kIssuers);
+    }
+    for (int s = 0; s < kASlots; ++s) {
+      ptx::mbar_init(bar(kBarAFull + s), kDecodeWarps);
+      ptx::mbar_init(bar(kBarAEmpty + s), kIssuers);
     }
     for (int s = 0; s < kSStages; ++s) {
       ptx::mbar_init(bar(kBarSFull + s), 1);
-      ptx::mbar_init(bar(kBarSEmpty + s), kDecodeWarps * 32);
+      ptx::mbar_init(bar(kBarSEmpty + s), kDecodeWarps);
     }
-    ptx::mbar_init(bar(kBarDFull), 1);
+    ptx::mbar_init(bar(kBarDFull), kIssuers);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -186,27 +195,28 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   if (warp < kDecodeWarps) {
     // ================================================================ decoders, then epilogue
     const int r = warp * 32 + lane;  // weight row of the tile
-    const int t = r >> 7, rr = r & (kMmaM - 1);
-    const int swz = rr & 7;
-    const uint32_t a_off = (uint32_t)(t * kATileBytes + (rr >> 3) * 1024 + (rr & 7) * 128);
+    const int t = r >> 7;
+    const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // lanes of this warp's 32 rows
     bool ok = true;
     for (int j = 0; j < nsteps; ++j) {
-      const int st = j % kP;
-      const uint32_t ph = (uint32_t)((j / kP) & 1);
-      const int u = j >> 2, q = j & 3, ss = u & 1;
+      const int st = j % LP;
+      const int u = j >> 2, q = j & 3, ss = u & 1, as = j & 1;
       if (q == 0 && ok) ok = wait_bar(bar(kBarSFull + ss), (uint32_t)((u >> 1) & 1), ab);
-      if (ok) ok = wait_bar(bar(kBarCFull + st), ph, ab);
+      if (ok) ok = wait_bar(bar(kBarCFull + st), (uint32_t)((j / LP) & 1), ab);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
-      uint8_t* stage = smem + st * kStageBytes;
-      const uint4 c0 = *reinterpret_cast<const uint4*>(stage + kCOff + r * 32);
-      const uint4 c1 = *reinterpret_cast<const uint4*>(stage + kCOff + r * 32 + 16);
+      const uint8_t* codes = smem + kSmemLoad + st * LS + r * 32;
+      const uint4 c0 = *reinterpret_cast<const uint4*>(codes);
+      const uint4 c1 = *reinterpret_cast<const uint4*>(codes + 16);
       const uint32_t sw = *reinterpret_cast<const uint32_t*>(smem + kSmemScales + ss * kSBytes + r * 16 + q * 4);
-      if (q == kStepsPerUnit - 1) ptx::mbar_arrive(bar(kBarSEmpty + ss));  // this unit's scales are read
       const uint32_t s0 = ptx::e4m3_pair(sw, 0), s1 = ptx::e4m3_pair(sw, 1);
       const uint32_t s2 = ptx::e4m3_pair(sw, 2), s3 = ptx::e4m3_pair(sw, 3);
+      if (q == kStepsPerUnit - 1) {  // this unit's scales are in registers: one arrival per warp
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar(kBarSEmpty + ss));
+      }
       uint32_t o[32];
       ptx::e2m1x8_scaled(c0.x, s0, o[0], o[1], o[2], o[3]);
       ptx::e2m1x8_scaled(c0.y, s0, o[4], o[5], o[6], o[7]);
@@ -216,14 +226,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       ptx::e2m1x8_scaled(c1.y, s2, o[20], o[21], o[22], o[23]);
       ptx::e2m1x8_scaled(c1.z, s3, o[24], o[25], o[26], o[27]);
       ptx::e2m1x8_scaled(c1.w, s3, o[28], o[29], o[30], o[31]);
-      // 16-byte chunk c (k 8c .. 8c + 7) of the row goes to chunk c ^ (row % 8) of its line; the
-      // stage's A area is free: its codes were copied only after the MMAs that last read it ended
-      uint8_t* arow = stage + a_off;
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(arow + ((c ^ swz) << 4)) = make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
-      ptx::fence_proxy_async_smem();  // generic-proxy writes -> the tensor core's reads
-      ptx::mbar_arrive(bar(kBarAFull + st));
+      // the A slot must be free: the MMAs of step j - 2 have completed
+      if (!__all_sync(0xffffffffu, wait_bar(bar(kBarAEmpty + as), (uint32_t)(((j >> 1) & 1) ^ 1), ab))) {
+        ok = false;
+        break;
+      }
+      // column c of the row's A slot holds k 2c, 2c + 1 of the step
+      ptx::tc_fence_after();
+      ptx::tmem_st32(t_lane + a_col_pf(as, t), o);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();  // the warp's stores are complete before its one arrival
+      if (lane == 0) ptx::mbar_arrive(bar(kBarAFull + as));
     }
 
     // ---- epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. + 31 of half w / 4
@@ -234,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const int quad = warp & 3;
       const int64_t n = n0 + r;  // r = t * 128 + quad * 32 + lane
       const bool n_in = n < p.N;
-      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(t * kBMMax);
+      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)t * kDCol;
       const int M = p.M;
       const float gs = p.gs;
       for (int c = 0; c < BM / 16; ++c) {
@@ -282,45 +296,49 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                            n0, bar(kBarSFull + ss), pol_w);
           units_issued = u + 1;
         }
-        const int st = j % kP;
-        if (!wait_bar(bar(kBarEmpty + st), (uint32_t)(((j / kP) & 1) ^ 1), ab)) break;
+        const int st = j % LP;
+        if (!wait_bar(bar(kBarLEmpty + st), (uint32_t)(((j / LP) & 1) ^ 1), ab)) break;
         const int64_t g = u0 * kStepsPerUnit + j;  // global k-step
-        const uint32_t stage = smem_base + (uint32_t)(st * kStageBytes);
+        const uint32_t stage = smem_base + (uint32_t)(kSmemLoad + st * LS);
         ptx::mbar_arrive_expect_tx(bar(kBarCFull + st), (uint32_t)kCBytes);
-        ptx::tma_load_2d(stage + kCOff, &p.tm_codes, (int32_t)(g * (kKS / 2)), n0, bar(kBarCFull + st), pol_w);
+        ptx::tma_load_2d(stage, &p.tm_codes, (int32_t)(g * (kKS / 2)), n0, bar(kBarCFull + st), pol_w);
         ptx::mbar_arrive_expect_tx(bar(kBarBFull + st), xbytes);
-        ptx::tma_load_2d(stage + kBOff, &p.tm_x, (int32_t)(g * kKS), m0, bar(kBarBFull + st), pol_x);
+        ptx::tma_load_2d(stage + kCBytes, &p.tm_x, (int32_t)(g * kKS), m0, bar(kBarBFull + st), pol_x);
         issued = j + 1;
       }
       // every copy this thread started has landed before the block can exit (normally they were
       // all consumed already; after an abort this bounded wait keeps shared memory owned)
-      for (int j = issued - kP < 0 ? 0 : issued - kP; j < issued; ++j) {
-        const uint32_t ph = (uint32_t)((j / kP) & 1);
-        (void)wait_bar(bar(kBarCFull + j % kP), ph, ab, false);
-        (void)wait_bar(bar(kBarBFull + j % kP), ph, ab, false);
+      for (int j = issued - LP < 0 ? 0 : issued - LP; j < issued; ++j) {
+        const uint32_t ph = (uint32_t)((j / LP) & 1);
+        (void)wait_bar(bar(kBarCFull + j % LP), ph, ab, false);
+        (void)wait_bar(bar(kBarBFull + j % LP), ph, ab, false);
       }
       for (int u = units_issued - kSStages < 0 ? 0 : units_issued - kSStages; u < units_issued; ++u)
         (void)wait_bar(bar(kBarSFull + (u & 1)), (uint32_t)((u >> 1) & 1), ab, false);
     }
   } else {
-    // ================================================================ MMA issuer
+    // ================================================================ MMA issuers
+    // Four issuing threads, one per (weight half t, activation-row half h): one thread sustains
+    // only about one MMA per 70-100 cycles, so the k-step's MMAs are spread over four of them,
+    // each into its own accumulator columns [192 t + h BM / 2, + BM / 2).
     if (lane == 0) {
-      const uint32_t id = idesc_bm(BM);
+      const int q = warp - kIssuerWarp0, t = q >> 1, h = q & 1;
+      const int nh = BM / 2;
+      const uint32_t id = idesc_bm(nh);
+      const uint32_t d = tmem + (uint32_t)t * kDCol + (uint32_t)(h * nh);
       for (int j = 0; j < nsteps; ++j) {
-        const int st = j % kP;
-        const uint32_t ph = (uint32_t)((j / kP) & 1);
-        if (!wait_bar(bar(kBarAFull + st), ph, ab)) break;
-        if (!wait_bar(bar(kBarBFull + st), ph, ab)) break;
+        const int st = j % LP, as = j & 1;
+        if (!wait_bar(bar(kBarAFull + as), (uint32_t)((j >> 1) & 1), ab)) break;
+        if (!wait_bar(bar(kBarBFull + st), (uint32_t)((j / LP) & 1), ab)) break;
         ptx::tc_fence_after();
-        const uint32_t stage = smem_base + (uint32_t)(st * kStageBytes);
+        // activation rows h BM / 2 .. of the stage: (BM / 2) / 8 groups of 1 KB further on
+        const uint32_t xb = smem_base + (uint32_t)(kSmemLoad + st * LS + kCBytes + h * nh * (kKS * 2));
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-#pragma unroll
-          for (int kk = 0; kk < kKS / 16; ++kk)
-            mma_f16_ss(tmem + (uint32_t)(t * kBMMax), x_desc(stage + (uint32_t)(t * kATileBytes + kk * 32)),
-                       x_desc(stage + (uint32_t)(kBOff + kk * 32)), id, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        ptx::mma_commit(bar(kBarEmpty + st));
+        for (int kk = 0; kk < kKS / 16; ++kk)
+          ptx::mma_f16_ts(d, tmem + a_col_pf(as, t) + (uint32_t)(kk * 8), x_desc(xb + (uint32_t)(kk * 32)), id,
+                          (j > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_commit(bar(kBarLEmpty + st));
+        ptx::mma_commit(bar(kBarAEmpty + as));
       }
       // every MMA issued so far completes before the accumulators are read or released
       ptx::mma_commit(bar(kBarDFull));

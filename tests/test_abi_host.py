@@ -177,13 +177,13 @@ def test_prefill_geometry_invariants(N, K, sms):
         g = nb.nvfp4_prefill_geometry(N, K, M, sms)
         assert g == nb.nvfp4_prefill_geometry(N, K, M, sms)
         bm, mt = g["bm"], g["m_tiles"]
-        assert bm % 16 == 0 and 16 <= bm <= 256, g
+        assert bm % 32 == 0 and 32 <= bm <= 192, g
         assert mt * bm >= M and (mt - 1) * bm < M, g
         assert g["n_tiles"] == -(-N // 256)
         assert 1 <= g["splits"] <= min(U, 32)
         assert g["grid"] == mt * g["n_tiles"] * g["splits"]
         assert g["launches_per_call"] == (3 if g["splits"] > 1 else 2)
-        assert g["threads"] == 320 and g["sm_count"] == sms
+        assert g["threads"] == 416 and g["sm_count"] == sms
         assert 0 < g["smem_bytes"] <= 232448
         assert g["M"] == M and g["N"] == N and g["K"] == K
 

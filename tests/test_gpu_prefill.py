@@ -3,7 +3,7 @@ through the C ABI against the CPU oracle.
 
 Same acceptance bound as the skinny path: |y - y_ref| <= 4e-3 * sum_k |w_k x_k| + one bfloat16
 ulp of |y_ref|, per element.  The shapes are chosen so that the launch geometry covers one and
-several activation tiles with a ragged last tile, tile heights from 16 to 256, weight row counts
+several activation tiles with a ragged last tile, tile heights from 32 to 192, weight row counts
 below one tile and with a ragged last tile, and one and several k-splits (the reduction launch).
 """
 import numpy as np
@@ -37,12 +37,12 @@ def _geometry(plan, M):
 
 
 @pytest.mark.parametrize("N,K,M", [
-    (640, 512, 33),      # three activation tiles of 16, three weight tiles (ragged)
+    (640, 512, 33),      # two activation tiles of 32, three weight tiles (ragged)
     (300, 768, 100),     # N between one and two weight tiles
     (17, 256, 40),       # N below one weight tile, one 256-k unit
-    (513, 1280, 257),    # seventeen activation tiles, ragged in both dimensions
-    (1024, 4096, 64),    # k split eight ways: the reduction launch
-    (1024, 8192, 100),   # k split eleven ways with a 48-row tile
+    (513, 1280, 257),    # nine activation tiles, ragged in both dimensions
+    (1024, 4096, 64),    # k split sixteen ways: the reduction launch
+    (1024, 8192, 100),   # k split eight ways, four activation tiles
 ])
 def test_small_shapes_every_element(N, K, M):
     case = Case(N, K, M, seed=900 + N + K + M, outlier_frac=0.01)
@@ -79,7 +79,7 @@ def _sampled(plan, case, M, n_samples=512, seed=0):
 
 @pytest.mark.parametrize("N,K,M", [
     (34816, 512, 160),   # one 160-row activation tile, 136 weight tiles
-    (38400, 256, 250),   # a 256-row tile with 6 rows past M
+    (38400, 256, 250),   # two 128-row tiles, 6 rows past M
     (20000, 1024, 200),  # three 80-row tiles, ragged weight tile
 ])
 def test_tall_tiles_sampled(N, K, M):
@@ -157,3 +157,54 @@ def test_argument_errors():
             nb.nvfp4_prefill_plan_create(*bad)
     info = nb.nvfp4_prefill_plan_get_info(plan, 64)
     assert info["max_M"] == 64 and info["workspace_bytes"] > 0
+
+
+@pytest.mark.parametrize("bm,splits", [(32, 1), (32, 3), (64, 8), (64, 1), (96, 5), (128, 2), (160, 4), (192, 1)])
+def test_forced_geometries_every_element(bm, splits):
+    """Every tile height band and split through the explicit-geometry entry point: each one is
+    within the tolerance on every element (N = 1024, K = 4096, M = 100)."""
+    N, K, M = 1024, 4096, 100
+    case = _forced_case()
+    plan = nb.nvfp4_prefill_plan_create(N, K, M)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    nb.nvfp4_prefill_linear_ex(plan, case.d_x, M, case.d_codes, case.d_scales, case.gs, y, bm=bm, splits=splits)
+    torch.cuda.synchronize()
+    assert nb.nvfp4_prefill_plan_check(plan) == nb.NVFP4_OK
+    y_ref, absdot = _forced_ref()
+    ok, ratio = within_tolerance(to_f64(y), y_ref, absdot)
+    assert ok, (bm, splits, "max |err|/tol = %.3g" % ratio)
+
+
+_FORCED = {}
+
+
+def _forced_case():
+    if "case" not in _FORCED:
+        _FORCED["case"] = Case(1024, 4096, 100, seed=77, outlier_frac=0.01)
+    return _FORCED["case"]
+
+
+def _forced_ref():
+    if "ref" not in _FORCED:
+        _FORCED["ref"] = _forced_case().oracle_full()
+    return _FORCED["ref"]
+
+
+def test_forced_geometry_refusals():
+    N, K, M = 512, 512, 40
+    plan = nb.nvfp4_prefill_plan_create(N, K, M)
+    case = Case(N, K, M, seed=4)
+    y = torch.full((M, N), 3.0, dtype=torch.bfloat16, device="cuda")
+
+    def call(bm, splits):
+        return nb.nvfp4_prefill_linear_ex(plan, case.d_x, M, case.d_codes, case.d_scales, 1.0, y, bm=bm,
+                                          splits=splits, check=False)
+
+    for bm, splits in [(16, 1), (48, 1), (208, 1), (256, 1), (-32, 1), (32, -1), (32, 3), (32, 33)]:
+        assert call(bm, splits) == nb.NVFP4_ERR_ARG, (bm, splits)
+    # a split the plan's part buffer was not sized for
+    info = nb.nvfp4_prefill_plan_get_info(plan, M)
+    if info["workspace_bytes"] < 2 * M * N * 4:
+        assert call(32, 2) == nb.NVFP4_ERR_SCRATCH_LIMIT
+    torch.cuda.synchronize()
+    assert bool((y == 3.0).all()), "a refused call wrote y"
