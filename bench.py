@@ -14,6 +14,9 @@ activations copied in and the output copied back, every call.
 
 Under torchrun (N > 1) every rank runs its own replica of the workload (weak
 scaling); the time is the max over ranks and `value` sums all ranks' bytes.
+
+`other_workloads` adds the other projection shapes, the 64-layer decode round and the prefill
+projection (M = 64 / 256 / 1024, TFLOP/s against the dense bf16 tensor peak).
 """
 import argparse
 import hashlib
@@ -368,7 +371,56 @@ def run_other_workloads(stream, rank, peak):
             del proj
             torch.cuda.empty_cache()
     res["round"] = run_round(stream, rank, peak)
+    res["prefill"] = run_prefill(stream, rank)
     return res
+
+
+def bf16_peak():
+    """Dense bf16 tensor peak in TFLOP/s (the fp16 MMAs of the prefill run at the same rate)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+PREFILL_MS = (64, 256, 1024)
+
+
+def run_prefill(stream, rank):
+    """The prefill projection (row counts above the skinny band) on the stated projection shapes:
+    time per call over rotating cold weight copies, TFLOP/s against the dense bf16 tensor peak."""
+    import torch
+    from nvfp4_skinny_gb300 import binding as nb
+    from nvfp4_skinny_gb300 import synth
+    tpeak, tsrc = bf16_peak()
+    out = {"peak_tflops": tpeak, "peak_source": tsrc,
+           "timing": "CUDA graph of back-to-back calls (activation preparation, projection and, when the "
+                     "k-range is split, the reduction), rotating weight copies > 2x L2"}
+    for name, N, K in (("square", 5120, 5120), ("qkv", 7168, 5120), ("gate_up", 34816, 5120),
+                       ("down", 5120, 17408)):
+        per_copy = call_bytes(N, K, 1)
+        copies = min(16, max(2, -(-2 * L2_BYTES // per_copy)))
+        ws = [synth.weights(N, K, 300 + 7919 * i + 1000 * rank, device="cuda") for i in range(copies)]
+        plan = nb.nvfp4_prefill_plan_create(N, K, max(PREFILL_MS))
+        entry = {}
+        for M in PREFILL_MS:
+            x = synth.activations(M, K, 5, device="cuda")
+            y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            calls = [(lambda c=c, sc=sc, gs=gs: nb.nvfp4_prefill_linear(plan, x, M, c, sc, gs, y, stream=stream))
+                     for (c, sc, gs) in ws]
+            t_call = _time_graph(make_graph(calls, stream), stream, 5) / copies  # ms
+            tf = 2.0 * M * N * K / (t_call * 1e-3) / 1e12
+            g = nb.nvfp4_prefill_plan_get_info(plan, M)
+            entry[str(M)] = {"us_per_call": round(t_call * 1e3, 2), "TFLOPs": round(tf, 1),
+                             "frac_of_peak": round(tf / tpeak, 4), "bm": g["bm"], "m_tiles": g["m_tiles"],
+                             "splits": g["splits"], "grid": g["grid"], "launches": g["launches_per_call"]}
+        assert nb.nvfp4_prefill_plan_check(plan, stream) == nb.NVFP4_OK
+        out["%s %dx%d" % (name, N, K)] = entry
+        del ws, plan
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_round(stream, rank, peak):
@@ -519,6 +571,31 @@ def profile_shape(args):
     print("profiled shape N=%d K=%d M=%d copies=%d calls=%d" % (N, K, M, copies, args.warmup + args.steps))
 
 
+def profile_prefill(args):
+    """A few prefill calls of one shape on rotating cold weights (> 2x L2), for ncu captures."""
+    import torch
+    from nvfp4_skinny_gb300 import binding as nb
+    from nvfp4_skinny_gb300 import build as nbuild
+    from nvfp4_skinny_gb300 import synth
+    nbuild.build()
+    N, K, M = (int(v) for v in args.profile_prefill.split(","))
+    copies = max(2, -(-2 * L2_BYTES // call_bytes(N, K, 1)))
+    ws = [synth.weights(N, K, 77 + 7919 * i, device="cuda") for i in range(copies)]
+    plan = nb.nvfp4_prefill_plan_create(N, K, M)
+    x = synth.activations(M, K, 77, device="cuda")
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
+    for i in range(args.warmup + args.steps):
+        c, sc, gs = ws[i % copies]
+        nb.nvfp4_prefill_linear(plan, x, M, c, sc, gs, y)
+    torch.cuda.synchronize()
+    st = nb.nvfp4_prefill_plan_check(plan)
+    if st != nb.NVFP4_OK:
+        raise RuntimeError(nb.nvfp4_status_string(st))
+    print("profiled prefill N=%d K=%d M=%d copies=%d calls=%d geometry=%s" % (
+        N, K, M, copies, args.warmup + args.steps, nb.nvfp4_prefill_plan_get_info(plan, M)))
+
+
 # ----------------------------------------------------------------------------- distributed plumbing
 
 def dist_init():
@@ -563,9 +640,13 @@ def main(argv=None):
     ap.add_argument("--quick", action="store_true", help="skip the other workloads")
     ap.add_argument("--profile-shape", default=None, metavar="N,K,M[,f32]",
                     help="profiling driver: run --warmup then --steps calls of one shape on cold weights, no JSON")
+    ap.add_argument("--profile-prefill", default=None, metavar="N,K,M",
+                    help="run a few prefill calls of one shape (for ncu) and exit")
     args = ap.parse_args(argv)
     if args.profile_shape:
         return profile_shape(args)
+    if args.profile_prefill:
+        return profile_prefill(args)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world = dist_init()
