@@ -61,18 +61,19 @@ void fill(int64_t N, int M, int bm, int splits, int sms, nvfp4_prefill_info* g) 
 }
 
 // The geometry of a call: for every tile height bm (a multiple of 32, balanced over the m-tiles)
-// and k-split s, the modelled time is the waves of blocks times a block's k-loop (a k-step costs
-// the larger of its 8 MMAs and the decode) plus a fixed cost per block, bounded below by the HBM
-// time of the call's bytes; a split adds the parts' write and read and one launch.  The smallest
-// wins; ties keep fewer splits and then the taller tile.  Integer and double host arithmetic only,
-// so the choice is the same on every host.
+// and k-split s, the modelled time is the waves of blocks times a block's k-loop plus a fixed cost
+// per block, bounded below by the HBM time of the call's bytes; a split adds the parts' write and
+// read and one launch.  A 64-k step costs the larger of its MMAs at the tensor peak and a hand-off
+// floor of about 1,400 cycles that grows slowly with bm (measured on GB300: 0.67 us at bm = 64,
+// 0.75 us at bm = 160).  The smallest wins; ties keep fewer splits and then the taller tile.
+// Double host arithmetic only, so the choice is the same on every host.
 bool geometry(int64_t N, int64_t K, int M, int sms, nvfp4_prefill_info* g) {
   const int64_t U = K / 256;
   const int64_t n_tiles = (N + pf::kBN - 1) / pf::kBN;
   double best = 1e300;
   int best_bm = 32, best_s = 1;
   int64_t best_mt = 0;
-  const double clock_hz = 1.9e9, hbm_bps = 6.5e12;
+  const double clock_hz = 2.0e9, hbm_bps = 6.5e12;
   const double t_hbm = ((double)N * (double)K * 0.5625 + 2.0 * M * (double)K + 2.0 * M * (double)N) / hbm_bps;
   for (int bm = 32; bm <= pf::kBMMax; bm += 32) {
     const int64_t mt = (M + bm - 1) / bm;
@@ -84,9 +85,10 @@ bool geometry(int64_t N, int64_t K, int M, int sms, nvfp4_prefill_info* g) {
       if (blocks > 0x7FFFFFFF) continue;  // one launch's grid
       const int64_t waves = (blocks + sms - 1) / sms;
       const int64_t steps = 4 * ((U + s - 1) / s);
-      const double mma = 8.0 * (0.58 * bm > 40.0 ? 0.58 * bm : 40.0);
-      const double step = mma > 260.0 ? mma : 260.0;
-      double t = (double)waves * ((double)steps * step + 3000.0 + 24.0 * bm) / clock_hz;
+      const double mma = 16.0 * 0.29 * bm;  // 16 MMAs of N = bm / 2 at 128 x 16 per 0.29 column-cycle
+      const double floor = 1350.0 + 1.2 * bm;
+      const double step = mma > floor ? mma : floor;
+      double t = (double)waves * ((double)steps * step + 4000.0 + 24.0 * bm) / clock_hz;
       if (t < t_hbm) t = t_hbm;
       if (s > 1) t += (2.0 * (double)s * M * (double)N * 4.0) / hbm_bps + 2e-6;
       if (t < best * (1.0 - 1e-9)) {
