@@ -45,7 +45,8 @@ extern "C" {
 typedef struct nvfp4_prefill_plan* nvfp4_prefill_plan_t;
 
 /* Launch geometry of one call: tiles of 256 weight rows x bm activation rows (bm a multiple of
- * 32, at most 192), split over `splits` contiguous k-ranges of 256-k units. */
+ * 32, at most 192 with 64-k pipeline steps and at most 128 with 128-k steps), split over
+ * `splits` contiguous k-ranges of 256-k units. */
 typedef struct nvfp4_prefill_info {
   int64_t N, K;
   int32_t M;
@@ -58,7 +59,7 @@ typedef struct nvfp4_prefill_info {
   int32_t sm_count;
   int32_t max_M;             /* the plan's (0 from nvfp4_prefill_geometry) */
   int32_t load_stages;       /* depth of the main launch's copy ring (codes + activations) */
-  int32_t reserved;
+  int32_t k_step;            /* k per pipeline step of the main launch: 64 (bm <= 192) or 128 (bm <= 128) */
   int64_t workspace_bytes;   /* the plan's device workspace (0 from nvfp4_prefill_geometry) */
   int64_t smem_bytes;        /* dynamic shared memory per block of the main launch */
 } nvfp4_prefill_info;
@@ -82,15 +83,16 @@ void nvfp4_prefill_plan_destroy(nvfp4_prefill_plan_t plan);
 nvfp4_status nvfp4_prefill_linear(nvfp4_prefill_plan_t plan, const void* x, int M, const uint8_t* w_codes,
                                   const uint8_t* w_block_scales, float w_global_scale, void* y, void* stream);
 
-/* As nvfp4_prefill_linear with an explicit geometry: bm (a multiple of 32 in 32..192) activation
- * rows per tile and `splits` k-ranges (1..min(K/256, 32)); 0 keeps the automatic choice of either.
- * NVFP4_ERR_ARG for values outside those ranges; NVFP4_ERR_SCRATCH_LIMIT when the split's parts
+/* As nvfp4_prefill_linear with an explicit geometry: bm (a multiple of 32) activation rows per
+ * tile, `splits` k-ranges (1..min(K/256, 32)) and the k per pipeline step, k_step (64, with
+ * bm <= 192, or 128, with bm <= 128); 0 keeps the automatic choice of each (a bm above 128 implies
+ * 64-k steps).  NVFP4_ERR_ARG for values outside those ranges; NVFP4_ERR_SCRATCH_LIMIT when the split's parts
  * (splits x M x N x 4 bytes) exceed the plan's part buffer, which is sized for the automatic
  * geometry of every M <= max_M.  The result stays within the stated tolerance for every geometry;
  * its bits depend on the split. */
 nvfp4_status nvfp4_prefill_linear_ex(nvfp4_prefill_plan_t plan, const void* x, int M, const uint8_t* w_codes,
                                      const uint8_t* w_block_scales, float w_global_scale, void* y, int bm, int splits,
-                                     void* stream);
+                                     int k_step, void* stream);
 
 /* Synchronises `stream`, then reads and clears the plan's error word: NVFP4_ERR_TIMEOUT if a
  * kernel-side wait ran out since the last check. */

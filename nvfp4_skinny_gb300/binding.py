@@ -73,7 +73,7 @@ class PrefillInfo(ctypes.Structure):
                 ("m_tiles", ctypes.c_int32), ("n_tiles", ctypes.c_int32), ("splits", ctypes.c_int32),
                 ("grid", ctypes.c_int32), ("threads", ctypes.c_int32), ("launches_per_call", ctypes.c_int32),
                 ("sm_count", ctypes.c_int32), ("max_M", ctypes.c_int32), ("load_stages", ctypes.c_int32),
-                ("reserved", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
+                ("k_step", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
                 ("smem_bytes", ctypes.c_int64)]
 
 
@@ -129,7 +129,7 @@ def cuda_lib():
         lib.nvfp4_prefill_linear.restype = i32
         lib.nvfp4_prefill_linear.argtypes = [p, p, i32, p, p, ctypes.c_float, p, p]
         lib.nvfp4_prefill_linear_ex.restype = i32
-        lib.nvfp4_prefill_linear_ex.argtypes = [p, p, i32, p, p, ctypes.c_float, p, i32, i32, p]
+        lib.nvfp4_prefill_linear_ex.argtypes = [p, p, i32, p, p, ctypes.c_float, p, i32, i32, i32, p]
         lib.nvfp4_prefill_plan_check.restype = i32
         lib.nvfp4_prefill_plan_check.argtypes = [p, p]
         lib.nvfp4_prefill_plan_get_info.restype = i32
@@ -377,12 +377,13 @@ def nvfp4_prefill_linear(plan, x, M, w_codes, w_block_scales, w_global_scale, y,
     return st
 
 
-def nvfp4_prefill_linear_ex(plan, x, M, w_codes, w_block_scales, w_global_scale, y, bm=0, splits=0, stream=None,
-                            check=True):
-    """nvfp4_prefill_linear with an explicit tile height bm and k-split (0 = automatic)."""
+def nvfp4_prefill_linear_ex(plan, x, M, w_codes, w_block_scales, w_global_scale, y, bm=0, splits=0, k_step=0,
+                            stream=None, check=True):
+    """nvfp4_prefill_linear with an explicit tile height bm, k-split and k per pipeline step
+    (0 = automatic)."""
     st = cuda_lib().nvfp4_prefill_linear_ex(plan.as_parameter if isinstance(plan, PrefillPlan) else plan, _ptr(x),
                                             int(M), _ptr(w_codes), _ptr(w_block_scales), float(w_global_scale),
-                                            _ptr(y), int(bm), int(splits), _stream(stream))
+                                            _ptr(y), int(bm), int(splits), int(k_step), _stream(stream))
     if check:
         _check(st, "nvfp4_prefill_linear_ex")
     return st

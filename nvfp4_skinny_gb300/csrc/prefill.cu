@@ -20,9 +20,9 @@ struct nvfp4_prefill_plan {
   int max_M = 0;
   int device = 0;
   int sm_count = 0;
-  const void* tm_codes_ptr = nullptr;
+  const void* tm_codes_ptr[2] = {nullptr, nullptr};  // per k-step: 64, 128
   const void* tm_scales_ptr = nullptr;
-  CUtensorMap tm_codes;
+  CUtensorMap tm_codes[2];
   CUtensorMap tm_scales;
   int tm_x_M = 0, tm_x_bm = 0;  // the activation map depends on (M, bm) only: the plan owns x16
   CUtensorMap tm_x;
@@ -45,7 +45,7 @@ bool shape_ok(int64_t N, int64_t K) {
   return N < (int64_t(1) << 31) && K <= (int64_t(1) << 24) && N <= (int64_t(1) << 40) / K;
 }
 
-void fill(int64_t N, int M, int bm, int splits, int sms, nvfp4_prefill_info* g) {
+void fill(int64_t N, int M, int ks, int bm, int splits, int sms, nvfp4_prefill_info* g) {
   const int64_t n_tiles = (N + pf::kBN - 1) / pf::kBN, mt = (M + bm - 1) / bm;
   g->M = M;
   g->bm = bm;
@@ -57,25 +57,28 @@ void fill(int64_t N, int M, int bm, int splits, int sms, nvfp4_prefill_info* g) 
   g->launches_per_call = splits > 1 ? 3 : 2;
   g->sm_count = sms;
   g->smem_bytes = pf::kSmemBytes;
-  g->load_stages = pf::load_stages(bm);
+  g->load_stages = pf::load_stages(ks, bm);
+  g->k_step = ks;
 }
 
-// The geometry of a call: for every tile height bm (a multiple of 32, balanced over the m-tiles)
-// and k-split s, the modelled time is the waves of blocks times a block's k-loop plus a fixed cost
-// per block, bounded below by the HBM time of the call's bytes; a split adds the parts' write and
-// read and one launch.  A 64-k step costs the larger of its MMAs at the tensor peak and a hand-off
-// floor of about 1,400 cycles that grows slowly with bm (measured on GB300: 0.67 us at bm = 64,
-// 0.75 us at bm = 160).  The smallest wins; ties keep fewer splits and then the taller tile.
-// Double host arithmetic only, so the choice is the same on every host.
+// The geometry of a call: for each k-step KS (64 or 128), tile height bm (a multiple of 32 up to
+// the KS's limit, balanced over the m-tiles) and k-split s, the modelled time is the waves of
+// blocks times a block's k-loop plus a fixed cost per block, bounded below by the HBM time of the
+// call's bytes; a split adds the parts' write and read and one launch.  A step costs the larger of
+// its MMAs at the tensor peak and a hand-off floor that grows slowly with bm (measured on GB300:
+// about 1,430 cycles per 64-k step at bm = 64 and 1,550 at bm = 160; about 2,180 per 128-k step at
+// bm = 128).  The smallest wins; ties keep the first found (64-k steps, fewer splits, shorter
+// tiles first).  Double host arithmetic only, so the choice is the same on every host.
 bool geometry(int64_t N, int64_t K, int M, int sms, nvfp4_prefill_info* g) {
   const int64_t U = K / 256;
   const int64_t n_tiles = (N + pf::kBN - 1) / pf::kBN;
   double best = 1e300;
-  int best_bm = 32, best_s = 1;
+  int best_bm = 32, best_s = 1, best_ks = 64;
   int64_t best_mt = 0;
   const double clock_hz = 2.0e9, hbm_bps = 6.5e12;
   const double t_hbm = ((double)N * (double)K * 0.5625 + 2.0 * M * (double)K + 2.0 * M * (double)N) / hbm_bps;
-  for (int bm = 32; bm <= pf::kBMMax; bm += 32) {
+  for (int ks = 64; ks <= 128; ks *= 2)
+  for (int bm = 32; bm <= pf::bm_max(ks); bm += 32) {
     const int64_t mt = (M + bm - 1) / bm;
     const int64_t bal = ((M + mt - 1) / mt + 31) / 32 * 32;  // the balanced height for mt tiles
     if (bal != bm) continue;
@@ -84,9 +87,9 @@ bool geometry(int64_t N, int64_t K, int M, int sms, nvfp4_prefill_info* g) {
       const int64_t blocks = n_tiles * mt * s;
       if (blocks > 0x7FFFFFFF) continue;  // one launch's grid
       const int64_t waves = (blocks + sms - 1) / sms;
-      const int64_t steps = 4 * ((U + s - 1) / s);
-      const double mma = 16.0 * 0.29 * bm;  // 16 MMAs of N = bm / 2 at 128 x 16 per 0.29 column-cycle
-      const double floor = 1350.0 + 1.2 * bm;
+      const int64_t steps = (256 / ks) * ((U + s - 1) / s);
+      const double mma = (ks / 64) * 16.0 * 0.29 * bm;  // MMAs of N = bm / 2, 0.29 cycles per column
+      const double floor = ks == 64 ? 1350.0 + 1.2 * bm : 1900.0 + 2.2 * bm;
       const double step = mma > floor ? mma : floor;
       double t = (double)waves * ((double)steps * step + 4000.0 + 24.0 * bm) / clock_hz;
       if (t < t_hbm) t = t_hbm;
@@ -96,11 +99,12 @@ bool geometry(int64_t N, int64_t K, int M, int sms, nvfp4_prefill_info* g) {
         best_bm = bm;
         best_s = (int)s;
         best_mt = mt;
+        best_ks = ks;
       }
     }
   }
   if (best_mt == 0) return false;
-  fill(N, M, best_bm, best_s, sms, g);
+  fill(N, M, best_ks, best_bm, best_s, sms, g);
   return true;
 }
 
@@ -137,12 +141,13 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t esize, cons
              swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool prepare_maps(nvfp4_prefill_plan* p, const uint8_t* codes, const uint8_t* scales, int M, int bm) {
-  if (p->tm_codes_ptr != codes) {
-    if (!encode_2d(&p->tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, codes, (uint64_t)p->K / 2, (uint64_t)p->N,
-                   pf::kKS / 2, pf::kBN, CU_TENSOR_MAP_SWIZZLE_NONE))
+bool prepare_maps(nvfp4_prefill_plan* p, const uint8_t* codes, const uint8_t* scales, int M, int bm, int ks) {
+  const int w = ks == 64 ? 0 : 1;
+  if (p->tm_codes_ptr[w] != codes) {
+    if (!encode_2d(&p->tm_codes[w], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, codes, (uint64_t)p->K / 2, (uint64_t)p->N,
+                   (uint32_t)(ks / 2), pf::kBN, CU_TENSOR_MAP_SWIZZLE_NONE))
       return false;
-    p->tm_codes_ptr = codes;
+    p->tm_codes_ptr[w] = codes;
   }
   if (p->tm_scales_ptr != scales) {
     if (!encode_2d(&p->tm_scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, scales, (uint64_t)p->K / 16, (uint64_t)p->N, 16,
@@ -151,7 +156,7 @@ bool prepare_maps(nvfp4_prefill_plan* p, const uint8_t* codes, const uint8_t* sc
     p->tm_scales_ptr = scales;
   }
   if (p->tm_x_M != M || p->tm_x_bm != bm) {
-    if (!encode_2d(&p->tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p->x16, (uint64_t)p->K, (uint64_t)M, pf::kKS,
+    if (!encode_2d(&p->tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p->x16, (uint64_t)p->K, (uint64_t)M, pf::kKAtom,
                    (uint32_t)bm, CU_TENSOR_MAP_SWIZZLE_128B))
       return false;
     p->tm_x_M = M;
@@ -183,8 +188,10 @@ nvfp4_status nvfp4_prefill_plan_create(int64_t N, int64_t K, int max_M, nvfp4_pr
   if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
     return NVFP4_ERR_CUDA;
-  if (cudaFuncSetAttribute(pf::prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, pf::kSmemBytes) !=
-      cudaSuccess)
+  if (cudaFuncSetAttribute(pf::prefill_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, pf::kSmemBytes) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(pf::prefill_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, pf::kSmemBytes) !=
+          cudaSuccess)
     return NVFP4_ERR_CUDA;
 
   size_t pb = 0;
@@ -239,27 +246,30 @@ void nvfp4_prefill_plan_destroy(nvfp4_prefill_plan_t plan) {
 
 nvfp4_status nvfp4_prefill_linear(nvfp4_prefill_plan_t plan, const void* x, int M, const uint8_t* w_codes,
                                   const uint8_t* w_block_scales, float w_global_scale, void* y, void* stream) {
-  return nvfp4_prefill_linear_ex(plan, x, M, w_codes, w_block_scales, w_global_scale, y, 0, 0, stream);
+  return nvfp4_prefill_linear_ex(plan, x, M, w_codes, w_block_scales, w_global_scale, y, 0, 0, 0, stream);
 }
 
 nvfp4_status nvfp4_prefill_linear_ex(nvfp4_prefill_plan_t plan, const void* x, int M, const uint8_t* w_codes,
                                      const uint8_t* w_block_scales, float w_global_scale, void* y, int bm,
-                                     int splits, void* stream) {
+                                     int splits, int k_step, void* stream) {
   if (!plan || !x || !w_codes || !w_block_scales || !y) return NVFP4_ERR_ARG;
   if (M < 1 || M > plan->max_M) return NVFP4_ERR_M_RANGE;
   if (!aligned16(x) || !aligned16(y) || !aligned16(w_codes) || !aligned16(w_block_scales)) return NVFP4_ERR_ALIGN;
   nvfp4_prefill_info g{};
   if (!geometry(plan->N, plan->K, M, plan->sm_count, &g)) return NVFP4_ERR_SHAPE;
-  if (bm != 0 || splits != 0) {
+  if (bm != 0 || splits != 0 || k_step != 0) {
     const int64_t U = plan->K / 256;
     const int b = bm != 0 ? bm : g.bm, sp = splits != 0 ? splits : g.splits;
-    if (b < 32 || b > pf::kBMMax || b % 32 != 0 || sp < 1 || sp > U || sp > 32) return NVFP4_ERR_ARG;
+    const int ks = k_step != 0 ? k_step : (b > pf::bm_max(128) ? 64 : g.k_step);
+    if (ks != 64 && ks != 128) return NVFP4_ERR_ARG;
+    if (b < 32 || b > pf::bm_max(ks) || b % 32 != 0 || sp < 1 || sp > U || sp > 32) return NVFP4_ERR_ARG;
     const int64_t blocks = (int64_t)((plan->N + pf::kBN - 1) / pf::kBN) * ((M + b - 1) / b) * sp;
     if (blocks > 0x7FFFFFFF) return NVFP4_ERR_SHAPE;
     if (sp > 1 && (size_t)sp * (size_t)M * (size_t)plan->N * 4 > plan->parts_bytes) return NVFP4_ERR_SCRATCH_LIMIT;
-    fill(plan->N, M, b, sp, plan->sm_count, &g);
+    fill(plan->N, M, ks, b, sp, plan->sm_count, &g);
   }
-  if (!prepare_maps(plan, w_codes, w_block_scales, M, g.bm)) return NVFP4_ERR_CUDA;  // before anything is enqueued
+  // before anything is enqueued
+  if (!prepare_maps(plan, w_codes, w_block_scales, M, g.bm, g.k_step)) return NVFP4_ERR_CUDA;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[1];
@@ -277,7 +287,7 @@ nvfp4_status nvfp4_prefill_linear_ex(nvfp4_prefill_plan_t plan, const void* x, i
     return NVFP4_ERR_CUDA;
 
   pf::PrefillParams p;
-  p.tm_codes = plan->tm_codes;
+  p.tm_codes = plan->tm_codes[g.k_step == 64 ? 0 : 1];
   p.tm_scales = plan->tm_scales;
   p.tm_x = plan->tm_x;
   p.xs = plan->xs;
@@ -300,7 +310,9 @@ nvfp4_status nvfp4_prefill_linear_ex(nvfp4_prefill_plan_t plan, const void* x, i
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, pf::prefill_kernel, p) != cudaSuccess) return NVFP4_ERR_CUDA;
+  const cudaError_t le = g.k_step == 64 ? cudaLaunchKernelEx(&cfg, pf::prefill_kernel<64>, p)
+                                        : cudaLaunchKernelEx(&cfg, pf::prefill_kernel<128>, p);
+  if (le != cudaSuccess) return NVFP4_ERR_CUDA;
 
   if (g.splits > 1) {
     const int64_t items = ((plan->N & 3) == 0 ? (int64_t)M * plan->N / 4 : (int64_t)M * plan->N);

@@ -6,21 +6,24 @@
 // magnitude fixes a power of two 2^e (the maximum lands in [2^15, 2^16)); the row is written as
 // fp16 times 2^e into a plain row-major [M, K] operand, and 2^-e goes to xs[m].
 //
-// prefill_kernel: one block per (256 weight rows, BM <= 192 activation rows, k-split) tile, 13 warps:
-//   warps 0-7  decoders: one weight row per thread.  Per k-step of 64 they read the row's 32 bytes
-//              of E2M1 codes and 4 E4M3 scales from shared memory, decode with the hardware
-//              converters (exact in fp16) and write the 64 fp16 weights into a tensor-memory A slot
+// prefill_kernel<KS>: one block per (256 weight rows, BM activation rows, k-split) tile, 13 warps;
+// a pipeline step covers KS = 64 k (BM <= 192) or 128 k (BM <= 128):
+//   warps 0-7  decoders: one weight row per thread.  Per k-step they read the row's KS / 2 bytes
+//              of E2M1 codes and KS / 16 E4M3 scales from shared memory, decode with the hardware
+//              converters (exact in fp16) and write the KS fp16 weights into a tensor-memory A slot
 //              (tcgen05.st, the row's own lane), so the decoded weights never pass through shared
 //              memory.  After the k-loop they are the epilogue: tensor memory -> registers, times
 //              2^-e and the per-tensor scale, rounded to bf16 (one k-split) or stored as fp32 parts;
-//   warp 8     producer (one lane): 2-D tensor copies of the codes (32 B x 256 rows per k-step)
-//              and the fp16 activations (64 k x BM rows, 128-byte swizzle) into a load ring as
-//              deep as shared memory allows for BM (6 stages at BM = 192, up to 8), and of the
+//   warp 8     producer (one lane): 2-D tensor copies of the codes (KS / 2 bytes x 256 rows per
+//              k-step) and the fp16 activations (KS / 64 boxes of 64 k x BM rows, 128-byte swizzle)
+//              into a load ring as deep as shared memory allows (at least 4 stages, up to 8), and of the
 //              scales (16 B x 256 rows per 256 k) into two stages; it also owns the tensor-memory
 //              allocation.  The decoded weights go to a separate 2-slot ring, so the copies run
-//              several k-steps ahead of the decode and the MMAs;
+//              several k-steps ahead of the decode and the MMAs.  Each step hands work from the
+//              decoders to the issuers and back at a roughly fixed cost, so the longer step
+//              halves that cost per k where the tile height allows it;
 //   warps 9-12 MMA issuers (one lane each), one per (128-row weight half, BM / 2 activation rows):
-//              per k-step four tcgen05.mma kind::f16 (M = 128, N = BM / 2, K = 16), A from tensor
+//              per k-step KS / 16 tcgen05.mma kind::f16 (M = 128, N = BM / 2, K = 16), A from tensor
 //              memory and B from shared memory, fp32 accumulation in tensor memory.
 // The weights are the MMA's A operand (M = weight rows) and the activations its B operand
 // (N = activation rows), so one decoded weight tile serves every activation row of the tile.
@@ -43,28 +46,37 @@ namespace prefill {
 
 constexpr int kBN = 256;                 // weight rows per tile (two MMA tiles of 128)
 constexpr int kMmaM = 128;
-constexpr int kBMMax = 192;              // activation rows per tile: a multiple of 32 (two MMAs of N = BM / 2)
-constexpr int kKS = 64;                  // k per pipeline step: one 128-byte line of fp16
-constexpr int kStepsPerUnit = 4;         // one scale copy covers 256 k
-constexpr int kASlots = 2;                    // decoded-weight ring (tensor memory)
-constexpr int kCBytes = kBN * kKS / 2;        // 8192: codes of a k-step, 32 bytes per row
-constexpr int kSBytes = kBN * 16;             // 4096: scales of 256 k, 16 bytes per row
+constexpr int kKAtom = 64;               // k per 128-byte swizzle atom of fp16
+constexpr int kUnitK = 256;              // one scale copy covers 256 k
+constexpr int kASlots = 2;               // decoded-weight ring (tensor memory)
+constexpr int kSBytes = kBN * 16;        // 4096: scales of 256 k, 16 bytes per row
 constexpr int kSStages = 2;
-constexpr int kLPMax = 8;                     // load ring depth (codes + activations) at most
+constexpr int kLPMax = 8;                // load ring depth (codes + activations) at most
+// A k-step is KS = 64 or 128 k (the kernel's template parameter).  Per step a decoder thread
+// turns KS / 2 bytes of codes into KS / 2 tensor-memory columns of fp16 pairs.  Tensor memory:
+// the A ring (2 slots x 2 weight halves x KS / 2 columns) takes the top 2 KS columns; half t
+// accumulates in columns [t D, t D + BM) below it, D = (512 - 2 KS) / 2, so BM <= D (192 or 128).
+constexpr uint32_t kTmemCols = 512;
+__host__ __device__ constexpr int a_col0(int ks) { return (int)kTmemCols - 2 * ks; }
+__host__ __device__ constexpr int d_stride(int ks) { return a_col0(ks) / 2; }
+__host__ __device__ constexpr int bm_max(int ks) { return d_stride(ks) / 32 * 32; }
+__host__ __device__ constexpr int c_bytes(int ks) { return kBN * ks / 2; }  // codes of a k-step
 // shared memory (offsets from the 1024-aligned base): barriers and misc in the first 1 KB, then
-// the scale stages and the load ring.  A load stage is [codes | activations]; its size (8 KB +
-// BM x 128 bytes, rounded up to 1 KB) and the ring depth lp depend on BM.
+// the scale stages and the load ring.  A load stage is [codes | activations]; its size (codes +
+// BM x 2 KS bytes, rounded up to 1 KB) and the ring depth lp depend on (KS, BM).
 constexpr int kSmemMisc = 768;                // +0 tensor-memory base, +4 abort flag
 constexpr int kSmemScales = 1024;
 constexpr int kSmemLoad = kSmemScales + kSStages * kSBytes;    // 9216
 constexpr int kSmemBytes = 232448;                             // the per-block maximum
 constexpr int kLoadBudget = kSmemBytes - 1024 - kSmemLoad;     // 1024: alignment slack
-// load stage bytes for a tile height bm, and the ring depth that fits
-__host__ __device__ constexpr int load_stage_bytes(int bm) { return (kCBytes + bm * kKS * 2 + 1023) / 1024 * 1024; }
-__host__ __device__ constexpr int load_stages(int bm) {
-  return kLoadBudget / load_stage_bytes(bm) < kLPMax ? kLoadBudget / load_stage_bytes(bm) : kLPMax;
+__host__ __device__ constexpr int load_stage_bytes(int ks, int bm) {
+  return (c_bytes(ks) + bm * ks * 2 + 1023) / 1024 * 1024;
 }
-static_assert(load_stages(kBMMax) >= 3, "ring depth at the tallest tile");
+__host__ __device__ constexpr int load_stages(int ks, int bm) {
+  return kLoadBudget / load_stage_bytes(ks, bm) < kLPMax ? kLoadBudget / load_stage_bytes(ks, bm) : kLPMax;
+}
+static_assert(load_stages(64, bm_max(64)) >= 3 && load_stages(128, bm_max(128)) >= 3, "ring depth at the tallest tile");
+static_assert(bm_max(64) == 192 && bm_max(128) == 128, "tile heights");
 // mbarriers
 constexpr int kBarCFull = 0;                        // [lp] codes copied (tx)        -> decoders
 constexpr int kBarBFull = kBarCFull + kLPMax;       // [lp] activations copied (tx)  -> issuer
@@ -83,11 +95,6 @@ constexpr int kProducerWarp = 8;
 constexpr int kIssuerWarp0 = 9;  // issuer q: weight half q / 2, activation-row half q % 2
 constexpr int kIssuers = 4;
 constexpr int kThreads = (kIssuerWarp0 + kIssuers) * 32;  // 416
-// tensor memory: half t accumulates in columns [192 t, 192 t + BM); A slot s of half t (64 k of
-// fp16 pairs) is columns 384 + 64 s + 32 t; one block per SM
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kDCol = 192;
-__device__ __forceinline__ uint32_t a_col_pf(int s, int t) { return 384u + (uint32_t)(64 * s + 32 * t); }
 constexpr int kPrepThreads = 256;
 
 // instruction descriptor: kind::f16, D = f32, A = B = f16, both K-major, N = bm, M = 128
@@ -96,7 +103,7 @@ __host__ __device__ constexpr uint32_t idesc_bm(int bm) {
 }
 
 struct PrefillParams {
-  CUtensorMap tm_codes;   // uint8 [N rows, K/2 bytes], box 32 B x 256 rows
+  CUtensorMap tm_codes;   // uint8 [N rows, K/2 bytes], box KS / 2 bytes x 256 rows
   CUtensorMap tm_scales;  // uint8 [N rows, K/16 bytes], box 16 B x 256 rows
   CUtensorMap tm_x;       // fp16 [M rows, K], box 64 x BM rows, 128-byte swizzle
   const float* xs;        // [M] 2^-e per activation row
@@ -105,7 +112,7 @@ struct PrefillParams {
   int* err;               // error word
   float gs;
   int M, bm, m_tiles, n_tiles, splits;
-  int lp;                 // load ring depth: load_stages(bm)
+  int lp;                 // load ring depth: load_stages(KS, bm)
   int64_t N, K;
 };
 
@@ -141,7 +148,16 @@ __global__ void __launch_bounds__(kPrepThreads) prefill_x_prep_kernel(const uint
 }
 
 // ------------------------------------------------------------------ main kernel
+template <int KS>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+  static_assert(KS == 64 || KS == 128, "k-step");
+  constexpr int kAtoms = KS / kKAtom;            // 128-byte swizzle atoms of activations per step
+  constexpr int kStepsPerUnit = kUnitK / KS;     // steps per scale copy
+  constexpr int kCBytes = c_bytes(KS);
+  constexpr uint32_t kDCol = (uint32_t)d_stride(KS);
+  constexpr uint32_t kA0 = (uint32_t)a_col0(KS);
+  // A slot s of weight half t: KS / 2 columns of fp16 pairs
+  auto a_col = [](int s, int t) { return kA0 + (uint32_t)((2 * s + t) * (KS / 2)); };
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + kSmemMisc);
@@ -155,10 +171,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const int mt = b % p.m_tiles, rest = b / p.m_tiles;
   const int nt = rest % p.n_tiles, sp = rest / p.n_tiles;
   const int BM = p.bm, LP = p.lp;
-  const int LS = load_stage_bytes(BM);
+  const int LS = load_stage_bytes(KS, BM);
   const int m0 = mt * BM;
   const int n0 = nt * kBN;
-  const int64_t U = p.K / (kKS * kStepsPerUnit);
+  const int64_t U = p.K / kUnitK;
   const int64_t u0 = sp * U / p.splits, u1 = (sp + 1) * U / p.splits;
   const int nsteps = (int)(u1 - u0) * kStepsPerUnit;
 
@@ -200,32 +216,37 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     bool ok = true;
     for (int j = 0; j < nsteps; ++j) {
       const int st = j % LP;
-      const int u = j >> 2, q = j & 3, ss = u & 1, as = j & 1;
+      const int u = j / kStepsPerUnit, q = j % kStepsPerUnit, ss = u & 1, as = j & 1;
       if (q == 0 && ok) ok = wait_bar(bar(kBarSFull + ss), (uint32_t)((u >> 1) & 1), ab);
       if (ok) ok = wait_bar(bar(kBarCFull + st), (uint32_t)((j / LP) & 1), ab);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
-      const uint8_t* codes = smem + kSmemLoad + st * LS + r * 32;
-      const uint4 c0 = *reinterpret_cast<const uint4*>(codes);
-      const uint4 c1 = *reinterpret_cast<const uint4*>(codes + 16);
-      const uint32_t sw = *reinterpret_cast<const uint32_t*>(smem + kSmemScales + ss * kSBytes + r * 16 + q * 4);
-      const uint32_t s0 = ptx::e4m3_pair(sw, 0), s1 = ptx::e4m3_pair(sw, 1);
-      const uint32_t s2 = ptx::e4m3_pair(sw, 2), s3 = ptx::e4m3_pair(sw, 3);
+      // the row's KS / 2 bytes of codes and KS / 16 scales, one 64-k atom (32 bytes, 4 scales) at a time
+      const uint8_t* codes = smem + kSmemLoad + st * LS + r * (KS / 2);
+      const uint8_t* scl = smem + kSmemScales + ss * kSBytes + r * 16 + q * (KS / 16);
+      uint32_t o[kAtoms][32];
+#pragma unroll
+      for (int a = 0; a < kAtoms; ++a) {
+        const uint4 c0 = *reinterpret_cast<const uint4*>(codes + 32 * a);
+        const uint4 c1 = *reinterpret_cast<const uint4*>(codes + 32 * a + 16);
+        const uint32_t sw = *reinterpret_cast<const uint32_t*>(scl + 4 * a);
+        const uint32_t s0 = ptx::e4m3_pair(sw, 0), s1 = ptx::e4m3_pair(sw, 1);
+        const uint32_t s2 = ptx::e4m3_pair(sw, 2), s3 = ptx::e4m3_pair(sw, 3);
+        ptx::e2m1x8_scaled(c0.x, s0, o[a][0], o[a][1], o[a][2], o[a][3]);
+        ptx::e2m1x8_scaled(c0.y, s0, o[a][4], o[a][5], o[a][6], o[a][7]);
+        ptx::e2m1x8_scaled(c0.z, s1, o[a][8], o[a][9], o[a][10], o[a][11]);
+        ptx::e2m1x8_scaled(c0.w, s1, o[a][12], o[a][13], o[a][14], o[a][15]);
+        ptx::e2m1x8_scaled(c1.x, s2, o[a][16], o[a][17], o[a][18], o[a][19]);
+        ptx::e2m1x8_scaled(c1.y, s2, o[a][20], o[a][21], o[a][22], o[a][23]);
+        ptx::e2m1x8_scaled(c1.z, s3, o[a][24], o[a][25], o[a][26], o[a][27]);
+        ptx::e2m1x8_scaled(c1.w, s3, o[a][28], o[a][29], o[a][30], o[a][31]);
+      }
       if (q == kStepsPerUnit - 1) {  // this unit's scales are in registers: one arrival per warp
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bar(kBarSEmpty + ss));
       }
-      uint32_t o[32];
-      ptx::e2m1x8_scaled(c0.x, s0, o[0], o[1], o[2], o[3]);
-      ptx::e2m1x8_scaled(c0.y, s0, o[4], o[5], o[6], o[7]);
-      ptx::e2m1x8_scaled(c0.z, s1, o[8], o[9], o[10], o[11]);
-      ptx::e2m1x8_scaled(c0.w, s1, o[12], o[13], o[14], o[15]);
-      ptx::e2m1x8_scaled(c1.x, s2, o[16], o[17], o[18], o[19]);
-      ptx::e2m1x8_scaled(c1.y, s2, o[20], o[21], o[22], o[23]);
-      ptx::e2m1x8_scaled(c1.z, s3, o[24], o[25], o[26], o[27]);
-      ptx::e2m1x8_scaled(c1.w, s3, o[28], o[29], o[30], o[31]);
       // the A slot must be free: the MMAs of step j - 2 have completed
       if (!__all_sync(0xffffffffu, wait_bar(bar(kBarAEmpty + as), (uint32_t)(((j >> 1) & 1) ^ 1), ab))) {
         ok = false;
@@ -233,7 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       }
       // column c of the row's A slot holds k 2c, 2c + 1 of the step
       ptx::tc_fence_after();
-      ptx::tmem_st32(t_lane + a_col_pf(as, t), o);
+#pragma unroll
+      for (int a = 0; a < kAtoms; ++a) ptx::tmem_st32(t_lane + a_col(as, t) + (uint32_t)(32 * a), o[a]);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();  // the warp's stores are complete before its one arrival
@@ -284,11 +306,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       ptx::prefetch_tensormap(&p.tm_codes);
       ptx::prefetch_tensormap(&p.tm_scales);
       ptx::prefetch_tensormap(&p.tm_x);
-      const uint32_t xbytes = (uint32_t)BM * (uint32_t)(kKS * 2);
+      const uint32_t xbytes = (uint32_t)BM * (uint32_t)(kKAtom * 2);  // one atom of the activations
       int issued = 0, units_issued = 0;
       for (int j = 0; j < nsteps; ++j) {
-        const int u = j >> 2;
-        if ((j & 3) == 0) {
+        const int u = j / kStepsPerUnit;
+        if (j % kStepsPerUnit == 0) {
           const int ss = u & 1;
           if (!wait_bar(bar(kBarSEmpty + ss), (uint32_t)(((u >> 1) & 1) ^ 1), ab)) break;
           ptx::mbar_arrive_expect_tx(bar(kBarSFull + ss), (uint32_t)kSBytes);
@@ -301,9 +323,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const int64_t g = u0 * kStepsPerUnit + j;  // global k-step
         const uint32_t stage = smem_base + (uint32_t)(kSmemLoad + st * LS);
         ptx::mbar_arrive_expect_tx(bar(kBarCFull + st), (uint32_t)kCBytes);
-        ptx::tma_load_2d(stage, &p.tm_codes, (int32_t)(g * (kKS / 2)), n0, bar(kBarCFull + st), pol_w);
-        ptx::mbar_arrive_expect_tx(bar(kBarBFull + st), xbytes);
-        ptx::tma_load_2d(stage + kCBytes, &p.tm_x, (int32_t)(g * kKS), m0, bar(kBarBFull + st), pol_x);
+        ptx::tma_load_2d(stage, &p.tm_codes, (int32_t)(g * (KS / 2)), n0, bar(kBarCFull + st), pol_w);
+        ptx::mbar_arrive_expect_tx(bar(kBarBFull + st), (uint32_t)kAtoms * xbytes);
+#pragma unroll
+        for (int a = 0; a < kAtoms; ++a)
+          ptx::tma_load_2d(stage + kCBytes + (uint32_t)a * xbytes, &p.tm_x, (int32_t)(g * KS + a * kKAtom), m0,
+                           bar(kBarBFull + st), pol_x);
         issued = j + 1;
       }
       // every copy this thread started has landed before the block can exit (normally they were
@@ -332,10 +357,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         if (!wait_bar(bar(kBarBFull + st), (uint32_t)((j / LP) & 1), ab)) break;
         ptx::tc_fence_after();
         // activation rows h BM / 2 .. of the stage: (BM / 2) / 8 groups of 1 KB further on
-        const uint32_t xb = smem_base + (uint32_t)(kSmemLoad + st * LS + kCBytes + h * nh * (kKS * 2));
+        // atom a of the step holds k 64 a .. 64 a + 63 of all BM rows; rows h BM / 2 .. start
+        // (BM / 2) / 8 groups of 1 KB into it
+        const uint32_t xb = smem_base + (uint32_t)(kSmemLoad + st * LS + kCBytes + h * nh * (kKAtom * 2));
 #pragma unroll
-        for (int kk = 0; kk < kKS / 16; ++kk)
-          ptx::mma_f16_ts(d, tmem + a_col_pf(as, t) + (uint32_t)(kk * 8), x_desc(xb + (uint32_t)(kk * 32)), id,
+        for (int kk = 0; kk < KS / 16; ++kk)
+          ptx::mma_f16_ts(d, tmem + a_col(as, t) + (uint32_t)(kk * 8),
+                          x_desc(xb + (uint32_t)((kk >> 2) * BM * (kKAtom * 2) + (kk & 3) * 32)), id,
                           (j > 0 || kk > 0) ? 1u : 0u);
         ptx::mma_commit(bar(kBarLEmpty + st));
         ptx::mma_commit(bar(kBarAEmpty + as));

@@ -177,7 +177,8 @@ def test_prefill_geometry_invariants(N, K, sms):
         g = nb.nvfp4_prefill_geometry(N, K, M, sms)
         assert g == nb.nvfp4_prefill_geometry(N, K, M, sms)
         bm, mt = g["bm"], g["m_tiles"]
-        assert bm % 32 == 0 and 32 <= bm <= 192, g
+        assert bm % 32 == 0 and 32 <= bm <= (192 if g["k_step"] == 64 else 128), g
+        assert g["k_step"] in (64, 128) and 4 <= g["load_stages"] <= 8, g
         assert mt * bm >= M and (mt - 1) * bm < M, g
         assert g["n_tiles"] == -(-N // 256)
         assert 1 <= g["splits"] <= min(U, 32)

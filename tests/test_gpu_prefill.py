@@ -3,8 +3,9 @@ through the C ABI against the CPU oracle.
 
 Same acceptance bound as the skinny path: |y - y_ref| <= 4e-3 * sum_k |w_k x_k| + one bfloat16
 ulp of |y_ref|, per element.  The shapes are chosen so that the launch geometry covers one and
-several activation tiles with a ragged last tile, tile heights from 32 to 192, weight row counts
-below one tile and with a ragged last tile, and one and several k-splits (the reduction launch).
+several activation tiles with a ragged last tile, tile heights from 32 to 192, both pipeline
+steps (64 and 128 k), weight row counts below one tile and with a ragged last tile, and one and
+several k-splits (the reduction launch).
 """
 import numpy as np
 import pytest
@@ -159,20 +160,22 @@ def test_argument_errors():
     assert info["max_M"] == 64 and info["workspace_bytes"] > 0
 
 
-@pytest.mark.parametrize("bm,splits", [(32, 1), (32, 3), (64, 8), (64, 1), (96, 5), (128, 2), (160, 4), (192, 1)])
-def test_forced_geometries_every_element(bm, splits):
-    """Every tile height band and split through the explicit-geometry entry point: each one is
-    within the tolerance on every element (N = 1024, K = 4096, M = 100)."""
+@pytest.mark.parametrize("bm,splits,k_step", [(32, 1, 64), (32, 3, 128), (64, 8, 64), (64, 1, 128), (96, 5, 64),
+                                              (96, 2, 128), (128, 2, 128), (128, 4, 64), (160, 4, 64), (192, 1, 64)])
+def test_forced_geometries_every_element(bm, splits, k_step):
+    """Every tile height band, split and pipeline step through the explicit-geometry entry point:
+    each one is within the tolerance on every element (N = 1024, K = 4096, M = 100)."""
     N, K, M = 1024, 4096, 100
     case = _forced_case()
     plan = nb.nvfp4_prefill_plan_create(N, K, M)
     y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    nb.nvfp4_prefill_linear_ex(plan, case.d_x, M, case.d_codes, case.d_scales, case.gs, y, bm=bm, splits=splits)
+    nb.nvfp4_prefill_linear_ex(plan, case.d_x, M, case.d_codes, case.d_scales, case.gs, y, bm=bm, splits=splits,
+                               k_step=k_step)
     torch.cuda.synchronize()
     assert nb.nvfp4_prefill_plan_check(plan) == nb.NVFP4_OK
     y_ref, absdot = _forced_ref()
     ok, ratio = within_tolerance(to_f64(y), y_ref, absdot)
-    assert ok, (bm, splits, "max |err|/tol = %.3g" % ratio)
+    assert ok, (bm, splits, k_step, "max |err|/tol = %.3g" % ratio)
 
 
 _FORCED = {}
@@ -196,12 +199,14 @@ def test_forced_geometry_refusals():
     case = Case(N, K, M, seed=4)
     y = torch.full((M, N), 3.0, dtype=torch.bfloat16, device="cuda")
 
-    def call(bm, splits):
+    def call(bm, splits, k_step=0):
         return nb.nvfp4_prefill_linear_ex(plan, case.d_x, M, case.d_codes, case.d_scales, 1.0, y, bm=bm,
-                                          splits=splits, check=False)
+                                          splits=splits, k_step=k_step, check=False)
 
     for bm, splits in [(16, 1), (48, 1), (208, 1), (256, 1), (-32, 1), (32, -1), (32, 3), (32, 33)]:
         assert call(bm, splits) == nb.NVFP4_ERR_ARG, (bm, splits)
+    for bm, k_step in [(160, 128), (192, 128), (64, 96), (64, 256), (64, -64)]:
+        assert call(bm, 1, k_step) == nb.NVFP4_ERR_ARG, (bm, k_step)
     # a split the plan's part buffer was not sized for
     info = nb.nvfp4_prefill_plan_get_info(plan, M)
     if info["workspace_bytes"] < 2 * M * N * 4:
