@@ -91,9 +91,10 @@ class ClockSampler:
     def __init__(self, device_index):
         self.dev = device_index
         self.proc = None
-        out_dir = os.path.join(ROOT, "gpurun_out")
-        self.path = (os.path.join(out_dir, "clocks_rank%d.csv" % device_index) if os.path.isdir(out_dir)
-                     else "/tmp/nvfp4_clocks_%d.csv" % os.getpid())
+        # the raw samples go to $NVFP4_CLOCKS_DIR when set (the summary is in the JSON line)
+        out_dir = os.environ.get("NVFP4_CLOCKS_DIR", "")
+        self.path = (os.path.join(out_dir, "clocks_rank%d.csv" % device_index) if out_dir and os.path.isdir(out_dir)
+                     else "/tmp/nvfp4_clocks_%d_%d.csv" % (device_index, os.getpid()))
 
     def start(self):
         try:
