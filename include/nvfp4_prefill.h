@@ -1,8 +1,10 @@
 /* C ABI of the NVFP4 prefill projection on sm_103a (libnvfp4skinny.so).
  *
  * y[M, N] = x[M, K] . dequant(W)[N, K]^T for activation row counts above the skinny band
- * ("10.2 NVFP4 matrix products": the engine serves 1-32 rows with the skinny kernel and prefill
- * chunks of 33 to about 1,024 rows with a second kernel over the same stored weight format).
+ * ("10 Kernels" §10.2 NVFP4 matrix products: the engine serves 1-32 rows with the skinny kernel
+ * and prefill chunks of 33 to about 1,024 rows with a second kernel over the same stored weight
+ * format; "Module ops", Functions `w4a16_gemm`: C = A . dequant(B), bf16 A and C, FP32
+ * per-tensor scale).
  * The weight format, the dequantisation (E2M1 code x E4M3 block scale x FP32 per-tensor scale,
  * "Module ops", `dequant_nvfp4_to_bf16`) and the output rounding are those of nvfp4_skinny.h;
  * any M >= 1 up to the plan's max_M is accepted.

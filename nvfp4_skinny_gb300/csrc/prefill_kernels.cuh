@@ -1,6 +1,6 @@
 // Device kernels of the NVFP4 prefill projection y = x . dequant(W)^T for activation row counts
-// above the skinny band ("10.2 NVFP4 matrix products": a second kernel over the same stored format
-// serves prefill chunks of 33 to about 1,024 rows), on sm_103a.
+// above the skinny band ("10 Kernels" §10.2 NVFP4 matrix products: a second kernel over the same
+// stored format serves prefill chunks of 33 to about 1,024 rows), on sm_103a.
 //
 // prefill_x_prep_kernel (one block per activation row): as in the skinny path, the row's largest
 // magnitude fixes a power of two 2^e (the maximum lands in [2^15, 2^16)); the row is written as
@@ -16,12 +16,12 @@
 //              2^-e and the per-tensor scale, rounded to bf16 (one k-split) or stored as fp32 parts;
 //   warp 8     producer (one lane): 2-D tensor copies of the codes (KS / 2 bytes x 256 rows per
 //              k-step) and the fp16 activations (KS / 64 boxes of 64 k x BM rows, 128-byte swizzle)
-//              into a load ring as deep as shared memory allows (at least 4 stages, up to 8), and of the
-//              scales (16 B x 256 rows per 256 k) into two stages; it also owns the tensor-memory
+//              into a load ring as deep as shared memory allows (at least 4 stages, up to 8), and
+//              of the scales (16 B x 256 rows per 256 k) into two stages; it also owns the tensor-memory
 //              allocation.  The decoded weights go to a separate 2-slot ring, so the copies run
 //              several k-steps ahead of the decode and the MMAs.  Each step hands work from the
 //              decoders to the issuers and back at a roughly fixed cost, so the longer step
-//              halves that cost per k where the tile height allows it;
+//              cuts that cost per k (by about a third, measured) where the tile height allows it;
 //   warps 9-12 MMA issuers (one lane each), one per (128-row weight half, BM / 2 activation rows):
 //              per k-step KS / 16 tcgen05.mma kind::f16 (M = 128, N = BM / 2, K = 16), A from tensor
 //              memory and B from shared memory, fp32 accumulation in tensor memory.
