@@ -289,7 +289,10 @@ def run_ours(args, rank, world):
 
 
 def run_e2e(args, proj, x_all, stream, world):
-    """Public call with host buffers: H2D of x from pinned memory, the call, D2H of y, every call."""
+    """Public call with host buffers: H2D of x from pinned memory, the call, D2H of y, around every
+    call.  The step is timed as one CUDA graph of those copies and calls (how a serving loop
+    issues it; the copies move host memory on every replay) and, for comparison, eagerly from
+    Python."""
     import torch
     from nvfp4_skinny_gb300 import binding as nb
     N, K = proj.N, proj.K
@@ -309,22 +312,35 @@ def run_e2e(args, proj, x_all, stream, world):
                     nb.nvfp4_skinny_linear(proj.plan, dx[M], M, c, sc, gs, dy[M], stream=stream)
                     hy[M].copy_(dy[M], non_blocking=True)
 
-    step()
-    torch.cuda.synchronize()
-    barrier(world)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        step()
-    b.record(stream)
-    torch.cuda.synchronize()
-    ms = max_over_ranks(a.elapsed_time(b), world)
+    def timed(run, n):
+        # everything (the graph replays included) runs on `stream`, between its two events
+        torch.cuda.synchronize()
+        barrier(world)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for _ in range(n):
+                run()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(a.elapsed_time(b), world)
+
     byts = sum(copies * call_bytes(N, K, M) for M in HEAD_MS)
     h2d = sum(copies * M * K * 2 for M in HEAD_MS)
     d2h = sum(copies * M * N * 2 for M in HEAD_MS)
-    return {"value": round(byts * steps * world / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
-            "how": "eager public calls from Python, pinned host x copied in and y copied out around every call"}
+    step()
+    ms_eager = timed(step, steps)
+    g = make_graph([step], stream)
+    with torch.cuda.stream(stream):
+        g.replay()
+    ms_graph = timed(lambda: g.replay(), steps)
+    rate = lambda ms: round(byts * steps * world / (ms * 1e-3) / 1e9, 1)
+    return {"value": rate(ms_graph), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": steps,
+            "how": "public calls with pinned host x copied in and y copied out around every call, the step "
+                   "replayed as one CUDA graph",
+            "eager": {"value": rate(ms_eager), "unit": "GB/s",
+                      "how": "the same step issued eagerly from Python, call by call"}}
 
 
 def _time_graph(g, stream, reps, warm=3):
