@@ -21,7 +21,7 @@
 //              allocation.  The decoded weights go to a separate 2-slot ring, so the copies run
 //              several k-steps ahead of the decode and the MMAs.  Each step hands work from the
 //              decoders to the issuers and back at a roughly fixed cost, so the longer step
-//              cuts that cost per k (by about a third, measured) where the tile height allows it;
+//              cuts that cost per k (by about a quarter, measured) where the tile height allows it;
 //   warps 9-12 MMA issuers (one lane each), one per (128-row weight half, BM / 2 activation rows):
 //              per k-step KS / 16 tcgen05.mma kind::f16 (M = 128, N = BM / 2, K = 16), A from tensor
 //              memory and B from shared memory, fp32 accumulation in tensor memory.
