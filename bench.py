@@ -531,10 +531,49 @@ def _oracle_sample(seconds_target, M_list=HEAD_MS):
     return byts / elapsed / 1e9, elapsed, sample, threads
 
 
+def _oracle_configs(seconds_each):
+    """The oracle on every other single-projection shape and on one layer of the decode round
+    (the round is 64 such layers): for M = 1 and 32, a bounded sample of weight rows, in the
+    metric's bytes for the covered fraction.  Timing does not depend on the values, so each
+    shape's sample rows are generated on their own (2048 rows, the shape's K)."""
+    import numpy as np
+    import torch
+    import oracle
+    from nvfp4_skinny_gb300 import synth
+    orc = oracle.default()
+    shapes = (("qkv", 7168, 5120, 2, 3), ("o", 5120, 5120, 2, 2), ("down", 5120, 17408, 2, 4),
+              ("gate_up", 34816, 5120, 2, 5), ("head", 152064, 5120, 4, 6))
+    out, layer_t, layer_b = {}, {1: 0.0, 32: 0.0}, {1: 0.0, 32: 0.0}
+    for name, N, K, ob, seed in shapes:
+        codes, scales, gs = synth.weights(2048, K, seed)
+        c, sc = codes.numpy(), scales.numpy()
+        xb = synth.activations(32, K, seed).contiguous().view(torch.int16).numpy().view(np.uint16)
+        t0 = time.perf_counter()
+        orc.linear(xb[:1], c[:16], sc[:16], gs)
+        per_row_m = max((time.perf_counter() - t0) / 16, 1e-7)
+        entry = {}
+        for M in (1, 32):
+            rows = int(max(8, min(2048, seconds_each / 2 / (per_row_m * M))))
+            t0 = time.perf_counter()
+            orc.linear(xb[:M], c[:rows], sc[:rows], gs)
+            dt = time.perf_counter() - t0
+            gbs = call_bytes(N, K, M, ob) * rows / N / dt / 1e9
+            entry[str(M)] = {"GBps": round(gbs, 6), "rows": rows, "seconds": round(dt, 3)}
+            if name != "head":  # a decode-round layer is qkv, o, gate|up and down
+                layer_t[M] += dt * N / rows
+                layer_b[M] += call_bytes(N, K, M, ob)
+        out["%s %dx%d%s" % (name, N, K, " f32-out" if ob == 4 else "")] = entry
+    out["round layer (x64 for the round)"] = {str(M): {"GBps": round(layer_b[M] / layer_t[M] / 1e9, 6),
+                                                       "round_seconds_estimate": round(64 * layer_t[M], 1)}
+                                              for M in (1, 32)}
+    return out
+
+
 def cpu_baseline(seconds_target):
     gbs, elapsed, sample, threads = _oracle_sample(seconds_target)
     return {"value": round(gbs, 6), "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample,
-            "seconds": round(elapsed, 2)}
+            "seconds": round(elapsed, 2),
+            "other_configs": _oracle_configs(max(0.5, seconds_target / 10))}
 
 
 def run_reference(args, rank, world):
