@@ -36,36 +36,50 @@
  *   nvfp4_plan_create* on the device that is current then; all later calls
  *   on the plan must run on that device.  nvfp4_skinny_linear never
  *   allocates, never synchronizes and only enqueues kernels on `stream`, so
- *   it can be captured in a CUDA graph: one kernel when every block of the
- *   work split has at most `stages` units (it then prepares its own
- *   activations), else an activation-preparation kernel and then the
- *   projection kernel (nvfp4_plan_info.launches_per_call says which).  The
- *   kernels are launched with programmatic dependent launch: the projection
- *   kernel starts reading the weights before the kernels before it on the
- *   stream have finished (x, y and the workspace are touched only after they
- *   have), so the weights must not be written by a kernel still running on
- *   `stream`.
+ *   it can be captured in a CUDA graph.  A plan runs one of two kernels,
+ *   chosen at plan creation from (N, K) and the SM count (or forced with
+ *   nvfp4_plan_create_flags); nvfp4_plan_info.kernel says which:
+ *   - NVFP4_KERNEL_TCGEN05 (the default): a warp-specialised projection
+ *     kernel (weights staged by tensor copies, decoded into tensor memory,
+ *     tcgen05.mma), preceded by an activation-preparation kernel unless every
+ *     block of its work split has at most `stages` units;
+ *   - NVFP4_KERNEL_MMA_SYNC: an activation-preparation kernel, then a
+ *     register-direct projection kernel (each warp copies its own weight rows
+ *     into a private shared-memory ring with cp.async, decodes them into
+ *     registers and multiplies them with mma.sync); no in-kernel wait of any
+ *     kind.
+ *   The kernels are launched with programmatic dependent launch: by default
+ *   the projection kernel starts reading the weights before the kernels
+ *   before it on the stream have finished (x, y and the workspace are
+ *   touched only after they have), so the weights must not be written by a
+ *   kernel still running on `stream`.  A plan created with
+ *   NVFP4_PLAN_WEIGHTS_AFTER_WAIT reads no weight byte before that point, so
+ *   a kernel that writes the weights (for example nvfp4_quantize_bf16) may
+ *   run just before the projection on the same stream.
  *   Calls that share a plan must not run concurrently (the workspace is
  *   reused); calls on one stream are ordered and safe.
  *
  * Errors
  *   Argument errors are detected on the host before anything is enqueued;
  *   the call then returns a status and launches nothing.  A launch failure
- *   returns NVFP4_ERR_CUDA.  Every wait inside the kernels is bounded: if one
- *   runs out, the kernel records NVFP4_ERR_TIMEOUT in the plan's error word,
- *   skips the remaining work and exits; nvfp4_plan_check reports it.
+ *   returns NVFP4_ERR_CUDA.  Every wait inside the tcgen05 kernel is bounded:
+ *   if one runs out, the kernel records NVFP4_ERR_TIMEOUT in the plan's error
+ *   word, skips the remaining work and exits; nvfp4_plan_check reports it.
  *
  * Numerics
  *   Each activation row is converted to fp16 after multiplying it by a power
- *   of two chosen from its largest magnitude (over all of K, or, when one
- *   launch does the call, over the k-steps of each block of the work split;
- *   which applies depends on (N, K) and the SM count only), exact for every
- *   element within 2^-32 of that maximum; weights are decoded to fp16
- *   (E2M1 x E4M3 is exact in fp16); products accumulate in fp32 on the
- *   tensor cores over a block's whole share of a row block's K; that sum is
- *   multiplied back by the inverse power of two (exact); split shares are
+ *   of two chosen from its largest magnitude (over all of K; or, for the
+ *   tcgen05 kernel when one launch does the call, over the k-steps of each
+ *   block of the work split, which depends on (N, K) and the SM count only),
+ *   exact for every element within 2^-32 of that maximum; weights are decoded
+ *   to fp16 (E2M1 x E4M3 is exact in fp16); products accumulate in fp32 on
+ *   the tensor cores over a warp's (or block's) share of a row block's K; that
+ *   sum is multiplied back by the inverse power of two (exact); shares are
  *   added in a fixed order; w_global_scale multiplies the total, which is
- *   then rounded to nearest-even bfloat16 (or returned as fp32).
+ *   then rounded to nearest-even bfloat16 (or returned as fp32).  Which kernel
+ *   runs, its work split and every order of addition depend on (N, K), the
+ *   plan's flags and the SM count only, never on M: row r of an M-row call
+ *   has the same bits as the same row computed in a 1-row call.
  */
 #ifndef NVFP4_SKINNY_H
 #define NVFP4_SKINNY_H
@@ -102,14 +116,30 @@ const char* nvfp4_status_string(nvfp4_status status);
 /* Version of this ABI (incremented on incompatible change). */
 int nvfp4_abi_version(void);
 
+/* Kernels a plan can run (nvfp4_plan_info.kernel). */
+#define NVFP4_KERNEL_TCGEN05 0
+#define NVFP4_KERNEL_MMA_SYNC 1
+
+/* Plan flags (nvfp4_plan_create_flags). */
+#define NVFP4_PLAN_DEFAULT 0u
+#define NVFP4_PLAN_KERNEL_TCGEN05 1u        /* force the tcgen05 kernel */
+#define NVFP4_PLAN_KERNEL_MMA_SYNC 2u       /* force the register-direct mma.sync kernel */
+#define NVFP4_PLAN_WEIGHTS_AFTER_WAIT 4u    /* read no weight byte before the kernels before the
+                                               call on the stream have finished */
+
 /* Create a plan for an [N, K] weight with bfloat16 output.  The launch
- * configuration (rows per block, k-step, split of K across blocks, grid) is a
+ * configuration (kernel, rows per block, k-step, split of K across blocks, grid) is a
  * function of (N, K) and the device's SM count only, never of M.
  * On success *out_plan receives the plan; on failure it is set to NULL. */
 nvfp4_status nvfp4_plan_create(int64_t N, int64_t K, nvfp4_plan_t* out_plan);
 
 /* Same, choosing the output element type (NVFP4_OUT_F32 for fp32 logits). */
 nvfp4_status nvfp4_plan_create_ex(int64_t N, int64_t K, nvfp4_out_dtype out_dtype, nvfp4_plan_t* out_plan);
+
+/* Same, with NVFP4_PLAN_* flags (0 = the default kernel choice and ordering).  At most one
+ * NVFP4_PLAN_KERNEL_* flag may be given; unknown bits are refused with NVFP4_ERR_ARG. */
+nvfp4_status nvfp4_plan_create_flags(int64_t N, int64_t K, nvfp4_out_dtype out_dtype, uint32_t flags,
+                                     nvfp4_plan_t* out_plan);
 
 /* Free a plan and its workspace (NULL is ignored).  Synchronizes the device
  * the plan was created on before freeing device memory. */
@@ -180,7 +210,8 @@ nvfp4_status nvfp4_skinny_linear_grouped(nvfp4_plan_t plan, const nvfp4_group_it
 
 /* Synchronize `stream`, then read and clear the plan's device error word.
  * Returns NVFP4_OK, NVFP4_ERR_TIMEOUT, or NVFP4_ERR_CUDA if the stream
- * reported an error. */
+ * reported an error.  (The mma.sync kernel has no in-kernel wait, so its plans
+ * only ever report NVFP4_OK or NVFP4_ERR_CUDA.) */
 nvfp4_status nvfp4_plan_check(nvfp4_plan_t plan, void* stream);
 
 /* Description of a plan's launch configuration (for tests and benchmarks). */
@@ -189,7 +220,8 @@ typedef struct {
   int32_t out_dtype;
   int32_t rows_per_block;   /* weight rows per unit of work */
   int32_t k_step;           /* k per unit of work */
-  int32_t stages;           /* shared-memory pipeline depth */
+  int32_t stages;           /* tcgen05: shared-memory pipeline depth; mma.sync: units of weights
+                               each lane holds in flight */
   int32_t threads;          /* threads per block of the main kernel */
   int32_t grid;             /* blocks of the main kernel (<= SM count) */
   int32_t sm_count;
@@ -201,6 +233,10 @@ typedef struct {
   int64_t smem_bytes;       /* dynamic shared memory of the main kernel */
   int32_t launches_per_call; /* 1: the projection kernel prepares its activations; 2: a
                                 preparation kernel runs before it */
+  int32_t kernel;            /* NVFP4_KERNEL_TCGEN05 or NVFP4_KERNEL_MMA_SYNC */
+  int32_t warps_rows;        /* mma.sync: row groups of 32 rows per block (1 for tcgen05) */
+  int32_t warps_k;           /* mma.sync: k-slices of 128 per block, added in order (1 for tcgen05) */
+  uint32_t flags;            /* the plan's NVFP4_PLAN_* flags */
   int32_t reserved;
 } nvfp4_plan_info;
 

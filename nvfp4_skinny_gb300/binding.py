@@ -28,6 +28,13 @@ NVFP4_NOALLOC_MAX_N = 4194304
 NVFP4_OUT_BF16 = 0
 NVFP4_OUT_F32 = 1
 NVFP4_MAX_M = 32
+NVFP4_ABI_VERSION = 3
+NVFP4_KERNEL_TCGEN05 = 0
+NVFP4_KERNEL_MMA_SYNC = 1
+NVFP4_PLAN_DEFAULT = 0
+NVFP4_PLAN_KERNEL_TCGEN05 = 1
+NVFP4_PLAN_KERNEL_MMA_SYNC = 2
+NVFP4_PLAN_WEIGHTS_AFTER_WAIT = 4
 
 NVFP4_PACK_OK = 0
 NVFP4_PACK_ERR_ARG = -1
@@ -35,7 +42,7 @@ NVFP4_PACK_ERR_VALUE = -2
 
 # every symbol the headers declare, per library
 CUDA_SYMBOLS = ("nvfp4_status_string", "nvfp4_abi_version", "nvfp4_plan_create", "nvfp4_plan_create_ex",
-                "nvfp4_plan_destroy", "nvfp4_skinny_linear", "nvfp4_plan_check", "nvfp4_plan_get_info",
+                "nvfp4_plan_create_flags", "nvfp4_plan_destroy", "nvfp4_skinny_linear", "nvfp4_plan_check", "nvfp4_plan_get_info",
                 "nvfp4_skinny_linear_noalloc", "nvfp4_skinny_linear_strided", "nvfp4_skinny_linear_silu_mul",
                 "nvfp4_quantize_bf16", "nvfp4_skinny_linear_grouped")
 PREFILL_SYMBOLS = ("nvfp4_prefill_geometry", "nvfp4_prefill_plan_create", "nvfp4_prefill_plan_destroy",
@@ -65,7 +72,8 @@ class PlanInfo(ctypes.Structure):
                 ("threads", ctypes.c_int32), ("grid", ctypes.c_int32), ("sm_count", ctypes.c_int32),
                 ("device", ctypes.c_int32), ("row_blocks", ctypes.c_int64), ("k_steps", ctypes.c_int64),
                 ("units", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64), ("smem_bytes", ctypes.c_int64),
-                ("launches_per_call", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("launches_per_call", ctypes.c_int32), ("kernel", ctypes.c_int32), ("warps_rows", ctypes.c_int32),
+                ("warps_k", ctypes.c_int32), ("flags", ctypes.c_uint32), ("reserved", ctypes.c_int32)]
 
 
 class PrefillInfo(ctypes.Structure):
@@ -102,6 +110,8 @@ def cuda_lib():
         lib.nvfp4_plan_create.argtypes = [i64, i64, ctypes.POINTER(p)]
         lib.nvfp4_plan_create_ex.restype = i32
         lib.nvfp4_plan_create_ex.argtypes = [i64, i64, i32, ctypes.POINTER(p)]
+        lib.nvfp4_plan_create_flags.restype = i32
+        lib.nvfp4_plan_create_flags.argtypes = [i64, i64, i32, ctypes.c_uint32, ctypes.POINTER(p)]
         lib.nvfp4_plan_destroy.restype = None
         lib.nvfp4_plan_destroy.argtypes = [p]
         lib.nvfp4_skinny_linear.restype = i32
@@ -229,6 +239,14 @@ def nvfp4_plan_create(N, K):
 def nvfp4_plan_create_ex(N, K, out_dtype=NVFP4_OUT_BF16):
     h = ctypes.c_void_p()
     _check(cuda_lib().nvfp4_plan_create_ex(int(N), int(K), int(out_dtype), ctypes.byref(h)), "nvfp4_plan_create_ex")
+    return Plan(h.value, N, K, out_dtype)
+
+
+def nvfp4_plan_create_flags(N, K, out_dtype=NVFP4_OUT_BF16, flags=NVFP4_PLAN_DEFAULT):
+    """Plan with NVFP4_PLAN_* flags (kernel choice, weights read only after the dependency wait)."""
+    h = ctypes.c_void_p()
+    _check(cuda_lib().nvfp4_plan_create_flags(int(N), int(K), int(out_dtype), int(flags), ctypes.byref(h)),
+           "nvfp4_plan_create_flags")
     return Plan(h.value, N, K, out_dtype)
 
 

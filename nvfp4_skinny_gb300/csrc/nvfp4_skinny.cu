@@ -1,6 +1,6 @@
 // C ABI of the skinny NVFP4 projection (declared and documented in include/nvfp4_skinny.h).
-// Host side: plan creation (work split from (N, K) and the SM count only), argument checks
-// before anything is enqueued, and the two launches of a call (activation preparation, then
+// Host side: plan creation (kernel and work split from (N, K) and the SM count only), argument
+// checks before anything is enqueued, and the launches of a call (activation preparation, then
 // the projection), with programmatic dependent launch so that a call's weight stream starts
 // while the kernels before it finish.
 #include <cuda.h>
@@ -12,22 +12,59 @@
 #include <mutex>
 #include <new>
 
+#include "gemv_kernels.cuh"
 #include "nvfp4_skinny.h"
 #include "skinny_kernels.cuh"
 
 namespace {
 
-constexpr int kAbiVersion = 2;
+constexpr int kAbiVersion = 3;
+constexpr uint32_t kKnownFlags = NVFP4_PLAN_KERNEL_TCGEN05 | NVFP4_PLAN_KERNEL_MMA_SYNC | NVFP4_PLAN_WEIGHTS_AFTER_WAIT;
 
 struct Workspace {
-  float* partials = nullptr; // [2 * grid][32][256]
-  int* counters = nullptr;   // [2][row_blocks]
+  float* partials = nullptr; // tcgen05: [2 * grid][32][256]; mma.sync: [2 * grid][wr] parts of 4 KB
+  int* counters = nullptr;   // tcgen05: [2][row_blocks]; mma.sync: [row_blocks][wr]
   int* err = nullptr;        // [1]
-  uint8_t* x16 = nullptr;    // fp16 activation operand: [K / 256][32 rows x 256 k x 2 bytes]
+  uint8_t* x16 = nullptr;    // fp16 activation operand (layout per kernel)
   float* xs = nullptr;       // [32] 2^-e per activation row
   void* base = nullptr;
   size_t bytes = 0;
 };
+
+// Work split of the register-direct kernel: wr row groups of 32 rows x wk k-slices of 256 per
+// block of 8 warps, two blocks per SM.  A function of (N, K, SM count) only.
+struct GemvGeometry {
+  int wr = 8, wk = 1, wk_shift = 0;
+  int depth = nvfp4::gemv::kMaxDepth;  // shared-memory stages per warp
+  int64_t row_blocks = 0, S = 0, units = 0;
+  int grid = 0;
+};
+
+// The fewest k-slices per block (wk) for which the blocks sharing a row block are, on average,
+// at most 2.5: more row groups per block keep the parts few, more k-slices keep the split-K
+// reductions short on narrow weights.
+GemvGeometry gemv_geometry(int64_t N, int64_t K, int sms) {
+  const int64_t steps = K / nvfp4::gemv::kUnitK;
+  GemvGeometry best;
+  for (int sh = 0; sh <= 3; ++sh) {
+    const int wk = 1 << sh;
+    if (steps % wk != 0) break;
+    GemvGeometry g;
+    g.wk = wk;
+    g.wk_shift = sh;
+    g.wr = nvfp4::gemv::kWarps / wk;
+    const int64_t rows = (int64_t)g.wr * nvfp4::gemv::kWarpRows;
+    g.row_blocks = (N + rows - 1) / rows;
+    g.S = steps / wk;
+    g.units = g.row_blocks * g.S;
+    const int64_t slots = (int64_t)sms * nvfp4::gemv::kBlocksPerSM;
+    g.grid = (int)(g.units < slots ? g.units : slots);
+    g.depth = wk == 1 ? nvfp4::gemv::kMaxDepth : nvfp4::gemv::kMaxDepth - 1;  // room for the k-slice parts
+    best = g;
+    if (2 * (int64_t)g.grid <= 5 * g.row_blocks) break;
+  }
+  return best;
+}
 
 }  // namespace
 
@@ -39,10 +76,13 @@ struct nvfp4_plan {
   CUtensorMap tm_codes;
   CUtensorMap tm_scales;
   nvfp4_out_dtype out = NVFP4_OUT_BF16;
+  uint32_t flags = 0;
+  int kernel = NVFP4_KERNEL_TCGEN05;
   int device = 0;
   int sm_count = 0;
   int grid = 0;
   int64_t row_blocks = 0, k_steps = 0, units = 0;
+  GemvGeometry gg;  // mma.sync kernel
   Workspace ws;
 };
 
@@ -50,17 +90,17 @@ namespace {
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
+// The driver's tensor-map encoder, looked up once (a function-local static is initialised
+// exactly once even when plans are created on several threads at the same time).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
     void* f = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    return nullptr;
+  }();
   return fn;
 }
 
@@ -108,8 +148,94 @@ cudaError_t set_smem_limits() {
   cudaError_t e = cudaFuncSetAttribute(nvfp4::skinny_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        nvfp4::kSmemBytes);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(nvfp4::skinny_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              nvfp4::kSmemBytes);
+  e = cudaFuncSetAttribute(nvfp4::skinny_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, nvfp4::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int gs = nvfp4::gemv::kSmemMaxBytes;
+  if ((e = cudaFuncSetAttribute(nvfp4::gemv::gemv_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs)) !=
+          cudaSuccess ||
+      (e = cudaFuncSetAttribute(nvfp4::gemv::gemv_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs)) !=
+          cudaSuccess ||
+      (e = cudaFuncSetAttribute(nvfp4::gemv::gemv_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs)) !=
+          cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(nvfp4::gemv::gemv_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs);
+}
+
+// Raise the kernels' shared-memory limits once per device (thread-safe).
+cudaError_t set_smem_limits_once(int dev) {
+  static std::mutex mu;
+  static bool done[64] = {false};
+  if (dev < 0 || dev >= 64) return set_smem_limits();
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev]) return cudaSuccess;
+  const cudaError_t e = set_smem_limits();
+  if (e == cudaSuccess) done[dev] = true;
+  return e;
+}
+
+// The two launches of a call on the register-direct kernel: activation preparation, then the
+// projection, ordered by programmatic dependent launch.
+template <int NT>
+cudaError_t launch_gemv_nt(const nvfp4::gemv::Params& p, const void* x, int64_t lda, int silu_mul,
+                           cudaStream_t stream) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t pcfg = {};
+  pcfg.gridDim = dim3((unsigned)(8 * NT));
+  pcfg.blockDim = dim3(nvfp4::gemv::kPrepThreads);
+  pcfg.stream = stream;
+  pcfg.attrs = attr;
+  pcfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&pcfg, nvfp4::gemv::gemv_x_prep_kernel<NT>, static_cast<const uint16_t*>(x),
+                                     lda, p.M, p.K, silu_mul, const_cast<uint4*>(p.x16), const_cast<float*>(p.xs));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.grid);
+  cfg.blockDim = dim3(nvfp4::gemv::kThreads);
+  cfg.dynamicSmemBytes = (size_t)nvfp4::gemv::smem_bytes(p.depth, NT, p.wk);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, nvfp4::gemv::gemv_kernel<NT>, p);
+}
+
+nvfp4_status launch_gemv(const GemvGeometry& gg, const void* x, int64_t lda, int M, const uint8_t* codes,
+                         const uint8_t* scales, float gs, void* y, int64_t ldc, float* partials, int* counters,
+                         uint8_t* x16, float* xs, int out_f32, int64_t N, int64_t K, int weights_after_wait,
+                         cudaStream_t stream, int silu_mul = 0) {
+  nvfp4::gemv::Params p;
+  p.codes = codes;
+  p.scales = scales;
+  p.x16 = reinterpret_cast<const uint4*>(x16);
+  p.xs = xs;
+  p.y = y;
+  p.parts = reinterpret_cast<float4*>(partials);
+  p.counters = counters;
+  p.ldc = ldc;
+  p.N = N;
+  p.K = K;
+  p.units = gg.units;
+  p.S = gg.S;
+  p.row_blocks = gg.row_blocks;
+  p.gs = gs;
+  p.M = M;
+  p.out_f32 = out_f32;
+  p.grid = gg.grid;
+  p.wr = gg.wr;
+  p.wk = gg.wk;
+  p.wk_shift = gg.wk_shift;
+  p.depth = gg.depth;
+  p.weights_after_wait = weights_after_wait;
+  const int nt = (M + 7) / 8;
+  cudaError_t e;
+  switch (nt) {
+    case 1: e = launch_gemv_nt<1>(p, x, lda, silu_mul, stream); break;
+    case 2: e = launch_gemv_nt<2>(p, x, lda, silu_mul, stream); break;
+    case 3: e = launch_gemv_nt<3>(p, x, lda, silu_mul, stream); break;
+    default: e = launch_gemv_nt<4>(p, x, lda, silu_mul, stream); break;
+  }
+  return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
 // The two launches of a call (shared by the plan and allocation-free entry points).
@@ -175,6 +301,10 @@ nvfp4_status launch_main(const CUtensorMap& tm_codes, const CUtensorMap& tm_scal
 nvfp4_status launch_call(nvfp4_plan* plan, const void* x, int64_t lda, int M, const uint8_t* codes,
                          const uint8_t* scales, float gs, void* y, int64_t ldc, cudaStream_t stream,
                          int silu_mul = 0) {
+  if (plan->kernel == NVFP4_KERNEL_MMA_SYNC)
+    return launch_gemv(plan->gg, x, lda, M, codes, scales, gs, y, ldc, plan->ws.partials, plan->ws.counters,
+                       plan->ws.x16, plan->ws.xs, plan->out == NVFP4_OUT_F32 ? 1 : 0, plan->N, plan->K,
+                       (plan->flags & NVFP4_PLAN_WEIGHTS_AFTER_WAIT) ? 1 : 0, stream, silu_mul);
   if (!prepare_tensor_maps(plan, codes, scales)) return NVFP4_ERR_CUDA;  // before anything is enqueued
   return launch_main(plan->tm_codes, plan->tm_scales, x, lda, M, gs, y, ldc, plan->ws.partials, plan->ws.counters,
                      plan->ws.err, plan->ws.x16, plan->ws.xs, plan->out == NVFP4_OUT_F32 ? 1 : 0, plan->grid,
@@ -203,10 +333,15 @@ const char* nvfp4_status_string(nvfp4_status status) {
 
 int nvfp4_abi_version(void) { return kAbiVersion; }
 
-nvfp4_status nvfp4_plan_create_ex(int64_t N, int64_t K, nvfp4_out_dtype out_dtype, nvfp4_plan_t* out_plan) {
+nvfp4_status nvfp4_plan_create_flags(int64_t N, int64_t K, nvfp4_out_dtype out_dtype, uint32_t flags,
+                                     nvfp4_plan_t* out_plan) {
   if (!out_plan) return NVFP4_ERR_ARG;
   *out_plan = nullptr;
   if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_F32) return NVFP4_ERR_ARG;
+  if ((flags & ~kKnownFlags) != 0u ||
+      (flags & (NVFP4_PLAN_KERNEL_TCGEN05 | NVFP4_PLAN_KERNEL_MMA_SYNC)) ==
+          (NVFP4_PLAN_KERNEL_TCGEN05 | NVFP4_PLAN_KERNEL_MMA_SYNC))
+    return NVFP4_ERR_ARG;
   if (N < 1 || K < nvfp4::kKStep || K % nvfp4::kKStep != 0) return NVFP4_ERR_SHAPE;
   // TMA row coordinates are 32-bit; byte offsets stay far from int64 overflow
   if (N >= (int64_t(1) << 31) || K > (int64_t(1) << 24) || N > (int64_t(1) << 40) / K) return NVFP4_ERR_SHAPE;
@@ -215,30 +350,44 @@ nvfp4_status nvfp4_plan_create_ex(int64_t N, int64_t K, nvfp4_out_dtype out_dtyp
   if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
     return NVFP4_ERR_CUDA;
-  static bool smem_attr_set[64] = {false};
-  if (dev < 64 && !smem_attr_set[dev]) {
-    if (set_smem_limits() != cudaSuccess)
-      return NVFP4_ERR_CUDA;
-    smem_attr_set[dev] = true;
-  }
+  if (set_smem_limits_once(dev) != cudaSuccess) return NVFP4_ERR_CUDA;
 
   nvfp4_plan* plan = new (std::nothrow) nvfp4_plan();
   if (!plan) return NVFP4_ERR_NOMEM;
   plan->N = N;
   plan->K = K;
   plan->out = out_dtype;
+  plan->flags = flags;
+  // The tcgen05 kernel is the default for every (N, K): over M = 1, 16, 17 and 32 it streams the
+  // weights faster than the register-direct kernel on every measured shape (the latter is ahead
+  // only for M <= 8 on the widest weights, and far behind above 16 rows, where its mma.sync
+  // operands all pass through the register file).
+  plan->kernel = (flags & NVFP4_PLAN_KERNEL_MMA_SYNC) ? NVFP4_KERNEL_MMA_SYNC : NVFP4_KERNEL_TCGEN05;
   plan->device = dev;
   plan->sm_count = sms;
-  plan->row_blocks = (N + nvfp4::kRowsPerBlock - 1) / nvfp4::kRowsPerBlock;
-  plan->k_steps = K / nvfp4::kKStep;
-  plan->units = plan->row_blocks * plan->k_steps;
-  plan->grid = (int)(plan->units < sms ? plan->units : sms);
 
-  const size_t part_bytes = round_up((size_t)2 * plan->grid * nvfp4::kNmma * nvfp4::kRowsPerBlock * 4, 256);
-  const size_t cnt_bytes = round_up((size_t)plan->row_blocks * 2 * 4, 256);
+  size_t part_bytes, cnt_bytes, x16b, cnt_count;
+  if (plan->kernel == NVFP4_KERNEL_MMA_SYNC) {
+    plan->gg = gemv_geometry(N, K, sms);
+    plan->row_blocks = plan->gg.row_blocks;
+    plan->k_steps = plan->gg.S;
+    plan->units = plan->gg.units;
+    plan->grid = plan->gg.grid;
+    part_bytes = round_up((size_t)2 * plan->grid * plan->gg.wr * nvfp4::gemv::kPartFloat4 * 16, 256);
+    cnt_count = (size_t)plan->row_blocks * plan->gg.wr;
+    x16b = (size_t)nvfp4::gemv::x16_bytes(K);
+  } else {
+    plan->row_blocks = (N + nvfp4::kRowsPerBlock - 1) / nvfp4::kRowsPerBlock;
+    plan->k_steps = K / nvfp4::kKStep;
+    plan->units = plan->row_blocks * plan->k_steps;
+    plan->grid = (int)(plan->units < sms ? plan->units : sms);
+    part_bytes = round_up((size_t)2 * plan->grid * nvfp4::kNmma * nvfp4::kRowsPerBlock * 4, 256);
+    cnt_count = (size_t)plan->row_blocks * 2;
+    x16b = x16_bytes(K);
+  }
+  cnt_bytes = round_up(cnt_count * 4, 256);
   const size_t err_bytes = 256;
   const size_t xs_bytes = 256;
-  const size_t x16b = x16_bytes(K);
   const size_t total = part_bytes + cnt_bytes + err_bytes + xs_bytes + x16b;
   void* base = nullptr;
   if (cudaMalloc(&base, total) != cudaSuccess) {
@@ -260,6 +409,10 @@ nvfp4_status nvfp4_plan_create_ex(int64_t N, int64_t K, nvfp4_out_dtype out_dtyp
   }
   *out_plan = plan;
   return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_plan_create_ex(int64_t N, int64_t K, nvfp4_out_dtype out_dtype, nvfp4_plan_t* out_plan) {
+  return nvfp4_plan_create_flags(N, K, out_dtype, NVFP4_PLAN_DEFAULT, out_plan);
 }
 
 nvfp4_status nvfp4_plan_create(int64_t N, int64_t K, nvfp4_plan_t* out_plan) {
@@ -341,7 +494,9 @@ nvfp4_status nvfp4_plan_check(nvfp4_plan_t plan, void* stream) {
   if (err != 0) {
     // an aborted call may leave split-K counters behind: clear them with the error word
     if (cudaMemsetAsync(plan->ws.err, 0, sizeof(int), s) != cudaSuccess ||
-        cudaMemsetAsync(plan->ws.counters, 0, (size_t)plan->row_blocks * 2 * sizeof(int), s) != cudaSuccess ||
+        cudaMemsetAsync(plan->ws.counters, 0,
+                        (size_t)plan->row_blocks * (plan->kernel == NVFP4_KERNEL_MMA_SYNC ? plan->gg.wr : 2) * sizeof(int),
+                        s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
       return NVFP4_ERR_CUDA;
     return NVFP4_ERR_TIMEOUT;
@@ -351,13 +506,14 @@ nvfp4_status nvfp4_plan_check(nvfp4_plan_t plan, void* stream) {
 
 nvfp4_status nvfp4_plan_get_info(nvfp4_plan_t plan, nvfp4_plan_info* info) {
   if (!plan || !info) return NVFP4_ERR_ARG;
+  const bool mma = plan->kernel == NVFP4_KERNEL_MMA_SYNC;
   info->N = plan->N;
   info->K = plan->K;
   info->out_dtype = (int32_t)plan->out;
-  info->rows_per_block = nvfp4::kRowsPerBlock;
-  info->k_step = nvfp4::kKStep;
-  info->stages = nvfp4::kStages;
-  info->threads = nvfp4::kThreads;
+  info->rows_per_block = mma ? plan->gg.wr * nvfp4::gemv::kWarpRows : nvfp4::kRowsPerBlock;
+  info->k_step = mma ? plan->gg.wk * nvfp4::gemv::kUnitK : nvfp4::kKStep;
+  info->stages = mma ? plan->gg.depth : nvfp4::kStages;
+  info->threads = mma ? nvfp4::gemv::kThreads : nvfp4::kThreads;
   info->grid = plan->grid;
   info->sm_count = plan->sm_count;
   info->device = plan->device;
@@ -365,8 +521,12 @@ nvfp4_status nvfp4_plan_get_info(nvfp4_plan_t plan, nvfp4_plan_info* info) {
   info->k_steps = plan->k_steps;
   info->units = plan->units;
   info->workspace_bytes = (int64_t)plan->ws.bytes;
-  info->smem_bytes = nvfp4::kSmemBytes;
-  info->launches_per_call = fused_mode(plan->row_blocks, plan->K, plan->grid) ? 1 : 2;
+  info->smem_bytes = mma ? nvfp4::gemv::smem_bytes(plan->gg.depth, nvfp4::gemv::kMaxNT, plan->gg.wk) : nvfp4::kSmemBytes;
+  info->launches_per_call = mma ? 2 : (fused_mode(plan->row_blocks, plan->K, plan->grid) ? 1 : 2);
+  info->kernel = plan->kernel;
+  info->warps_rows = mma ? plan->gg.wr : 1;
+  info->warps_k = mma ? plan->gg.wk : 1;
+  info->flags = plan->flags;
   info->reserved = 0;
   return NVFP4_OK;
 }
@@ -421,7 +581,7 @@ nvfp4_status noalloc_device(NoAllocDevice** out) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
       return NVFP4_ERR_CUDA;
-    if (set_smem_limits() != cudaSuccess)
+    if (set_smem_limits_once(dev) != cudaSuccess)
       return NVFP4_ERR_CUDA;
     d.scratch = static_cast<uint8_t*>(ptr);
     d.sms = sms;

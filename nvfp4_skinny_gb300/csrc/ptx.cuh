@@ -234,6 +234,14 @@ __device__ __forceinline__ int atom_acq_rel_gpu_add(int* ptr, int v) {
   return old;
 }
 
+// Compare-and-swap on a global int with acquire-release semantics at GPU scope; returns the old value.
+__device__ __forceinline__ int atom_cas_acq_rel_gpu(int* ptr, int expected, int desired) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.cas.b32 %0, [%1], %2, %3;" : "=r"(old) : "l"(ptr), "r"(expected), "r"(desired)
+               : "memory");
+  return old;
+}
+
 // fp32 -> bfloat16 bits, round to nearest even.
 __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
   uint16_t h;

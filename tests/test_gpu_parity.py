@@ -22,8 +22,16 @@ def _built():
     torch.cuda.init()
 
 
-def _plan(N, K, f32=False):
-    return nb.nvfp4_plan_create_ex(N, K, nb.NVFP4_OUT_F32 if f32 else nb.NVFP4_OUT_BF16)
+# both projection kernels: the default (tcgen05) and the register-direct mma.sync one
+KERNELS = {"tcgen05": nb.NVFP4_PLAN_KERNEL_TCGEN05, "mma": nb.NVFP4_PLAN_KERNEL_MMA_SYNC}
+kernel_param = pytest.mark.parametrize("kernel", list(KERNELS))
+
+
+def _plan(N, K, f32=False, kernel=None):
+    out = nb.NVFP4_OUT_F32 if f32 else nb.NVFP4_OUT_BF16
+    if kernel is None:
+        return nb.nvfp4_plan_create_ex(N, K, out)
+    return nb.nvfp4_plan_create_flags(N, K, out, KERNELS[kernel])
 
 
 def _full_check(case, plan, M=None):
@@ -46,17 +54,19 @@ def test_tiny_workload():
     _full_check(case, _plan(w.N, w.K))
 
 
+@kernel_param
 @pytest.mark.parametrize("N,K", [(256, 256), (300, 768), (1000, 2048), (17, 512), (513, 1280)])
 @pytest.mark.parametrize("M", [1, 5, 8, 9, 16, 17, 31, 32])
-def test_small_shapes_all_elements(N, K, M):
+def test_small_shapes_all_elements(N, K, M, kernel):
     """Several row blocks and k-steps, ragged last row block, every M band."""
     case = Case(N, K, M, seed=100 + N + K + M, outlier_frac=0.01)
-    _full_check(case, _plan(N, K))
+    _full_check(case, _plan(N, K, kernel=kernel))
 
 
-def test_f32_output_small():
+@kernel_param
+def test_f32_output_small(kernel):
     case = Case(640, 1024, 7, seed=7)
-    plan = _plan(640, 1024, f32=True)
+    plan = _plan(640, 1024, f32=True, kernel=kernel)
     y = case.run(plan)
     torch.cuda.synchronize()
     assert y.dtype == torch.float32
@@ -65,10 +75,11 @@ def test_f32_output_small():
     assert ok, ratio
 
 
-def test_split_k_fixup_path_every_element():
-    """More units than SMs with row blocks split across blocks: N=2048, K=8192 (every element)."""
-    N, K, M = 2048, 8192, 9
-    plan = _plan(N, K)
+@kernel_param
+def test_split_k_fixup_path_every_element(kernel):
+    """More units than blocks with row blocks split across blocks: N=4096, K=8192 (every element)."""
+    N, K, M = 4096, 8192, 9
+    plan = _plan(N, K, kernel=kernel)
     info = nb.nvfp4_plan_get_info(plan)
     assert info["units"] > info["grid"]
     case = Case(N, K, M, seed=21)
@@ -82,7 +93,8 @@ def _case_with_x(N, K, xf32, seed=5, gs=None):
     return Case(N, K, x.shape[0], seed, x=x, gs=gs)
 
 
-def test_zero_rows_and_mixed_magnitudes():
+@kernel_param
+def test_zero_rows_and_mixed_magnitudes(kernel):
     K = 1024
     rng = np.random.default_rng(3)
     x = np.zeros((6, K), np.float32)
@@ -93,11 +105,12 @@ def test_zero_rows_and_mixed_magnitudes():
     x[4] = rng.standard_normal(K) * 2.0 ** -120     # bf16 subnormal-range row
     x[5, ::3] = 1.0
     case = _case_with_x(384, K, x)
-    y = _full_check(case, _plan(384, K))
+    y = _full_check(case, _plan(384, K, kernel=kernel))
     assert torch.all(y[0] == 0)
 
 
-def test_extreme_scales_and_codes():
+@kernel_param
+def test_extreme_scales_and_codes(kernel):
     N, K = 256, 512
     codes = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, generator=torch.Generator().manual_seed(9))
     scales = torch.full((N, K // 16), 0x7E, dtype=torch.uint8)   # 448, the E4M3 maximum
@@ -106,7 +119,7 @@ def test_extreme_scales_and_codes():
     codes[7] = 0x88                                              # -0 codes
     x = synth.activations(4, K, 11)
     case = Case(N, K, 4, 0, x=x, codes=codes, scales=scales, gs=1.0)
-    _full_check(case, _plan(N, K))
+    _full_check(case, _plan(N, K, kernel=kernel))
 
 
 @pytest.mark.parametrize("gs", [0.0, -1.0, 1.0e-3, 7.5])
@@ -117,8 +130,8 @@ def test_global_scale_values(gs):
 
 # ------------------------------------------------------------------ row invariance (bitwise)
 
-def _row_invariance(N, K, seed, Ms=range(1, 33), f32=False):
-    plan = _plan(N, K, f32)
+def _row_invariance(N, K, seed, Ms=range(1, 33), f32=False, kernel=None):
+    plan = _plan(N, K, f32, kernel=kernel)
     x_all = synth.activations(32, K, seed, outlier_frac=0.01).cuda()
     case = Case(N, K, 32, seed, x=x_all.cpu())
     singles = []
@@ -131,24 +144,28 @@ def _row_invariance(N, K, seed, Ms=range(1, 33), f32=False):
     assert nb.nvfp4_plan_check(plan) == nb.NVFP4_OK
 
 
-def test_row_invariance_square():
-    _row_invariance(5120, 5120, seed=2)
+@kernel_param
+def test_row_invariance_square(kernel):
+    _row_invariance(5120, 5120, seed=2, kernel=kernel)
 
 
+@kernel_param
 @pytest.mark.parametrize("N,K", [(7168, 5120), (5120, 17408), (300, 768)])
-def test_row_invariance_other_shapes(N, K):
-    _row_invariance(N, K, seed=N % 97, Ms=(1, 2, 8, 9, 16, 17, 24, 32))
+def test_row_invariance_other_shapes(N, K, kernel):
+    _row_invariance(N, K, seed=N % 97, Ms=(1, 2, 8, 9, 16, 17, 24, 32), kernel=kernel)
 
 
-def test_row_invariance_head_f32():
-    _row_invariance(152064, 5120, seed=6, Ms=(1, 16, 17, 32), f32=True)
+@kernel_param
+def test_row_invariance_head_f32(kernel):
+    _row_invariance(152064, 5120, seed=6, Ms=(1, 16, 17, 32), f32=True, kernel=kernel)
 
 
 # ------------------------------------------------------------------ determinism, graphs
 
-def test_repeat_and_graph_bit_identical():
+@kernel_param
+def test_repeat_and_graph_bit_identical(kernel):
     N, K, M = 5120, 5120, 17
-    plan = _plan(N, K)
+    plan = _plan(N, K, kernel=kernel)
     case = Case(N, K, M, seed=33)
     y0 = case.run(plan)
     y1 = case.run(plan)
@@ -170,11 +187,12 @@ def test_repeat_and_graph_bit_identical():
     assert nb.nvfp4_plan_check(plan) == nb.NVFP4_OK
 
 
-def test_back_to_back_different_plans():
+@kernel_param
+def test_back_to_back_different_plans(kernel):
     """Calls of several plans queued on one stream (the decode-round pattern) give the
     same bits as the same calls made one at a time."""
     shapes = [(7168, 5120), (5120, 5120), (34816, 5120), (5120, 17408)]
-    plans = [_plan(N, K) for N, K in shapes]
+    plans = [_plan(N, K, kernel=kernel) for N, K in shapes]
     cases = [Case(N, K, 16, seed=40 + i) for i, (N, K) in enumerate(shapes)]
     alone = []
     for pl, c in zip(plans, cases):
@@ -190,11 +208,12 @@ def test_back_to_back_different_plans():
 
 # ------------------------------------------------------------------ row strides (pitched x and y)
 
+@kernel_param
 @pytest.mark.parametrize("N,K,M", [(5120, 5120, 3), (34816, 5120, 17), (300, 768, 32)])
-def test_strided_slices_match_contiguous_bitwise(N, K, M):
+def test_strided_slices_match_contiguous_bitwise(N, K, M, kernel):
     """x and y as column slices of wider row-major buffers: the same bits as the contiguous
     call for every row, and nothing outside the slices is written."""
-    plan = _plan(N, K)
+    plan = _plan(N, K, kernel=kernel)
     case = Case(N, K, M, seed=N + M)
     y_ref = case.run(plan)
     lda, ldc, x_off, y_off = K + 264, -(-N // 8) * 8 + 136, 8, 16  # row strides (lda + x_off, ldc + y_off) % 8 == 0
@@ -232,15 +251,16 @@ def _gate_up(M, K, seed):
     return (torch.randn((M, 2 * K), generator=gen) * 2).to(torch.bfloat16)
 
 
+@kernel_param
 @pytest.mark.parametrize("N,K,M", [(256, 512, 5), (640, 1024, 17), (5120, 17408, 8)])
-def test_silu_mul_input(N, K, M):
+def test_silu_mul_input(N, K, M, kernel):
     """The down projection fed by a [gate | up] row: every sampled element within the
     tolerance of the oracle applied to x = bf16(silu(gate) * up)."""
     gu = _gate_up(M, K, seed=N + M)
     x_bits = oracle.silu_mul_bf16(bf16_bits(gu), K)
     x = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16)
     case = Case(N, K, M, seed=N + K, x=x)
-    plan = _plan(N, K)
+    plan = _plan(N, K, kernel=kernel)
     y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     nb.nvfp4_skinny_linear_silu_mul(plan, gu.cuda(), 2 * K, M, case.d_codes, case.d_scales, case.gs, y, N)
     torch.cuda.synchronize()
@@ -256,9 +276,10 @@ def test_silu_mul_input(N, K, M):
     assert ok, ratio
 
 
-def test_silu_mul_row_invariance_and_refusals():
+@kernel_param
+def test_silu_mul_row_invariance_and_refusals(kernel):
     N, K = 5120, 5120
-    plan = _plan(N, K)
+    plan = _plan(N, K, kernel=kernel)
     case = Case(N, K, 1, seed=8)
     gu = _gate_up(32, K, seed=9).cuda()
     y32 = torch.empty((32, N), dtype=torch.bfloat16, device="cuda")
@@ -278,11 +299,12 @@ def test_silu_mul_row_invariance_and_refusals():
 
 # ------------------------------------------------------------------ grouped expert projections
 
-def test_grouped_experts_match_single_calls_and_oracle():
+@kernel_param
+def test_grouped_experts_match_single_calls_and_oracle(kernel):
     """Eight experts of one (N, K) with their own weights, global scales and row counts: each
     item's bits equal a single call's, and sampled elements meet the oracle's tolerance."""
     N, K = 2048, 1024
-    plan = _plan(N, K)
+    plan = _plan(N, K, kernel=kernel)
     cases = [Case(N, K, M, seed=70 + e, gs=0.01 * (e + 1)) for e, M in enumerate((1, 3, 8, 16, 17, 24, 32, 2))]
     ys = [torch.empty((c.M, N), dtype=torch.bfloat16, device="cuda") for c in cases]
     nb.nvfp4_skinny_linear_grouped(plan, [(c.d_x, c.M, c.d_codes, c.d_scales, c.gs, y) for c, y in zip(cases, ys)])
@@ -342,11 +364,12 @@ def _sampled(case, plan, M, n_samples=384, seed=0):
     assert ok, "max |err|/tol = %.3g" % ratio
 
 
+@kernel_param
 @pytest.mark.parametrize("wl", ["square", "qkv_down", "wide_head"])
-def test_full_size_workloads_sampled(wl):
+def test_full_size_workloads_sampled(wl, kernel):
     w = synth.WORKLOADS[wl]
     for pj in w.projections:
-        plan = _plan(pj.N, pj.K, pj.f32_out)
+        plan = _plan(pj.N, pj.K, pj.f32_out, kernel=kernel)
         x = synth.activations(32, pj.K, pj.seed, outlier_frac=w.outlier_frac)
         case = Case(pj.N, pj.K, 32, pj.seed, x=x)
         for M in w.Ms:
@@ -362,10 +385,11 @@ def test_full_size_workloads_sampled(wl):
         assert nb.nvfp4_plan_check(plan) == nb.NVFP4_OK
 
 
-def test_round_workload_first_layer_sampled():
+@kernel_param
+def test_round_workload_first_layer_sampled(kernel):
     """The decode-round shapes with their per-(layer, projection) seeds, layer 0."""
     for pj in synth.WORKLOADS["round"].projections[:4]:
-        plan = _plan(pj.N, pj.K)
+        plan = _plan(pj.N, pj.K, kernel=kernel)
         case = Case(pj.N, pj.K, 32, pj.seed)
         _sampled(case, plan, 32, seed=pj.seed)
 
@@ -392,10 +416,14 @@ def test_argument_errors():
     assert nb.nvfp4_plan_check(plan) == nb.NVFP4_OK
 
 
-def test_plan_info_independent_of_M():
+@kernel_param
+def test_plan_info_independent_of_M(kernel):
     for N, K in [(5120, 5120), (152064, 5120), (256, 512), (5120, 17408)]:
-        info = nb.nvfp4_plan_get_info(_plan(N, K))
+        info = nb.nvfp4_plan_get_info(_plan(N, K, kernel=kernel))
         assert info["N"] == N and info["K"] == K
+        assert info["kernel"] == (nb.NVFP4_KERNEL_TCGEN05 if kernel == "tcgen05" else nb.NVFP4_KERNEL_MMA_SYNC)
         assert info["row_blocks"] == -(-N // info["rows_per_block"])
         assert info["units"] == info["row_blocks"] * (K // info["k_step"])
-        assert info["grid"] == min(info["units"], info["sm_count"])
+        blocks_per_sm = 1 if kernel == "tcgen05" else 2  # the register-direct kernel runs two per SM
+        assert info["grid"] == min(info["units"], blocks_per_sm * info["sm_count"])
+        assert info["warps_rows"] * info["warps_k"] * 32 == (info["threads"] if kernel == "mma" else 32)
