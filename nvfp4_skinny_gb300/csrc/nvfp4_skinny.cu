@@ -242,7 +242,7 @@ nvfp4_status launch_gemv(const GemvGeometry& gg, const void* x, int64_t lda, int
 nvfp4_status launch_main(const CUtensorMap& tm_codes, const CUtensorMap& tm_scales, const void* x, int64_t lda, int M,
                          float gs, void* y, int64_t ldc, float* partials, int* counters, int* err, uint8_t* x16,
                          float* xs, int out_f32, int grid, int64_t N, int64_t K, int64_t row_blocks,
-                         cudaStream_t stream, int silu_mul = 0) {
+                         cudaStream_t stream, int silu_mul = 0, int weights_after_wait = 0) {
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -279,6 +279,7 @@ nvfp4_status launch_main(const CUtensorMap& tm_codes, const CUtensorMap& tm_scal
   p.gs = gs;
   p.M = M;
   p.out_f32 = out_f32;
+  p.weights_after_wait = weights_after_wait;
   p.grid = grid;
   p.N = N;
   p.K = K;
@@ -308,7 +309,8 @@ nvfp4_status launch_call(nvfp4_plan* plan, const void* x, int64_t lda, int M, co
   if (!prepare_tensor_maps(plan, codes, scales)) return NVFP4_ERR_CUDA;  // before anything is enqueued
   return launch_main(plan->tm_codes, plan->tm_scales, x, lda, M, gs, y, ldc, plan->ws.partials, plan->ws.counters,
                      plan->ws.err, plan->ws.x16, plan->ws.xs, plan->out == NVFP4_OUT_F32 ? 1 : 0, plan->grid,
-                     plan->N, plan->K, plan->row_blocks, stream, silu_mul);
+                     plan->N, plan->K, plan->row_blocks, stream, silu_mul,
+                     (plan->flags & NVFP4_PLAN_WEIGHTS_AFTER_WAIT) ? 1 : 0);
 }
 
 }  // namespace

@@ -144,6 +144,7 @@ struct MainParams {
   float gs;
   int M;
   int out_f32;
+  int weights_after_wait;  // 1: thread 0 waits for the kernels before this one before its first weight copy
   int grid;
   int64_t N, K;
   int64_t S;      // k-steps = K / 256
@@ -416,8 +417,11 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
     *abort_flag = 0;
     *n_red = 0;
     ptx::fence_mbar_init();
-    // The weights are read-only inputs that no kernel of this stream writes while calls are
-    // queued, so they are streamed before the dependency wait on the previous call.
+    // By default the weights are read-only inputs that no kernel of this stream writes while
+    // calls are queued, so they are streamed before the dependency wait on the previous call;
+    // with weights_after_wait the first copy waits for that call (and so for any producer of
+    // the weights before it) to finish.
+    if (p.weights_after_wait) ptx::grid_dependency_wait();
     ptx::prefetch_tensormap(&p.tm_codes);
     ptx::prefetch_tensormap(&p.tm_scales);
     for (int i = 0; i < kStages && i < n_local; ++i) issue_weights(i);

@@ -7,6 +7,7 @@ import torch
 import oracle
 from gpu_cases import bf16_bits
 from nvfp4_skinny_gb300 import binding as nb
+from nvfp4_skinny_gb300 import synth
 
 pytestmark = pytest.mark.gpu
 
@@ -93,3 +94,58 @@ def test_quantizer_refusals():
     assert q(64, 64, float("nan")) == nb.NVFP4_ERR_ARG
     assert q(64, 68, 1.0) == nb.NVFP4_ERR_ALIGN       # ldw not a multiple of 8
     assert q(64, 64, 1.0) == nb.NVFP4_OK
+
+
+@pytest.mark.parametrize("kernel", [nb.NVFP4_PLAN_KERNEL_TCGEN05, nb.NVFP4_PLAN_KERNEL_MMA_SYNC])
+def test_weights_written_on_the_stream_then_projected(kernel):
+    """Weights produced on the same stream, with no host synchronisation before the projection,
+    by plans created with NVFP4_PLAN_WEIGHTS_AFTER_WAIT:
+    - by the library's quantizer (device BF16 -> NVFP4);
+    - by a kernel that lets its dependents launch early: one of the library's own projections,
+      whose bf16 output bytes are then used as the next projection's codes.
+    Each projection must read the weights as written, which the oracle on the final bytes
+    checks."""
+    from gpu_cases import Case, to_f64, within_tolerance
+    flags = kernel | nb.NVFP4_PLAN_WEIGHTS_AFTER_WAIT
+    s = torch.cuda.Stream()
+    # 1) quantize -> project
+    rows, K, M = 768, 1024, 4
+    w = _weights(rows, K, seed=15).cuda()
+    codes = torch.empty((rows, K // 2), dtype=torch.uint8, device="cuda")
+    scales = torch.empty((rows, K // 16), dtype=torch.uint8, device="cuda")
+    x = synth.activations(M, K, 16).cuda()
+    y = torch.empty((M, rows), dtype=torch.bfloat16, device="cuda")
+    plan = nb.nvfp4_plan_create_flags(rows, K, nb.NVFP4_OUT_BF16, flags)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        nb.nvfp4_quantize_bf16(w, rows, K, K, 0.5, codes, scales, stream=s)
+        nb.nvfp4_skinny_linear(plan, x, M, codes, scales, 0.5, y, stream=s)
+    s.synchronize()
+    case = Case(rows, K, M, seed=16, x=x.cpu(), codes=codes.cpu(), scales=scales.cpu(), gs=0.5)
+    y_ref, absdot = case.oracle_full()
+    ok, ratio = within_tolerance(to_f64(y), y_ref, absdot)
+    assert ok, ratio
+    assert nb.nvfp4_plan_check(plan, s) == nb.NVFP4_OK
+    # 2) projection A writes y_a; projection B reads y_a's bytes as its codes
+    Na, Ka, Ma = 1024, 512, 16   # y_a: 16 x 1024 bf16 = 32 KB = codes of a [64, 1024] weight
+    Nb, Kb, Mb = 64, 1024, 3
+    ca, sa, gsa = synth.weights(Na, Ka, 17, device="cuda")
+    xa = synth.activations(Ma, Ka, 18, device="cuda")
+    y_a = torch.empty((Ma, Na), dtype=torch.bfloat16, device="cuda")
+    sb = torch.full((Nb, Kb // 16), 0x30, dtype=torch.uint8, device="cuda")  # E4M3 0.5
+    xb = synth.activations(Mb, Kb, 19, device="cuda")
+    y_b = torch.empty((Mb, Nb), dtype=torch.bfloat16, device="cuda")
+    plan_a = nb.nvfp4_plan_create_flags(Na, Ka, nb.NVFP4_OUT_BF16, kernel)
+    plan_b = nb.nvfp4_plan_create_flags(Nb, Kb, nb.NVFP4_OUT_BF16, flags)
+    y_a.zero_()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        nb.nvfp4_skinny_linear(plan_a, xa, Ma, ca, sa, gsa, y_a, stream=s)
+        nb.nvfp4_skinny_linear(plan_b, xb, Mb, y_a.view(torch.uint8).view(Nb, Kb // 2), sb, 1.0, y_b, stream=s)
+    s.synchronize()
+    cb = y_a.view(torch.uint8).view(Nb, Kb // 2).cpu()
+    assert bool((cb != 0).any())
+    case = Case(Nb, Kb, Mb, seed=20, x=xb.cpu(), codes=cb, scales=sb.cpu(), gs=1.0)
+    y_ref, absdot = case.oracle_full()
+    ok, ratio = within_tolerance(to_f64(y_b), y_ref, absdot)
+    assert ok, ratio

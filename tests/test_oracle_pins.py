@@ -113,3 +113,123 @@ def test_quantizer_special_blocks():
     deq = np.array([oracle.e2m1(int((codes[2, 8 + i // 2] >> (4 * (i % 2))) & 0xF)) for i in range(16)]) * sv
     xb = (_to_bf16_bits(x[2, 16:]).astype(np.uint32) << 16).view(np.float32)
     assert np.all(np.abs(deq - xb) <= sv * 1.0 + 1e-12)
+
+
+# ------------------------------------------------------------------ quantizer: E4M3 scale rounding
+
+def _e4m3_table():
+    """(values, bytes) of the finite non-negative E4M3 bytes, from the OCP definition written out
+    with exact rationals (independent of the oracle's decoders)."""
+    from fractions import Fraction
+    out = []
+    for b in range(0x7F):
+        e, m = b >> 3, b & 7
+        v = Fraction(m, 8) * Fraction(2) ** -6 if e == 0 else (1 + Fraction(m, 8)) * Fraction(2) ** (e - 7)
+        out.append((v, b))
+    return out
+
+
+def _rational_nearest_even(table, s):
+    """Byte of the E4M3 value nearest to the rational s (s >= 0), ties to the even byte, saturating
+    at 448."""
+    from fractions import Fraction
+    if s >= table[-1][0]:
+        return table[-1][1]
+    best = None
+    for v, b in table:
+        d = abs(v - s)
+        if best is None or d < best[0] or (d == best[0] and b % 2 == 0):
+            best = (d, b)
+    return best[1]
+
+
+def _scale_cases():
+    """Block maxima (bf16) whose amax / 6 lands exactly on every midpoint between adjacent E4M3
+    values that bf16 can reach, on both sides of it by one bf16 step of amax, and past 448."""
+    from fractions import Fraction
+    table = _e4m3_table()
+    amaxes = set()
+    for (a, _), (b, _) in zip(table, table[1:]):
+        mid = (a + b) / 2
+        am = 6 * mid
+        bits = int(np.float32(float(am)).view(np.uint32)) >> 16
+        for db in (-1, 0, 1):
+            v = np.array([(bits + db) << 16], np.uint32).view(np.float32)[0]
+            if v > 0:
+                amaxes.add(float(v))
+    amaxes.update([448.0 * 6, 460.0 * 6, 1.0e4, 6.0 * 2.0 ** -10])
+    return sorted(amaxes)
+
+
+def _check_scale_rounding(quantize):
+    """quantize(w_bits, gs) -> (codes, scales); every block's scale must be the rational
+    nearest-even E4M3 value of the fp32 quotient (amax / 6) / gs, saturating at 448."""
+    from fractions import Fraction
+    table = _e4m3_table()
+    amaxes = _scale_cases()
+    w = np.zeros((len(amaxes), 16), np.float32)
+    w[:, 3] = amaxes                       # the block maximum
+    w[:, 7] = -np.float32(0.25) * w[:, 3]  # smaller elements do not change the scale
+    _, scales = quantize(_to_bf16_bits(w), 1.0)
+    for i, am in enumerate(amaxes):
+        s32 = np.float32(np.float32(am) / np.float32(6.0)) / np.float32(1.0)
+        want = _rational_nearest_even(table, Fraction(float(s32)))
+        assert int(scales[i, 0]) == want, (am, float(s32), int(scales[i, 0]), want)
+
+
+def test_quantizer_scale_rounding_exact_rationals():
+    """The oracle's E4M3 scale choice against exact rationals: midpoints between adjacent E4M3
+    values (ties to the even byte), one bf16 step to either side, and saturation at 448."""
+    _check_scale_rounding(oracle.quantize_nvfp4)
+
+
+@pytest.mark.parametrize("mutant", ["ceil", "floor", "ties_away", "ties_odd"])
+def test_quantizer_scale_rounding_mutants_are_caught(mutant, monkeypatch):
+    """Plausible rounding mistakes planted in the oracle's nearest-value search must fail the
+    exact-rational pin above."""
+    real = oracle._nearest_even
+
+    def planted(values_sorted, codes_sorted, v):
+        v = np.asarray(v, np.float64)
+        hi = np.clip(np.searchsorted(values_sorted, v, side="left"), 0, len(values_sorted) - 1)
+        lo = np.clip(hi - 1, 0, len(values_sorted) - 1)
+        exact = values_sorted[hi] == v
+        dl, dh = np.abs(v - values_sorted[lo]), np.abs(values_sorted[hi] - v)
+        if mutant == "ceil":
+            pick_hi = np.ones_like(exact)
+        elif mutant == "floor":
+            pick_hi = exact
+        elif mutant == "ties_away":
+            pick_hi = dh <= dl
+        else:  # ties to the odd code
+            pick_hi = (dh < dl) | ((dh == dl) & (codes_sorted[hi] % 2 == 1))
+        return np.where(pick_hi, codes_sorted[hi], codes_sorted[lo])
+
+    # only the E4M3 search (the 127-entry table) is planted; the E2M1 one stays the real one
+    def routed(values_sorted, codes_sorted, v):
+        return planted(values_sorted, codes_sorted, v) if len(values_sorted) > 8 else real(values_sorted, codes_sorted, v)
+
+    monkeypatch.setattr(oracle, "_nearest_even", routed)
+    with pytest.raises(AssertionError):
+        _check_scale_rounding(oracle.quantize_nvfp4)
+
+
+# ------------------------------------------------------------------ gated-MLP input: one bf16 ulp
+
+def test_silu_mul_within_one_bf16_ulp_of_fp64():
+    """x = bf16(silu(g) * u) against silu(g) * u computed in binary64 from the closed form
+    g / (1 + e^-g): the oracle's fp32 steps may move the bf16 result by at most one ulp, and
+    only next to a rounding boundary."""
+    import math
+    rng = np.random.default_rng(11)
+    g = (rng.standard_normal((8, 256)) * 4).astype(np.float32)
+    u = (rng.standard_normal((8, 256)) * 2).astype(np.float32)
+    g = ((g.view(np.uint32) >> 16) << 16).view(np.float32)
+    u = ((u.view(np.uint32) >> 16) << 16).view(np.float32)
+    got = oracle.silu_mul_bf16(np.concatenate([_bits(g), _bits(u)], axis=1), g.shape[1])
+    gv = (got.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    ref = np.vectorize(lambda a, b: a / (1.0 + math.exp(-a)) * b)(g.astype(np.float64), u.astype(np.float64))
+    ulp = np.array([2.0 ** (math.frexp(abs(r))[1] - 8) if r != 0 else 2.0 ** -133 for r in ref.ravel()]).reshape(ref.shape)
+    err = np.abs(gv - ref)
+    assert np.all(err <= 1.0 * ulp), float(np.max(err / ulp))
+    assert np.mean(err <= 0.5 * ulp) > 0.97   # almost every element is the correctly rounded one
