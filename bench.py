@@ -16,7 +16,9 @@ Under torchrun (N > 1) every rank runs its own replica of the workload (weak
 scaling); the time is the max over ranks and `value` sums all ranks' bytes.
 
 `other_workloads` adds the other projection shapes, the 64-layer decode round and the prefill
-projection (M = 64 / 256 / 1024, TFLOP/s against the dense bf16 tensor peak).
+projection (M = 64 / 256 / 1024, TFLOP/s against the dense bf16 tensor peak); `kernel_ab` times
+the register-direct mma.sync kernel on the same large shapes and on the round (the plans' default
+is the tcgen05 kernel).
 """
 import argparse
 import hashlib
@@ -37,7 +39,9 @@ L2_BYTES = 129 * 1000 * 1000
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ("nvfp4_skinny_gb300/csrc/nvfp4_skinny.cu", "nvfp4_skinny_gb300/csrc/skinny_kernels.cuh",
                   "nvfp4_skinny_gb300/csrc/ptx.cuh")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "skinny_kernel_square5120_m16.md")
+# DRAM bytes per launch measured with ncu, one JSON object per line (written from a capture's
+# dram__bytes_read.sum + dram__bytes_write.sum, keyed by the kernel sources' hash)
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_records.txt")
 
 
 def call_bytes(N, K, M, out_bytes=2):
@@ -62,21 +66,19 @@ def hbm_peak():
 
 
 def recorded_traffic(N, K, M):
-    """DRAM bytes per launch of the main kernel from the committed ncu summary (its
-    `traffic-record:` line), if it was taken on the current kernel sources for this shape
-    and M; else None."""
+    """DRAM bytes per launch of the projection kernel from the traffic records, if one was taken
+    on the current kernel sources for this shape and M; else None."""
     try:
         with open(TRAFFIC_FILE) as f:
-            lines = [ln for ln in f if ln.startswith("traffic-record:")]
+            recs = [json.loads(ln) for ln in f if ln.strip().startswith("{")]
     except Exception:
         return None
-    for ln in lines:
-        rec = dict(kv.split("=", 1) for kv in ln.split()[1:] if "=" in kv)
+    for rec in recs:
         try:
             if (rec.get("kernel_source_hash") == kernel_source_hash() and int(rec["N"]) == N
                     and int(rec["K"]) == K and int(rec["M"]) == M):
                 return int(rec["dram_bytes_per_launch"])
-        except (KeyError, ValueError):
+        except (KeyError, ValueError, TypeError):
             continue
     return None
 
@@ -142,12 +144,12 @@ class ClockSampler:
 class Projection:
     """R rotating weight copies of one [N, K] shape, resident on the device, plus a plan."""
 
-    def __init__(self, N, K, seed, copies, f32_out=False):
+    def __init__(self, N, K, seed, copies, f32_out=False, flags=0):
         import torch
         from nvfp4_skinny_gb300 import binding as nb
         from nvfp4_skinny_gb300 import synth
         self.N, self.K, self.f32_out = N, K, f32_out
-        self.plan = nb.nvfp4_plan_create_ex(N, K, nb.NVFP4_OUT_F32 if f32_out else nb.NVFP4_OUT_BF16)
+        self.plan = nb.nvfp4_plan_create_flags(N, K, nb.NVFP4_OUT_F32 if f32_out else nb.NVFP4_OUT_BF16, flags)
         self.w = [synth.weights(N, K, seed + 7919 * i, device="cuda") for i in range(copies)]
         self.out_dtype = torch.float32 if f32_out else torch.bfloat16
         self.out_bytes = 4 if f32_out else 2
@@ -253,8 +255,9 @@ def run_ours(args, rank, world):
     traffic = recorded_traffic(sq.N, sq.K, 16)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
-                "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one M=16 launch "
-                                  "(profiles/skinny_kernel_square5120_m16.md); null once the kernel sources change",
+                "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one M=16 launch of the "
+                                  "projection kernel (the traffic records under profiles/); null once the kernel "
+                                  "sources change",
                 "algorithmic_bytes_per_launch": int(avg_bytes), "peak_source": peak_src,
                 "timing": "CUDA events on the launching stream over the timed region; a call is the "
                           "plan's launches (one skinny_kernel for this shape; back-to-back calls overlap "
@@ -265,6 +268,12 @@ def run_ours(args, rank, world):
 
     # ---------------- other workloads (reported alongside, not the headline)
     others = {} if args.quick else run_other_workloads(stream, rank, peak)
+    # ---------------- the register-direct mma.sync kernel on the same shapes (A/B)
+    ab = {} if args.quick else {
+        "kernel": "register-direct mma.sync (NVFP4_PLAN_KERNEL_MMA_SYNC); the default plans run tcgen05",
+        "square 5120x5120": run_square_ab(stream, rank, peak),
+        **run_other_workloads(stream, rank, peak, flags=nb.NVFP4_PLAN_KERNEL_MMA_SYNC, Ms=HEAD_MS,
+                              with_prefill=False)}
 
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -282,6 +291,7 @@ def run_ours(args, rank, world):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "other_workloads": others,
+        "kernel_ab": ab,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
@@ -343,6 +353,31 @@ def run_e2e(args, proj, x_all, stream, world):
                       "how": "the same step issued eagerly from Python, call by call"}}
 
 
+def run_square_ab(stream, rank, peak):
+    """The headline square projection on register-direct plans, each M as in other_workloads."""
+    import torch
+    from nvfp4_skinny_gb300 import binding as nb
+    from nvfp4_skinny_gb300 import synth
+    sq = synth.WORKLOADS["square"].projections[0]
+    copies = max(2, -(-3 * L2_BYTES // call_bytes(sq.N, sq.K, 1)))
+    proj = Projection(sq.N, sq.K, sq.seed + 1000 * rank, copies, False, nb.NVFP4_PLAN_KERNEL_MMA_SYNC)
+    x_all = synth.activations(32, sq.K, sq.seed, device="cuda")
+    entry = {}
+    for M in HEAD_MS:
+        xm = x_all[:M].contiguous()
+        y = torch.empty((M, sq.N), dtype=torch.bfloat16, device="cuda")
+        calls = [(lambda c=c, sc=sc, gs=gs: nb.nvfp4_skinny_linear(proj.plan, xm, M, c, sc, gs, y, stream=stream))
+                 for (c, sc, gs) in proj.w]
+        t_call = _time_graph(make_graph(calls, stream), stream, 10) / copies
+        gbs = call_bytes(sq.N, sq.K, M) / (t_call * 1e-3) / 1e9
+        entry[str(M)] = {"us_per_call": round(t_call * 1e3, 3), "GBps": round(gbs, 1),
+                         "frac_of_peak": round(gbs / peak, 4)}
+    assert nb.nvfp4_plan_check(proj.plan, stream) == nb.NVFP4_OK
+    del proj
+    torch.cuda.empty_cache()
+    return entry
+
+
 def _time_graph(g, stream, reps, warm=3):
     import torch
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -357,8 +392,9 @@ def _time_graph(g, stream, reps, warm=3):
     return a.elapsed_time(b) / reps
 
 
-def run_other_workloads(stream, rank, peak):
-    """QKV / down, wide gate|up / head (fp32 out), and the full 64-layer decode round."""
+def run_other_workloads(stream, rank, peak, flags=0, Ms=None, with_prefill=True):
+    """QKV / down, wide gate|up / head (fp32 out), and the full 64-layer decode round (on plans
+    made with `flags`; each shape at its workload's Ms, or at `Ms`)."""
     import torch
     from nvfp4_skinny_gb300 import binding as nb
     from nvfp4_skinny_gb300 import synth
@@ -368,10 +404,10 @@ def run_other_workloads(stream, rank, peak):
         for pj in w.projections:
             per_copy = call_bytes(pj.N, pj.K, 1, 4 if pj.f32_out else 2)
             copies = max(2, -(-3 * L2_BYTES // per_copy))
-            proj = Projection(pj.N, pj.K, pj.seed + 1000 * rank, copies, pj.f32_out)
+            proj = Projection(pj.N, pj.K, pj.seed + 1000 * rank, copies, pj.f32_out, flags)
             x_all = synth.activations(32, pj.K, pj.seed, device="cuda", outlier_frac=w.outlier_frac)
             entry = {}
-            for M in w.Ms:
+            for M in (Ms or w.Ms):
                 xm = x_all[:M].contiguous()
                 y = torch.empty((M, pj.N), dtype=proj.out_dtype, device="cuda")
                 calls = [(lambda c=c, sc=sc, gs=gs: nb.nvfp4_skinny_linear(proj.plan, xm, M, c, sc, gs, y,
@@ -387,8 +423,9 @@ def run_other_workloads(stream, rank, peak):
             assert nb.nvfp4_plan_check(proj.plan, stream) == nb.NVFP4_OK
             del proj
             torch.cuda.empty_cache()
-    res["round"] = run_round(stream, rank, peak)
-    res["prefill"] = run_prefill(stream, rank)
+    res["round"] = run_round(stream, rank, peak, flags)
+    if with_prefill:
+        res["prefill"] = run_prefill(stream, rank)
     return res
 
 
@@ -440,8 +477,8 @@ def run_prefill(stream, rank):
     return out
 
 
-def run_round(stream, rank, peak):
-    """64 layers x {qkv, o, gate|up, down}: 256 launches back to back, eager and as one CUDA graph."""
+def run_round(stream, rank, peak, flags=0):
+    """64 layers x {qkv, o, gate|up, down}: 256 calls back to back, eager and as one CUDA graph."""
     import torch
     from nvfp4_skinny_gb300 import binding as nb
     from nvfp4_skinny_gb300 import synth
@@ -451,7 +488,7 @@ def run_round(stream, rank, peak):
     for pj in w.projections:
         key = (pj.N, pj.K)
         if key not in plans:
-            plans[key] = nb.nvfp4_plan_create(pj.N, pj.K)
+            plans[key] = nb.nvfp4_plan_create_flags(pj.N, pj.K, nb.NVFP4_OUT_BF16, flags)
         weights.append((pj, synth.weights(pj.N, pj.K, pj.seed + 100000 * rank, device="cuda")))
     total_w = sum(pj.N * pj.K // 2 + pj.N * pj.K // 16 for pj, _ in weights)
     out = {"launches": len(weights), "weight_bytes": total_w}
@@ -613,7 +650,7 @@ def profile_shape(args):
     N, K, M = int(parts[0]), int(parts[1]), int(parts[2])
     f32 = len(parts) > 3 and parts[3] == "f32"
     copies = max(2, -(-2 * L2_BYTES // call_bytes(N, K, 1)))
-    proj = Projection(N, K, 77, copies, f32)
+    proj = Projection(N, K, 77, copies, f32, nb.NVFP4_PLAN_KERNEL_MMA_SYNC if args.mma else 0)
     x = synth.activations(M, K, 77, device="cuda")
     y = torch.empty((M, N), dtype=proj.out_dtype, device="cuda")
     torch.cuda.synchronize()
@@ -624,7 +661,8 @@ def profile_shape(args):
     st = nb.nvfp4_plan_check(proj.plan)
     if st != nb.NVFP4_OK:
         raise RuntimeError(nb.nvfp4_status_string(st))
-    print("profiled shape N=%d K=%d M=%d copies=%d calls=%d" % (N, K, M, copies, args.warmup + args.steps))
+    print("profiled shape N=%d K=%d M=%d copies=%d calls=%d kernel=%s" % (
+        N, K, M, copies, args.warmup + args.steps, "mma" if args.mma else "tcgen05"))
 
 
 def profile_prefill(args):
@@ -696,6 +734,7 @@ def main(argv=None):
     ap.add_argument("--quick", action="store_true", help="skip the other workloads")
     ap.add_argument("--profile-shape", default=None, metavar="N,K,M[,f32]",
                     help="profiling driver: run --warmup then --steps calls of one shape on cold weights, no JSON")
+    ap.add_argument("--mma", action="store_true", help="--profile-shape on register-direct mma.sync plans")
     ap.add_argument("--profile-prefill", default=None, metavar="N,K,M",
                     help="run a few prefill calls of one shape (for ncu) and exit")
     args = ap.parse_args(argv)

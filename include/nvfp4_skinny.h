@@ -258,15 +258,19 @@ nvfp4_status nvfp4_plan_get_info(nvfp4_plan_t plan, nvfp4_plan_info* info);
  * N <= NVFP4_NOALLOC_MAX_N; larger problems are refused with NVFP4_ERR_SCRATCH_LIMIT before
  * anything is enqueued.  It calls no cudaMalloc, cudaFree or other allocating routine.
  *
- * The first call on a device does a one-time set-up for that device (it looks up the device
- * address of the scratch array and the SM count, and raises the kernel's shared-memory limit);
- * make that first call before any stream capture on the device.  Every call on a device uses
- * the same scratch, which keeps the previous call's contents; each call clears the parts that
- * must start at zero (split-K counters and the error word) on `stream` before its kernels run.
- * Calls that can overlap on the GPU (different streams without ordering between them) race on
- * that scratch and give wrong results: order them.  In-kernel timeouts are not reported by this
- * entry point.  Arguments, layouts and the other status codes are those of nvfp4_skinny_linear;
- * N and K are the weight's shape and out_dtype the element type of y.
+ * The first call on a device does a one-time set-up for that device (it reads the SM count and
+ * raises the kernel's shared-memory limit); make that first call before any stream capture on
+ * the device.  Every call looks up the device address of the scratch array (a host-side query,
+ * no allocation).  The set-up does not survive cudaDeviceReset: after a reset, reload the
+ * library (the plan-based path is in the same position, since plans do not survive it either).
+ * Every call on a device uses the same scratch, which keeps the previous call's contents; each
+ * call clears the parts that must start at zero (its split-K counters) on `stream` before its
+ * kernels run.  Calls that can overlap on the GPU (different streams without ordering between
+ * them) race on that scratch and give wrong results: order them.  A bounded in-kernel wait that
+ * runs out is recorded in the scratch's error word, which accumulates over calls until
+ * nvfp4_noalloc_check reads and clears it.  Arguments, layouts and the other status codes are
+ * those of nvfp4_skinny_linear; N and K are the weight's shape and out_dtype the element type of
+ * y.  These calls always run the tcgen05 kernel.
  * ------------------------------------------------------------------------------------------- */
 #define NVFP4_NOALLOC_MAX_K 32768
 #define NVFP4_NOALLOC_MAX_N 4194304
@@ -275,6 +279,11 @@ nvfp4_status nvfp4_plan_get_info(nvfp4_plan_t plan, nvfp4_plan_info* info);
 nvfp4_status nvfp4_skinny_linear_noalloc(int64_t N, int64_t K, nvfp4_out_dtype out_dtype, const void* x, int M,
                                          const uint8_t* w_codes, const uint8_t* w_block_scales, float w_global_scale,
                                          void* y, void* stream);
+
+/* Synchronize `stream`, then read and clear the allocation-free scratch's error word on the
+ * current device: NVFP4_OK, NVFP4_ERR_TIMEOUT (some call since the last check gave up on a
+ * bounded wait) or NVFP4_ERR_CUDA.  No counterpart in the pages; it allocates nothing. */
+nvfp4_status nvfp4_noalloc_check(void* stream);
 
 #ifdef __cplusplus
 }

@@ -43,7 +43,7 @@ NVFP4_PACK_ERR_VALUE = -2
 # every symbol the headers declare, per library
 CUDA_SYMBOLS = ("nvfp4_status_string", "nvfp4_abi_version", "nvfp4_plan_create", "nvfp4_plan_create_ex",
                 "nvfp4_plan_create_flags", "nvfp4_plan_destroy", "nvfp4_skinny_linear", "nvfp4_plan_check", "nvfp4_plan_get_info",
-                "nvfp4_skinny_linear_noalloc", "nvfp4_skinny_linear_strided", "nvfp4_skinny_linear_silu_mul",
+                "nvfp4_skinny_linear_noalloc", "nvfp4_noalloc_check", "nvfp4_skinny_linear_strided", "nvfp4_skinny_linear_silu_mul",
                 "nvfp4_quantize_bf16", "nvfp4_skinny_linear_grouped")
 PREFILL_SYMBOLS = ("nvfp4_prefill_geometry", "nvfp4_prefill_plan_create", "nvfp4_prefill_plan_destroy",
                    "nvfp4_prefill_linear", "nvfp4_prefill_linear_ex", "nvfp4_prefill_plan_check",
@@ -130,6 +130,8 @@ def cuda_lib():
         lib.nvfp4_quantize_bf16.argtypes = [p, i64, i64, i64, ctypes.c_float, p, p, p]
         lib.nvfp4_skinny_linear_noalloc.restype = i32
         lib.nvfp4_skinny_linear_noalloc.argtypes = [i64, i64, i32, p, i32, p, p, ctypes.c_float, p, p]
+        lib.nvfp4_noalloc_check.restype = i32
+        lib.nvfp4_noalloc_check.argtypes = [p]
         lib.nvfp4_prefill_geometry.restype = i32
         lib.nvfp4_prefill_geometry.argtypes = [i64, i64, i32, i32, ctypes.POINTER(PrefillInfo)]
         lib.nvfp4_prefill_plan_create.restype = i32
@@ -321,6 +323,11 @@ def nvfp4_skinny_linear_noalloc(N, K, out_dtype, x, M, w_codes, w_block_scales, 
     if check:
         _check(st, "nvfp4_skinny_linear_noalloc")
     return st
+
+
+def nvfp4_noalloc_check(stream=None):
+    """Synchronise the stream; return and clear the allocation-free scratch's error status."""
+    return int(cuda_lib().nvfp4_noalloc_check(_stream(stream)))
 
 
 def nvfp4_plan_check(plan, stream=None):

@@ -328,7 +328,8 @@ const char* nvfp4_status_string(nvfp4_status status) {
     case NVFP4_ERR_NOMEM: return "NVFP4_ERR_NOMEM: allocation failed";
     case NVFP4_ERR_TIMEOUT: return "NVFP4_ERR_TIMEOUT: a bounded in-kernel wait ran out";
     case NVFP4_ERR_SCRATCH_LIMIT:
-      return "NVFP4_ERR_SCRATCH_LIMIT: the allocation-free entry point takes K <= 32768 and N <= 4194304";
+      return "NVFP4_ERR_SCRATCH_LIMIT: the problem needs more scratch than there is (the allocation-free entry "
+             "point takes K <= 32768 and N <= 4194304; a prefill call may not exceed its plan's max_M split parts)";
   }
   return "NVFP4_ERR_UNKNOWN";
 }
@@ -555,7 +556,6 @@ static_assert(kNaScratchBytes == NVFP4_NOALLOC_SCRATCH_BYTES, "header states the
 
 struct NoAllocDevice {
   bool ready = false;
-  uint8_t* scratch = nullptr;  // device address of g_noalloc_scratch on this device
   int sms = 0;
 };
 constexpr int kNaMaxDevices = 64;
@@ -570,26 +570,29 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNaScratchBytes
 
 namespace {
 
-// One-time set-up of the current device; returns NVFP4_OK and the device record.
-nvfp4_status noalloc_device(NoAllocDevice** out) {
+// Set-up of the current device: the SM count and the kernels' shared-memory limit once per
+// device, and, on every call, the device address of the scratch array (a host-side query; it
+// stays right even if the context was re-created).
+nvfp4_status noalloc_device(int* sms_out, uint8_t** scratch_out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;
   if (dev < 0 || dev >= kNaMaxDevices) return NVFP4_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_na_mutex);
-  NoAllocDevice& d = g_na_devices[dev];
-  if (!d.ready) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return NVFP4_ERR_CUDA;
-    int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
-      return NVFP4_ERR_CUDA;
-    if (set_smem_limits_once(dev) != cudaSuccess)
-      return NVFP4_ERR_CUDA;
-    d.scratch = static_cast<uint8_t*>(ptr);
-    d.sms = sms;
-    d.ready = true;
+  {
+    std::lock_guard<std::mutex> lock(g_na_mutex);
+    NoAllocDevice& d = g_na_devices[dev];
+    if (!d.ready) {
+      int sms = 0;
+      if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+        return NVFP4_ERR_CUDA;
+      if (set_smem_limits_once(dev) != cudaSuccess) return NVFP4_ERR_CUDA;
+      d.sms = sms;
+      d.ready = true;
+    }
+    *sms_out = d.sms;
   }
-  *out = &d;
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return NVFP4_ERR_CUDA;
+  *scratch_out = static_cast<uint8_t*>(ptr);
   return NVFP4_OK;
 }
 
@@ -605,17 +608,17 @@ extern "C" nvfp4_status nvfp4_skinny_linear_noalloc(int64_t N, int64_t K, nvfp4_
   if (K > kNaMaxK || N > kNaMaxN) return NVFP4_ERR_SCRATCH_LIMIT;
   if (!aligned16(x) || !aligned16(y) || !aligned16(w_codes) || !aligned16(w_block_scales)) return NVFP4_ERR_ALIGN;
 
-  NoAllocDevice* d = nullptr;
-  const nvfp4_status st = noalloc_device(&d);
+  int sms = 0;
+  uint8_t* base = nullptr;
+  const nvfp4_status st = noalloc_device(&sms, &base);
   if (st != NVFP4_OK) return st;
 
   const int64_t row_blocks = (N + nvfp4::kRowsPerBlock - 1) / nvfp4::kRowsPerBlock;
   const int64_t k_steps = K / nvfp4::kKStep;
   const int64_t units = row_blocks * k_steps;
-  int64_t grid = units < d->sms ? units : d->sms;
+  int64_t grid = units < sms ? units : sms;
   if (grid > kNaMaxGrid) grid = kNaMaxGrid;
 
-  uint8_t* base = d->scratch;
   int* err = reinterpret_cast<int*>(base);
   int* counters = reinterpret_cast<int*>(base + kNaErrBytes);
   float* parts = reinterpret_cast<float*>(base + kNaErrBytes + kNaCounterBytes);
@@ -630,11 +633,28 @@ extern "C" nvfp4_status nvfp4_skinny_linear_noalloc(int64_t N, int64_t K, nvfp4_
     return NVFP4_ERR_CUDA;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // what must start at zero: the split-K counters of this shape and the error word
-  if (cudaMemsetAsync(counters, 0, (size_t)row_blocks * 2 * sizeof(int), s) != cudaSuccess ||
-      cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess)
-    return NVFP4_ERR_CUDA;
+  // what must start at zero: the split-K counters of this shape (a call that gave up on a wait
+  // can leave some behind).  The error word keeps what earlier calls recorded until
+  // nvfp4_noalloc_check reads and clears it.
+  if (cudaMemsetAsync(counters, 0, (size_t)row_blocks * 2 * sizeof(int), s) != cudaSuccess) return NVFP4_ERR_CUDA;
 
   return launch_main(tm_codes, tm_scales, x, K, M, w_global_scale, y, N, parts, counters, err, x16, xs,
                      out_dtype == NVFP4_OUT_F32 ? 1 : 0, (int)grid, N, K, row_blocks, s);
+}
+
+extern "C" nvfp4_status nvfp4_noalloc_check(void* stream) {
+  int sms = 0;
+  uint8_t* base = nullptr;
+  const nvfp4_status st = noalloc_device(&sms, &base);
+  if (st != NVFP4_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int err = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess ||
+      cudaMemcpyAsync(&err, base, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return NVFP4_ERR_CUDA;
+  if (err == 0) return NVFP4_OK;
+  if (cudaMemsetAsync(base, 0, sizeof(int), s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+    return NVFP4_ERR_CUDA;
+  return NVFP4_ERR_TIMEOUT;
 }

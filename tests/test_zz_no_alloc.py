@@ -65,6 +65,27 @@ def test_noalloc_fp32_output():
     _check(case, y_plan, y_free)
 
 
+def test_noalloc_allocates_nothing_and_reports_no_error():
+    """After a first call (the per-device set-up), calls of several shapes leave the device's
+    free memory unchanged, and the error word reads clear."""
+    cases = [Case(2048, 8192, 9, seed=31), Case(640, 1024, 32, seed=32), Case(5120, 5120, 1, seed=33)]
+    ys = [torch.empty((c.M, c.N), dtype=torch.bfloat16, device="cuda") for c in cases]
+    c0 = cases[0]
+    nb.nvfp4_skinny_linear_noalloc(c0.N, c0.K, nb.NVFP4_OUT_BF16, c0.d_x, c0.M, c0.d_codes, c0.d_scales, c0.gs, ys[0])
+    torch.cuda.synchronize()
+    free_before, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        for c, y in zip(cases, ys):
+            nb.nvfp4_skinny_linear_noalloc(c.N, c.K, nb.NVFP4_OUT_BF16, c.d_x, c.M, c.d_codes, c.d_scales, c.gs, y)
+    torch.cuda.synchronize()
+    free_after, _ = torch.cuda.mem_get_info()
+    assert free_after == free_before
+    assert nb.nvfp4_noalloc_check() == nb.NVFP4_OK
+    for c, y in zip(cases, ys):
+        y_ref, absdot = c.oracle_full()
+        assert within_tolerance(to_f64(y), y_ref, absdot)[0]
+
+
 def test_noalloc_refuses_beyond_its_scratch():
     dev = torch.empty(64, dtype=torch.uint8, device="cuda")
     y = torch.empty(64, dtype=torch.uint8, device="cuda")
