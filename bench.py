@@ -38,7 +38,7 @@ HEAD_MS = (1, 16, 17, 32)
 L2_BYTES = 129 * 1000 * 1000
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ("nvfp4_skinny_gb300/csrc/nvfp4_skinny.cu", "nvfp4_skinny_gb300/csrc/skinny_kernels.cuh",
-                  "nvfp4_skinny_gb300/csrc/ptx.cuh")
+                  "nvfp4_skinny_gb300/csrc/gemv_kernels.cuh", "nvfp4_skinny_gb300/csrc/ptx.cuh")
 # DRAM bytes per launch measured with ncu, one JSON object per line (written from a capture's
 # dram__bytes_read.sum + dram__bytes_write.sum, keyed by the kernel sources' hash)
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_records.txt")
@@ -640,29 +640,35 @@ def run_reference(args, rank, world):
 
 
 def profile_shape(args):
-    """A few calls of one shape on rotating cold weights (> 2x L2), for ncu captures."""
+    """Calls of one shape on rotating cold weights (> 2x L2), for ncu captures: for each M in
+    turn (N,K,M1:M2:...), --warmup then --steps calls."""
     import torch
     from nvfp4_skinny_gb300 import binding as nb
     from nvfp4_skinny_gb300 import build as nbuild
     from nvfp4_skinny_gb300 import synth
     nbuild.build()
     parts = args.profile_shape.split(",")
-    N, K, M = int(parts[0]), int(parts[1]), int(parts[2])
+    N, K = int(parts[0]), int(parts[1])
+    Ms = [int(v) for v in parts[2].split(":")]
     f32 = len(parts) > 3 and parts[3] == "f32"
     copies = max(2, -(-2 * L2_BYTES // call_bytes(N, K, 1)))
     proj = Projection(N, K, 77, copies, f32, nb.NVFP4_PLAN_KERNEL_MMA_SYNC if args.mma else 0)
-    x = synth.activations(M, K, 77, device="cuda")
-    y = torch.empty((M, N), dtype=proj.out_dtype, device="cuda")
+    x_all = synth.activations(max(Ms), K, 77, device="cuda")
     torch.cuda.synchronize()
-    for i in range(args.warmup + args.steps):
-        c, sc, gs = proj.w[i % copies]
-        nb.nvfp4_skinny_linear(proj.plan, x, M, c, sc, gs, y)
-    torch.cuda.synchronize()
+    i = 0
+    for M in Ms:
+        x = x_all[:M].contiguous()
+        y = torch.empty((M, N), dtype=proj.out_dtype, device="cuda")
+        for _ in range(args.warmup + args.steps):
+            c, sc, gs = proj.w[i % copies]
+            nb.nvfp4_skinny_linear(proj.plan, x, M, c, sc, gs, y)
+            i += 1
+        torch.cuda.synchronize()
     st = nb.nvfp4_plan_check(proj.plan)
     if st != nb.NVFP4_OK:
         raise RuntimeError(nb.nvfp4_status_string(st))
-    print("profiled shape N=%d K=%d M=%d copies=%d calls=%d kernel=%s" % (
-        N, K, M, copies, args.warmup + args.steps, "mma" if args.mma else "tcgen05"))
+    print("profiled shape N=%d K=%d Ms=%s copies=%d calls per M=%d kernel=%s" % (
+        N, K, Ms, copies, args.warmup + args.steps, "mma" if args.mma else "tcgen05"))
 
 
 def profile_prefill(args):
@@ -732,8 +738,9 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true", help="skip the other workloads")
-    ap.add_argument("--profile-shape", default=None, metavar="N,K,M[,f32]",
-                    help="profiling driver: run --warmup then --steps calls of one shape on cold weights, no JSON")
+    ap.add_argument("--profile-shape", default=None, metavar="N,K,M[:M2...][,f32]",
+                    help="profiling driver: for each M, run --warmup then --steps calls of one shape on cold "
+                         "weights, no JSON")
     ap.add_argument("--mma", action="store_true", help="--profile-shape on register-direct mma.sync plans")
     ap.add_argument("--profile-prefill", default=None, metavar="N,K,M",
                     help="run a few prefill calls of one shape (for ncu) and exit")
