@@ -38,7 +38,8 @@ HEAD_MS = (1, 16, 17, 32)
 L2_BYTES = 129 * 1000 * 1000
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ("nvfp4_skinny_gb300/csrc/nvfp4_skinny.cu", "nvfp4_skinny_gb300/csrc/skinny_kernels.cuh",
-                  "nvfp4_skinny_gb300/csrc/gemv_kernels.cuh", "nvfp4_skinny_gb300/csrc/ptx.cuh")
+                  "nvfp4_skinny_gb300/csrc/gemv_kernels.cuh", "nvfp4_skinny_gb300/csrc/cluster_kernels.cuh",
+                  "nvfp4_skinny_gb300/csrc/ptx.cuh")
 # DRAM bytes per launch measured with ncu, one JSON object per line (written from a capture's
 # dram__bytes_read.sum + dram__bytes_write.sum, keyed by the kernel sources' hash)
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_records.txt")

@@ -119,6 +119,7 @@ int nvfp4_abi_version(void);
 /* Kernels a plan can run (nvfp4_plan_info.kernel). */
 #define NVFP4_KERNEL_TCGEN05 0
 #define NVFP4_KERNEL_MMA_SYNC 1
+#define NVFP4_KERNEL_CLUSTER 2
 
 /* Plan flags (nvfp4_plan_create_flags). */
 #define NVFP4_PLAN_DEFAULT 0u
@@ -126,6 +127,9 @@ int nvfp4_abi_version(void);
 #define NVFP4_PLAN_KERNEL_MMA_SYNC 2u       /* force the register-direct mma.sync kernel */
 #define NVFP4_PLAN_WEIGHTS_AFTER_WAIT 4u    /* read no weight byte before the kernels before the
                                                call on the stream have finished */
+#define NVFP4_PLAN_KERNEL_CLUSTER 8u        /* force the cluster-split mma.sync kernel; refused with
+                                               NVFP4_ERR_SHAPE when K / 128 has no split over a
+                                               cluster of 2, 4 or 8 blocks into at most 6 units each */
 
 /* Create a plan for an [N, K] weight with bfloat16 output.  The launch
  * configuration (kernel, rows per block, k-step, split of K across blocks, grid) is a
@@ -233,11 +237,12 @@ typedef struct {
   int64_t smem_bytes;       /* dynamic shared memory of the main kernel */
   int32_t launches_per_call; /* 1: the projection kernel prepares its activations; 2: a
                                 preparation kernel runs before it */
-  int32_t kernel;            /* NVFP4_KERNEL_TCGEN05 or NVFP4_KERNEL_MMA_SYNC */
+  int32_t kernel;            /* NVFP4_KERNEL_TCGEN05, NVFP4_KERNEL_MMA_SYNC or NVFP4_KERNEL_CLUSTER */
   int32_t warps_rows;        /* mma.sync: row groups of 32 rows per block (1 for tcgen05) */
   int32_t warps_k;           /* mma.sync: k-slices of 128 per block, added in order (1 for tcgen05) */
   uint32_t flags;            /* the plan's NVFP4_PLAN_* flags */
-  int32_t reserved;
+  int32_t cluster_size;      /* cluster kernel: blocks per cluster, each taking K / cluster_size
+                                (1 for the other kernels) */
 } nvfp4_plan_info;
 
 nvfp4_status nvfp4_plan_get_info(nvfp4_plan_t plan, nvfp4_plan_info* info);

@@ -28,13 +28,15 @@ NVFP4_NOALLOC_MAX_N = 4194304
 NVFP4_OUT_BF16 = 0
 NVFP4_OUT_F32 = 1
 NVFP4_MAX_M = 32
-NVFP4_ABI_VERSION = 3
+NVFP4_ABI_VERSION = 4
 NVFP4_KERNEL_TCGEN05 = 0
 NVFP4_KERNEL_MMA_SYNC = 1
+NVFP4_KERNEL_CLUSTER = 2
 NVFP4_PLAN_DEFAULT = 0
 NVFP4_PLAN_KERNEL_TCGEN05 = 1
 NVFP4_PLAN_KERNEL_MMA_SYNC = 2
 NVFP4_PLAN_WEIGHTS_AFTER_WAIT = 4
+NVFP4_PLAN_KERNEL_CLUSTER = 8
 
 NVFP4_PACK_OK = 0
 NVFP4_PACK_ERR_ARG = -1
@@ -73,7 +75,7 @@ class PlanInfo(ctypes.Structure):
                 ("device", ctypes.c_int32), ("row_blocks", ctypes.c_int64), ("k_steps", ctypes.c_int64),
                 ("units", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64), ("smem_bytes", ctypes.c_int64),
                 ("launches_per_call", ctypes.c_int32), ("kernel", ctypes.c_int32), ("warps_rows", ctypes.c_int32),
-                ("warps_k", ctypes.c_int32), ("flags", ctypes.c_uint32), ("reserved", ctypes.c_int32)]
+                ("warps_k", ctypes.c_int32), ("flags", ctypes.c_uint32), ("cluster_size", ctypes.c_int32)]
 
 
 class PrefillInfo(ctypes.Structure):

@@ -18,7 +18,8 @@ CUDA_LIB = os.path.join(OUT, "libnvfp4skinny.so")
 PACK_LIB = os.path.join(OUT, "libnvfp4pack.so")
 
 CUDA_SOURCES = ["nvfp4_skinny.cu", "quantize.cu", "prefill.cu"]
-CUDA_DEPS = ["nvfp4_skinny.cu", "quantize.cu", "prefill.cu", "skinny_kernels.cuh", "gemv_kernels.cuh", "prefill_kernels.cuh",
+CUDA_DEPS = ["nvfp4_skinny.cu", "quantize.cu", "prefill.cu", "skinny_kernels.cuh", "gemv_kernels.cuh", "cluster_kernels.cuh",
+             "prefill_kernels.cuh",
              "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -16,8 +16,9 @@
 //     rows, bytes 16 t .. 16 t + 15 and 64 + 16 t .. 64 + 16 t + 15 of the row's 128 code
 //     bytes (so each copy instruction reads 64 contiguous bytes of every row), and lane t = 0
 //     the row's 16 scale bytes, with cp.async (L2 evict-first, 256-byte L2 prefetch) into the
-//     warp's ring of `depth` shared-memory stages, depth - 1 units ahead of use, then reads
-//     them back into registers (the ring holds the bytes in flight, so they cost no registers);
+//     warp's ring of `depth` shared-memory stages (every stage is filled before the dependency
+//     wait; a stage is refilled, `depth` units ahead, as soon as its unit has been read back into
+//     registers), so the bytes in flight cost no registers;
 //   - the codes are decoded with cvt.rn.f16x2.e2m1x2 and multiplied by the block scale
 //     (cvt.rn.f16x2.e4m3x2) in fp16, which is exact ("10 Kernels" 10.2: at most six
 //     significant bits), straight into the A-operand registers of mma.sync.m16n8k16
@@ -55,7 +56,7 @@ constexpr int kWarpRows = 16 * kTilesPerWarp;  // 32
 constexpr int kUnitK = 256;            // k per warp per unit: 64 consecutive k per lane
 constexpr int kUnitCodeBytes = kUnitK / 2;     // 128 bytes of a row's codes per unit (32 per lane)
 constexpr int kUnitScaleBytes = kUnitK / 16;   // 16 scale bytes of a row per unit (4 per lane)
-constexpr int kMaxDepth = 3;           // shared-memory stages per warp (units in flight + 1)
+constexpr int kMaxDepth = 3;           // shared-memory stages per warp (units in flight)
 constexpr int kStageCodeBytes = 4 * 2 * 32 * 16;  // [row (tile, half)][16-byte piece][lane]
 constexpr int kStageScaleBytes = 4 * 8 * 16;      // [row][quad] the row's 16 scale bytes of the unit
 constexpr int kStageBytes = kStageCodeBytes + kStageScaleBytes;  // 4608 per warp per unit
@@ -119,6 +120,7 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) 
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes));
 }
 __device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+__device__ __forceinline__ void prefetch_l1(const void* p) { asm volatile("prefetch.global.L1 [%0];" ::"l"(p)); }
 __device__ __forceinline__ uint4 lds128(uint32_t a) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
@@ -336,13 +338,13 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM) gemv_kernel(const __gr
     }
     ptx::cp_async_commit();
   };
-  // The ring's first depth - 1 units, then the next kL2Ahead units of the range into L2 (lane L
-  // takes row L of the warp's 32): with one k-slice the units of a row block are consecutive
-  // k-steps, so one bulk prefetch per row covers them; otherwise one per unit.  Issued before
-  // the dependency wait, they keep DRAM busy while the kernels before this one finish.
+  // The ring's first `depth` units (every stage), then the next kL2Ahead units of the range into
+  // L2 (lane L takes row L of the warp's 32): with one k-slice the units of a row block are
+  // consecutive k-steps, so one bulk prefetch per row covers them; otherwise one per unit.  Issued
+  // before the dependency wait, they keep DRAM busy while the kernels before this one finish.
   auto prefetch = [&]() {
-    for (int j = 0; j < depth - 1; ++j) issue_next(j);
-    const int j0 = depth - 1, j1 = min(n_local, depth - 1 + kL2Ahead);
+    for (int j = 0; j < depth; ++j) issue_next(j);
+    const int j0 = depth, j1 = min(n_local, depth + kL2Ahead);
     if (j0 >= j1) return;
     const int rb = l_rb, ks = l_ks;  // unit j0 (issue_next advanced the cursor to it)
     const int64_t n = (int64_t)rb * row_block_rows + (int64_t)wr_i * kWarpRows + lane;
@@ -365,6 +367,20 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM) gemv_kernel(const __gr
   ptx::grid_launch_dependents();
   ptx::grid_dependency_wait();  // activations, parts and counters are touched only after this
   if (p.weights_after_wait) prefetch();
+
+  // The activation fragments of the unit at k-step ks into L1 (lane L: line L of each 4 KB
+  // n-tile run), so that the first warp to multiply it does not wait on L2 for each load.
+  constexpr int nt_stride = NT * 8 * 32;  // uint4 per 256-k step of x16
+  auto prefetch_x = [&](int ks) {
+    const uint8_t* base = reinterpret_cast<const uint8_t*>(p.x16 + (int64_t)(ks * p.wk + wk_i) * nt_stride);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) prefetch_l1(base + nt * 4096 + lane * 128);
+  };
+  {
+    const int ks0 = (int)(u_begin - (int64_t)rb_first * S);
+    if (n_local > 0) prefetch_x(ks0);
+    if (n_local > 1) prefetch_x((ks0 + 1) % S32);
+  }
 
   float acc[kTilesPerWarp][NT][4];
   auto zero_acc = [&]() {
@@ -401,7 +417,60 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM) gemv_kernel(const __gr
       }
   };
 
-  // end of a row-block segment: times 2^-e, k-slices added in slice order, then y or a part
+  // A part published by this warp whose count has not been read yet: the count comes back while
+  // the next unit is multiplied, and only then is it compared (row block pend_rb, -1: none).
+  int pend_rb = -1, pend_old = 0;
+
+  // Read the pending count: the warp that completed it adds every block's part in block order
+  // (all loads of a batch in flight together) and stores y.
+  auto finish_pending = [&]() {
+    const int rb = pend_rb;
+    pend_rb = -1;
+    const int old = __shfl_sync(0xffffffffu, pend_old, 0);
+    const int64_t b_first = block_of_unit64((int64_t)rb * S, T, G);
+    const int64_t b_last = block_of_unit64((int64_t)rb * S + S - 1, T, G);
+    if (old != (int)(b_last - b_first)) return;
+    if (lane == 0) ptx::fence_acq_rel_gpu();  // the other blocks' parts, released with their increments
+    __syncwarp();                             // ... are visible to every lane from here on
+    float v[kTilesPerWarp][NT][4];
+#pragma unroll
+    for (int r = 0; r < kTilesPerWarp; ++r)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) v[r][nt][c] = 0.f;
+    constexpr int kB = NT <= 2 ? 4 : 2;
+    for (int64_t b = b_first; b <= b_last; b += kB) {
+      float4 o[kB][kTilesPerWarp][NT];
+#pragma unroll
+      for (int j = 0; j < kB; ++j) {
+        const int64_t bj = b + j <= b_last ? b + j : b_last;
+        const float4* q = p.parts + ((bj * 2 + (rb == (bj * T / G) / S ? 0 : 1)) * p.wr + wr_i) * kPartFloat4;
+#pragma unroll
+        for (int r = 0; r < kTilesPerWarp; ++r)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) o[j][r][nt] = __ldcg(q + (r * kMaxNT + nt) * 32 + lane);
+      }
+#pragma unroll
+      for (int j = 0; j < kB; ++j) {
+        if (b + j > b_last) break;
+#pragma unroll
+        for (int r = 0; r < kTilesPerWarp; ++r)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            v[r][nt][0] = __fadd_rn(v[r][nt][0], o[j][r][nt].x);
+            v[r][nt][1] = __fadd_rn(v[r][nt][1], o[j][r][nt].y);
+            v[r][nt][2] = __fadd_rn(v[r][nt][2], o[j][r][nt].z);
+            v[r][nt][3] = __fadd_rn(v[r][nt][3], o[j][r][nt].w);
+          }
+      }
+    }
+    store_y(rb, v);
+    if (lane == 0) p.counters[(int64_t)rb * p.wr + wr_i] = 0;  // zero between calls
+  };
+
+  // end of a row-block segment: times 2^-e, k-slices added in slice order, then y, or a part
+  // published with a release increment of the row group's count (read later: finish_pending)
   auto flush = [&](int rb, bool complete) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -445,8 +514,6 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM) gemv_kernel(const __gr
       if (complete) {
         store_y(rb, acc);
       } else {
-        // publish this block's part of the row group; the block whose part completes the count
-        // adds every block's part in block order (all its loads issued before the additions)
         const int slot = rb == rb_first ? 0 : 1;
         float4* part = p.parts + (((int64_t)blockIdx.x * 2 + slot) * p.wr + wr_i) * kPartFloat4;  // this block's slot
 #pragma unroll
@@ -455,68 +522,32 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM) gemv_kernel(const __gr
           for (int nt = 0; nt < NT; ++nt)
             part[(r * kMaxNT + nt) * 32 + lane] = make_float4(acc[r][nt][0], acc[r][nt][1], acc[r][nt][2], acc[r][nt][3]);
         __syncwarp();  // every lane's stores are ordered before lane 0's release
-        const int64_t b_first = block_of_unit64((int64_t)rb * S, T, G);
-        const int64_t b_last = block_of_unit64((int64_t)rb * S + S - 1, T, G);
-        int* cnt = p.counters + (int64_t)rb * p.wr + wr_i;
-        int old = 0;
-        if (lane == 0) old = ptx::atom_acq_rel_gpu_add(cnt, 1);
-        old = __shfl_sync(0xffffffffu, old, 0);
-        if (old == (int)(b_last - b_first)) {
-          __syncwarp();  // the lanes' reads are ordered after lane 0's acquire
-          zero_acc();    // this block's own part is added again at its place in the order
-          // parts loaded kB blocks at a time (all loads of a batch in flight together), added in
-          // block order
-          constexpr int kB = NT <= 2 ? 4 : 2;
-          for (int64_t b = b_first; b <= b_last; b += kB) {
-            float4 o[kB][kTilesPerWarp][NT];
-#pragma unroll
-            for (int j = 0; j < kB; ++j) {
-              const int64_t bj = b + j <= b_last ? b + j : b_last;
-              const float4* q = p.parts + ((bj * 2 + (rb == (bj * T / G) / S ? 0 : 1)) * p.wr + wr_i) * kPartFloat4;
-#pragma unroll
-              for (int r = 0; r < kTilesPerWarp; ++r)
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) o[j][r][nt] = __ldcg(q + (r * kMaxNT + nt) * 32 + lane);
-            }
-#pragma unroll
-            for (int j = 0; j < kB; ++j) {
-              if (b + j > b_last) break;
-#pragma unroll
-              for (int r = 0; r < kTilesPerWarp; ++r)
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                  acc[r][nt][0] = __fadd_rn(acc[r][nt][0], o[j][r][nt].x);
-                  acc[r][nt][1] = __fadd_rn(acc[r][nt][1], o[j][r][nt].y);
-                  acc[r][nt][2] = __fadd_rn(acc[r][nt][2], o[j][r][nt].z);
-                  acc[r][nt][3] = __fadd_rn(acc[r][nt][3], o[j][r][nt].w);
-                }
-            }
-          }
-          store_y(rb, acc);
-          if (lane == 0) *cnt = 0;  // zero between calls
-        }
+        if (lane == 0) pend_old = ptx::atom_release_gpu_add(p.counters + (int64_t)rb * p.wr + wr_i, 1);
+        pend_rb = rb;
       }
     }
     if (p.wk > 1) __syncthreads();  // the shared parts are free for the next segment
   };
 
-  // ---- main loop: wait for unit i's copies, queue unit i + depth - 1 into the stage unit i - 1
-  // used, read unit i, multiply
+  // ---- main loop: wait for unit i's copies, multiply it, then queue unit i + depth into the
+  // stage it used; a part published at the previous segment's end is finished after one more unit
   int c_rb = rb_first, c_ks = (int)(u_begin - (int64_t)rb_first * S);
   int seg_ks0 = c_ks;
   int c_st = 0;
-  constexpr int nt_stride = NT * 8 * 32;  // uint4 per 256-k step of x16
   // the lane's scale bytes 2 t, 2 t + 1 (and 8 + 2 t, 9 + 2 t) of its row's 16: in word t / 2
   // (and 2 + t / 2), half t % 2
   const uint32_t s_off = (uint32_t)(g * 16 + (t >> 1) * 4), s_sh = (uint32_t)((t & 1) * 16);
   for (int i = 0; i < n_local; ++i) {
-    ptx::cp_async_wait(depth - 2);  // at most depth - 2 later groups still pending: unit i has landed
+    ptx::cp_async_wait(depth - 1);  // at most depth - 1 later groups still pending: unit i has landed
     __syncwarp();                   // a row's scale bytes were copied by lane t = 0 of its quad
-    issue_next(i + depth - 1);      // into the stage every lane finished reading last iteration
     const uint32_t stage = ring + (uint32_t)(c_st * kStageBytes);
     if (++c_st == depth) c_st = 0;
     const uint4* xq = p.x16 + (int64_t)(c_ks * p.wk + wk_i) * nt_stride + lane;
     mma_unit<NT>(acc, stage + (uint32_t)(lane * 16), stage + kStageCodeBytes + s_off, s_sh, xq);
+    __syncwarp();              // every lane has read the stage (a quad shares its scale words)
+    issue_next(i + depth);     // into the stage just read
+    if (i + 2 < n_local) prefetch_x((c_ks + 2) % S32);
+    if (pend_rb >= 0) finish_pending();
     if (c_ks == S32 - 1 || i == n_local - 1) {
       flush(c_rb, seg_ks0 == 0 && c_ks == S32 - 1);
       zero_acc();
@@ -527,8 +558,8 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM) gemv_kernel(const __gr
       ++c_rb;
     }
   }
+  if (pend_rb >= 0) finish_pending();
   ptx::cp_async_wait(0);  // no copy may still target shared memory when the block exits
-
 }
 
 }  // namespace gemv

@@ -12,14 +12,16 @@
 #include <mutex>
 #include <new>
 
+#include "cluster_kernels.cuh"
 #include "gemv_kernels.cuh"
 #include "nvfp4_skinny.h"
 #include "skinny_kernels.cuh"
 
 namespace {
 
-constexpr int kAbiVersion = 3;
-constexpr uint32_t kKnownFlags = NVFP4_PLAN_KERNEL_TCGEN05 | NVFP4_PLAN_KERNEL_MMA_SYNC | NVFP4_PLAN_WEIGHTS_AFTER_WAIT;
+constexpr int kAbiVersion = 4;
+constexpr uint32_t kKernelFlags = NVFP4_PLAN_KERNEL_TCGEN05 | NVFP4_PLAN_KERNEL_MMA_SYNC | NVFP4_PLAN_KERNEL_CLUSTER;
+constexpr uint32_t kKnownFlags = kKernelFlags | NVFP4_PLAN_WEIGHTS_AFTER_WAIT;
 
 struct Workspace {
   float* partials = nullptr; // tcgen05: [2 * grid][32][256]; mma.sync: [2 * grid][wr] parts of 4 KB
@@ -38,6 +40,15 @@ struct GemvGeometry {
   int depth = nvfp4::gemv::kMaxDepth;  // shared-memory stages per warp
   int64_t row_blocks = 0, S = 0, units = 0;
   int grid = 0;
+};
+
+// Work split of the cluster kernel: clusters of C blocks, each cluster a panel of 16-row tiles
+// over all of K (block rank r: k-units [r Uk, (r + 1) Uk) of 128), two blocks per SM.  A function
+// of (N, K) and the device (the clusters it can hold at once) only.
+struct ClusterGeometry {
+  bool ok = false;
+  int C = 0, clusters = 0, units_k = 0, tiles = 0, tiles_max = 0;
+  int depth[nvfp4::cluster::kMaxNT + 1] = {0};  // stages per warp by n-tiles (1..4): scheduling only
 };
 
 // The fewest k-slices per block (wk) for which the blocks sharing a row block are, on average,
@@ -82,7 +93,8 @@ struct nvfp4_plan {
   int sm_count = 0;
   int grid = 0;
   int64_t row_blocks = 0, k_steps = 0, units = 0;
-  GemvGeometry gg;  // mma.sync kernel
+  GemvGeometry gg;     // mma.sync kernel
+  ClusterGeometry cg;  // cluster kernel
   Workspace ws;
 };
 
@@ -158,7 +170,18 @@ cudaError_t set_smem_limits() {
       (e = cudaFuncSetAttribute(nvfp4::gemv::gemv_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs)) !=
           cudaSuccess)
     return e;
-  return cudaFuncSetAttribute(nvfp4::gemv::gemv_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs);
+  if ((e = cudaFuncSetAttribute(nvfp4::gemv::gemv_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs)) !=
+      cudaSuccess)
+    return e;
+  const int cs = nvfp4::cluster::kSmemLimit;
+  if ((e = cudaFuncSetAttribute(nvfp4::cluster::cluster_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, cs)) !=
+          cudaSuccess ||
+      (e = cudaFuncSetAttribute(nvfp4::cluster::cluster_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, cs)) !=
+          cudaSuccess ||
+      (e = cudaFuncSetAttribute(nvfp4::cluster::cluster_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, cs)) !=
+          cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(nvfp4::cluster::cluster_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, cs);
 }
 
 // Raise the kernels' shared-memory limits once per device (thread-safe).
@@ -171,6 +194,75 @@ cudaError_t set_smem_limits_once(int dev) {
   const cudaError_t e = set_smem_limits();
   if (e == cudaSuccess) done[dev] = true;
   return e;
+}
+
+// Clusters of C blocks that the device holds at once with `smem` bytes of dynamic shared memory
+// per block (0 on error).
+int max_active_clusters(int C, int smem) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)C);
+  cfg.blockDim = dim3(nvfp4::cluster::kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, nvfp4::cluster::cluster_kernel<nvfp4::cluster::kMaxNT>, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+// The largest cluster (8, 4 or 2 blocks) whose blocks' k-slices are whole 128-k units, at most
+// kMaxUnitsK of them; then as many clusters as the device holds at once (at most one per 16-row
+// tile), each a contiguous panel of tiles, with shared memory sized for the widest panel at
+// M = 32.  Not available (ok = false) when no cluster size fits.
+ClusterGeometry cluster_geometry(int64_t N, int64_t K, int sms) {
+  ClusterGeometry g;
+  const int64_t tiles = (N + 15) / 16;
+  for (int C = 8; C >= 2; C /= 2) {
+    if (K % ((int64_t)C * nvfp4::cluster::kUnitK) != 0) continue;
+    const int64_t uk = K / ((int64_t)C * nvfp4::cluster::kUnitK);
+    if (uk > nvfp4::cluster::kMaxUnitsK) continue;
+    int64_t clusters = (int64_t)2 * sms / C;
+    if (clusters > tiles) clusters = tiles;
+    for (int it = 0; it < 8 && clusters > 0; ++it) {
+      const int64_t tmax = (tiles + clusters - 1) / clusters;
+      const int64_t smem =
+          nvfp4::cluster::smem_bytes(nvfp4::cluster::kMinDepth, (int)uk, nvfp4::cluster::kMaxNT, (int)tmax);
+      if (smem > nvfp4::cluster::kSmemLimit) {
+        clusters = 0;
+        break;
+      }
+      const int active = max_active_clusters(C, (int)smem);
+      if (active >= clusters) {
+        g.ok = true;
+        g.C = C;
+        g.clusters = (int)clusters;
+        g.units_k = (int)uk;
+        g.tiles = (int)tiles;
+        g.tiles_max = (int)tmax;
+        // the deepest ring (up to a warp's whole share) that the shared memory of each M band allows;
+        // the band at M = 32 keeps kMinDepth, so two blocks per SM hold for every band
+        const int share = (int)((tmax * uk + nvfp4::cluster::kWarps - 1) / nvfp4::cluster::kWarps);
+        for (int nt = 1; nt <= nvfp4::cluster::kMaxNT; ++nt) {
+          int d = nvfp4::cluster::kMinDepth;
+          while (d < nvfp4::cluster::kMaxDepth && d < share &&
+                 nvfp4::cluster::smem_bytes(d + 1, (int)uk, nt, (int)tmax) <= nvfp4::cluster::kSmemLimit)
+            ++d;
+          g.depth[nt] = d;
+        }
+        return g;
+      }
+      clusters = active;
+    }
+  }
+  return g;
 }
 
 // The two launches of a call on the register-direct kernel: activation preparation, then the
@@ -299,9 +391,66 @@ nvfp4_status launch_main(const CUtensorMap& tm_codes, const CUtensorMap& tm_scal
   return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
+// The one launch of a call on the cluster kernel (cluster dimension C, programmatic dependent
+// launch after the kernels before it).
+template <int NT>
+cudaError_t launch_cluster_nt(const nvfp4::cluster::Params& p, cudaStream_t stream) {
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)p.C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(p.clusters * p.C));
+  cfg.blockDim = dim3(nvfp4::cluster::kThreads);
+  cfg.dynamicSmemBytes = (size_t)nvfp4::cluster::smem_bytes(p.depth, p.units_k, NT, p.tiles_max);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, nvfp4::cluster::cluster_kernel<NT>, p);
+}
+
+nvfp4_status launch_cluster(const ClusterGeometry& cg, const void* x, int64_t lda, int M, const uint8_t* codes,
+                            const uint8_t* scales, float gs, void* y, int64_t ldc, int out_f32, int64_t N, int64_t K,
+                            int weights_after_wait, cudaStream_t stream, int silu_mul = 0) {
+  nvfp4::cluster::Params p;
+  p.codes = codes;
+  p.scales = scales;
+  p.x = static_cast<const uint16_t*>(x);
+  p.lda = lda;
+  p.y = y;
+  p.ldc = ldc;
+  p.N = N;
+  p.K = K;
+  p.gs = gs;
+  p.M = M;
+  p.out_f32 = out_f32;
+  p.silu_mul = silu_mul;
+  p.weights_after_wait = weights_after_wait;
+  p.C = cg.C;
+  p.clusters = cg.clusters;
+  p.units_k = cg.units_k;
+  p.tiles = cg.tiles;
+  p.tiles_max = cg.tiles_max;
+  p.depth = cg.depth[(M + 7) / 8];
+  cudaError_t e;
+  switch ((M + 7) / 8) {
+    case 1: e = launch_cluster_nt<1>(p, stream); break;
+    case 2: e = launch_cluster_nt<2>(p, stream); break;
+    case 3: e = launch_cluster_nt<3>(p, stream); break;
+    default: e = launch_cluster_nt<4>(p, stream); break;
+  }
+  return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
 nvfp4_status launch_call(nvfp4_plan* plan, const void* x, int64_t lda, int M, const uint8_t* codes,
                          const uint8_t* scales, float gs, void* y, int64_t ldc, cudaStream_t stream,
                          int silu_mul = 0) {
+  if (plan->kernel == NVFP4_KERNEL_CLUSTER)
+    return launch_cluster(plan->cg, x, lda, M, codes, scales, gs, y, ldc, plan->out == NVFP4_OUT_F32 ? 1 : 0,
+                          plan->N, plan->K, (plan->flags & NVFP4_PLAN_WEIGHTS_AFTER_WAIT) ? 1 : 0, stream, silu_mul);
   if (plan->kernel == NVFP4_KERNEL_MMA_SYNC)
     return launch_gemv(plan->gg, x, lda, M, codes, scales, gs, y, ldc, plan->ws.partials, plan->ws.counters,
                        plan->ws.x16, plan->ws.xs, plan->out == NVFP4_OUT_F32 ? 1 : 0, plan->N, plan->K,
@@ -341,10 +490,8 @@ nvfp4_status nvfp4_plan_create_flags(int64_t N, int64_t K, nvfp4_out_dtype out_d
   if (!out_plan) return NVFP4_ERR_ARG;
   *out_plan = nullptr;
   if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_F32) return NVFP4_ERR_ARG;
-  if ((flags & ~kKnownFlags) != 0u ||
-      (flags & (NVFP4_PLAN_KERNEL_TCGEN05 | NVFP4_PLAN_KERNEL_MMA_SYNC)) ==
-          (NVFP4_PLAN_KERNEL_TCGEN05 | NVFP4_PLAN_KERNEL_MMA_SYNC))
-    return NVFP4_ERR_ARG;
+  const uint32_t kf = flags & kKernelFlags;
+  if ((flags & ~kKnownFlags) != 0u || (kf & (kf - 1u)) != 0u) return NVFP4_ERR_ARG;  // at most one kernel
   if (N < 1 || K < nvfp4::kKStep || K % nvfp4::kKStep != 0) return NVFP4_ERR_SHAPE;
   // TMA row coordinates are 32-bit; byte offsets stay far from int64 overflow
   if (N >= (int64_t(1) << 31) || K > (int64_t(1) << 24) || N > (int64_t(1) << 40) / K) return NVFP4_ERR_SHAPE;
@@ -368,9 +515,25 @@ nvfp4_status nvfp4_plan_create_flags(int64_t N, int64_t K, nvfp4_out_dtype out_d
   plan->kernel = (flags & NVFP4_PLAN_KERNEL_MMA_SYNC) ? NVFP4_KERNEL_MMA_SYNC : NVFP4_KERNEL_TCGEN05;
   plan->device = dev;
   plan->sm_count = sms;
+  if (flags & NVFP4_PLAN_KERNEL_CLUSTER) {
+    plan->cg = cluster_geometry(N, K, sms);
+    if (!plan->cg.ok) {
+      delete plan;
+      return NVFP4_ERR_SHAPE;
+    }
+    plan->kernel = NVFP4_KERNEL_CLUSTER;
+  }
 
   size_t part_bytes, cnt_bytes, x16b, cnt_count;
-  if (plan->kernel == NVFP4_KERNEL_MMA_SYNC) {
+  if (plan->kernel == NVFP4_KERNEL_CLUSTER) {  // nothing leaves a cluster but y
+    plan->row_blocks = plan->cg.tiles;
+    plan->k_steps = plan->cg.C * (int64_t)plan->cg.units_k;
+    plan->units = plan->row_blocks * plan->k_steps;
+    plan->grid = plan->cg.clusters * plan->cg.C;
+    part_bytes = 0;
+    cnt_count = 0;
+    x16b = 0;
+  } else if (plan->kernel == NVFP4_KERNEL_MMA_SYNC) {
     plan->gg = gemv_geometry(N, K, sms);
     plan->row_blocks = plan->gg.row_blocks;
     plan->k_steps = plan->gg.S;
@@ -497,9 +660,10 @@ nvfp4_status nvfp4_plan_check(nvfp4_plan_t plan, void* stream) {
   if (err != 0) {
     // an aborted call may leave split-K counters behind: clear them with the error word
     if (cudaMemsetAsync(plan->ws.err, 0, sizeof(int), s) != cudaSuccess ||
-        cudaMemsetAsync(plan->ws.counters, 0,
-                        (size_t)plan->row_blocks * (plan->kernel == NVFP4_KERNEL_MMA_SYNC ? plan->gg.wr : 2) * sizeof(int),
-                        s) != cudaSuccess ||
+        (plan->kernel != NVFP4_KERNEL_CLUSTER &&
+         cudaMemsetAsync(plan->ws.counters, 0,
+                         (size_t)plan->row_blocks * (plan->kernel == NVFP4_KERNEL_MMA_SYNC ? plan->gg.wr : 2) * sizeof(int),
+                         s) != cudaSuccess) ||
         cudaStreamSynchronize(s) != cudaSuccess)
       return NVFP4_ERR_CUDA;
     return NVFP4_ERR_TIMEOUT;
@@ -510,13 +674,14 @@ nvfp4_status nvfp4_plan_check(nvfp4_plan_t plan, void* stream) {
 nvfp4_status nvfp4_plan_get_info(nvfp4_plan_t plan, nvfp4_plan_info* info) {
   if (!plan || !info) return NVFP4_ERR_ARG;
   const bool mma = plan->kernel == NVFP4_KERNEL_MMA_SYNC;
+  const bool clu = plan->kernel == NVFP4_KERNEL_CLUSTER;
   info->N = plan->N;
   info->K = plan->K;
   info->out_dtype = (int32_t)plan->out;
-  info->rows_per_block = mma ? plan->gg.wr * nvfp4::gemv::kWarpRows : nvfp4::kRowsPerBlock;
-  info->k_step = mma ? plan->gg.wk * nvfp4::gemv::kUnitK : nvfp4::kKStep;
-  info->stages = mma ? plan->gg.depth : nvfp4::kStages;
-  info->threads = mma ? nvfp4::gemv::kThreads : nvfp4::kThreads;
+  info->rows_per_block = clu ? 16 : mma ? plan->gg.wr * nvfp4::gemv::kWarpRows : nvfp4::kRowsPerBlock;
+  info->k_step = clu ? nvfp4::cluster::kUnitK : mma ? plan->gg.wk * nvfp4::gemv::kUnitK : nvfp4::kKStep;
+  info->stages = clu ? plan->cg.depth[nvfp4::cluster::kMaxNT] : mma ? plan->gg.depth : nvfp4::kStages;
+  info->threads = clu ? nvfp4::cluster::kThreads : mma ? nvfp4::gemv::kThreads : nvfp4::kThreads;
   info->grid = plan->grid;
   info->sm_count = plan->sm_count;
   info->device = plan->device;
@@ -524,13 +689,16 @@ nvfp4_status nvfp4_plan_get_info(nvfp4_plan_t plan, nvfp4_plan_info* info) {
   info->k_steps = plan->k_steps;
   info->units = plan->units;
   info->workspace_bytes = (int64_t)plan->ws.bytes;
-  info->smem_bytes = mma ? nvfp4::gemv::smem_bytes(plan->gg.depth, nvfp4::gemv::kMaxNT, plan->gg.wk) : nvfp4::kSmemBytes;
-  info->launches_per_call = mma ? 2 : (fused_mode(plan->row_blocks, plan->K, plan->grid) ? 1 : 2);
+  info->smem_bytes = clu ? nvfp4::cluster::smem_bytes(plan->cg.depth[nvfp4::cluster::kMaxNT], plan->cg.units_k,
+                                                      nvfp4::cluster::kMaxNT, plan->cg.tiles_max)
+                     : mma ? nvfp4::gemv::smem_bytes(plan->gg.depth, nvfp4::gemv::kMaxNT, plan->gg.wk)
+                           : nvfp4::kSmemBytes;
+  info->launches_per_call = clu ? 1 : mma ? 2 : (fused_mode(plan->row_blocks, plan->K, plan->grid) ? 1 : 2);
   info->kernel = plan->kernel;
   info->warps_rows = mma ? plan->gg.wr : 1;
   info->warps_k = mma ? plan->gg.wk : 1;
   info->flags = plan->flags;
-  info->reserved = 0;
+  info->cluster_size = clu ? plan->cg.C : 1;
   return NVFP4_OK;
 }
 

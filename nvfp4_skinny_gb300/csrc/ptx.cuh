@@ -85,17 +85,19 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64
                : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// Wait until at most n (0..3; larger counts as 3) of this thread's committed groups are still
+// Wait until at most n (0..7; larger counts as 7) of this thread's committed groups are still
 // in flight.
 __device__ __forceinline__ void cp_async_wait(int n) {
-  if (n <= 0)
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-  else if (n == 1)
-    asm volatile("cp.async.wait_group 1;" ::: "memory");
-  else if (n == 2)
-    asm volatile("cp.async.wait_group 2;" ::: "memory");
-  else
-    asm volatile("cp.async.wait_group 3;" ::: "memory");
+  switch (n < 0 ? 0 : n) {
+    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+    case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+    case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+    case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
+    case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
+    default: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
+  }
 }
 // 2-D tiled tensor copy global -> shared (box and swizzle from the tensor map); x is the
 // inner (byte) coordinate and must be a multiple of 16.
@@ -234,12 +236,45 @@ __device__ __forceinline__ int atom_acq_rel_gpu_add(int* ptr, int v) {
   return old;
 }
 
-// Compare-and-swap on a global int with acquire-release semantics at GPU scope; returns the old value.
-__device__ __forceinline__ int atom_cas_acq_rel_gpu(int* ptr, int expected, int desired) {
+// Add to a global int with release semantics at GPU scope; returns the old value.  The issuing
+// thread does not wait for the result until it reads it, so later work overlaps the round trip.
+__device__ __forceinline__ int atom_release_gpu_add(int* ptr, int v) {
   int old;
-  asm volatile("atom.acq_rel.gpu.global.cas.b32 %0, [%1], %2, %3;" : "=r"(old) : "l"(ptr), "r"(expected), "r"(desired)
-               : "memory");
+  asm volatile("atom.release.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
   return old;
+}
+// Acquire-release fence at GPU scope: after observing a counter that other threads advanced with
+// release atomics, makes their earlier writes visible to this thread's later reads.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// ---------------------------------------------------------------- thread-block clusters
+// This block's rank within its cluster.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every block of the cluster arrives and waits: the writes to shared memory made
+// before it (release) are visible to every block of the cluster after it (acquire).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The address in block `rank`'s shared memory of the variable at this block's shared address a.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t a, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(a) : "memory");
+  return v;
 }
 
 // fp32 -> bfloat16 bits, round to nearest even.

@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(header, getter, listed):
 
 
 def test_status_strings_and_version():
-    assert nb.nvfp4_abi_version() == nb.NVFP4_ABI_VERSION == 3
+    assert nb.nvfp4_abi_version() == nb.NVFP4_ABI_VERSION == 4
     for s in range(9):
         assert nb.nvfp4_status_string(s).startswith("NVFP4_")
 

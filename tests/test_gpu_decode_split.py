@@ -18,7 +18,8 @@ from nvfp4_skinny_gb300 import binding as nb
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = {"tcgen05": nb.NVFP4_PLAN_KERNEL_TCGEN05, "mma": nb.NVFP4_PLAN_KERNEL_MMA_SYNC}
+KERNELS = {"tcgen05": nb.NVFP4_PLAN_KERNEL_TCGEN05, "mma": nb.NVFP4_PLAN_KERNEL_MMA_SYNC,
+           "cluster": nb.NVFP4_PLAN_KERNEL_CLUSTER}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -63,7 +64,7 @@ def test_decode_table_exhaustive(kernel, out, M):
     assert bad.size == 0, [(int(m), hex(SCALE_BYTES[n]), got[m, n], want[m, n]) for m, n in bad[:8]]
 
 
-@pytest.mark.parametrize("kernel", list(KERNELS))
+@pytest.mark.parametrize("kernel", ["tcgen05", "mma"])
 @pytest.mark.parametrize("N,K,Ms", [(100000, 512, (1, 17)), (100000, 1024, (16, 32)), (2000, 32768, (1, 17))])
 def test_split_modes_every_element(kernel, N, K, Ms):
     """Many units per block (the tcgen05 kernel's two-launch mode), blocks covering up to three
@@ -77,6 +78,25 @@ def test_split_modes_every_element(kernel, N, K, Ms):
     case = Case(N, K, max(Ms), seed=N % 1000 + K, outlier_frac=0.01)
     y_ref, absdot = case.oracle_full()
     for M in Ms:
+        y = case.run(plan, M, x=case.d_x[:M].contiguous())
+        torch.cuda.synchronize()
+        ok, ratio = within_tolerance(to_f64(y), y_ref[:M], absdot[:M])
+        assert ok, (M, ratio)
+    assert nb.nvfp4_plan_check(plan) == nb.NVFP4_OK
+
+
+@pytest.mark.parametrize("N,K", [(5120, 5120), (4000, 6144), (2000, 3072), (999, 1536), (2500, 2048), (160, 1280)])
+def test_cluster_split_every_element(N, K):
+    """The cluster kernel's work split on every element: clusters of 8, 4 and 2 blocks (K / C of
+    6, 3, 3, 2, 1 and 5 units of 128), tiles shared by two or more warps, warps with no tile-unit,
+    panels of unequal tile counts and a ragged last tile."""
+    plan = nb.nvfp4_plan_create_flags(N, K, nb.NVFP4_OUT_BF16, nb.NVFP4_PLAN_KERNEL_CLUSTER)
+    info = nb.nvfp4_plan_get_info(plan)
+    assert info["kernel"] == nb.NVFP4_KERNEL_CLUSTER and info["launches_per_call"] == 1
+    assert K % (info["cluster_size"] * 128) == 0 and K // (info["cluster_size"] * 128) <= 6
+    case = Case(N, K, 32, seed=N % 1000 + K, outlier_frac=0.01)
+    y_ref, absdot = case.oracle_full()
+    for M in (1, 9, 17, 32):
         y = case.run(plan, M, x=case.d_x[:M].contiguous())
         torch.cuda.synchronize()
         ok, ratio = within_tolerance(to_f64(y), y_ref[:M], absdot[:M])

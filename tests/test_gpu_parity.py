@@ -22,15 +22,30 @@ def _built():
     torch.cuda.init()
 
 
-# both projection kernels: the default (tcgen05) and the register-direct mma.sync one
-KERNELS = {"tcgen05": nb.NVFP4_PLAN_KERNEL_TCGEN05, "mma": nb.NVFP4_PLAN_KERNEL_MMA_SYNC}
+# the three projection kernels: tcgen05, the register-direct mma.sync one and the cluster-split
+# mma.sync one (which takes only the shapes whose K splits over a cluster, see cluster_takes)
+KERNELS = {"tcgen05": nb.NVFP4_PLAN_KERNEL_TCGEN05, "mma": nb.NVFP4_PLAN_KERNEL_MMA_SYNC,
+           "cluster": nb.NVFP4_PLAN_KERNEL_CLUSTER}
 kernel_param = pytest.mark.parametrize("kernel", list(KERNELS))
+KERNEL_IDS = {"tcgen05": nb.NVFP4_KERNEL_TCGEN05, "mma": nb.NVFP4_KERNEL_MMA_SYNC, "cluster": nb.NVFP4_KERNEL_CLUSTER}
+
+
+def cluster_takes(N, K):
+    """Whether the cluster kernel plans (N, K): refused with NVFP4_ERR_SHAPE otherwise."""
+    try:
+        nb.nvfp4_plan_create_flags(N, K, nb.NVFP4_OUT_BF16, nb.NVFP4_PLAN_KERNEL_CLUSTER).destroy()
+        return True
+    except nb.Nvfp4Error as e:
+        assert e.status == nb.NVFP4_ERR_SHAPE
+        return False
 
 
 def _plan(N, K, f32=False, kernel=None):
     out = nb.NVFP4_OUT_F32 if f32 else nb.NVFP4_OUT_BF16
     if kernel is None:
         return nb.nvfp4_plan_create_ex(N, K, out)
+    if kernel == "cluster" and not cluster_takes(N, K):
+        pytest.skip("the cluster kernel does not take N=%d K=%d" % (N, K))
     return nb.nvfp4_plan_create_flags(N, K, out, KERNELS[kernel])
 
 
@@ -192,6 +207,8 @@ def test_back_to_back_different_plans(kernel):
     """Calls of several plans queued on one stream (the decode-round pattern) give the
     same bits as the same calls made one at a time."""
     shapes = [(7168, 5120), (5120, 5120), (34816, 5120), (5120, 17408)]
+    if kernel == "cluster":
+        shapes = [s for s in shapes if cluster_takes(*s)] + [(300, 768)]
     plans = [_plan(N, K, kernel=kernel) for N, K in shapes]
     cases = [Case(N, K, 16, seed=40 + i) for i, (N, K) in enumerate(shapes)]
     alone = []
@@ -369,6 +386,8 @@ def _sampled(case, plan, M, n_samples=384, seed=0):
 def test_full_size_workloads_sampled(wl, kernel):
     w = synth.WORKLOADS[wl]
     for pj in w.projections:
+        if kernel == "cluster" and not cluster_takes(pj.N, pj.K):
+            continue
         plan = _plan(pj.N, pj.K, pj.f32_out, kernel=kernel)
         x = synth.activations(32, pj.K, pj.seed, outlier_frac=w.outlier_frac)
         case = Case(pj.N, pj.K, 32, pj.seed, x=x)
@@ -389,6 +408,8 @@ def test_full_size_workloads_sampled(wl, kernel):
 def test_round_workload_first_layer_sampled(kernel):
     """The decode-round shapes with their per-(layer, projection) seeds, layer 0."""
     for pj in synth.WORKLOADS["round"].projections[:4]:
+        if kernel == "cluster" and not cluster_takes(pj.N, pj.K):
+            continue
         plan = _plan(pj.N, pj.K, kernel=kernel)
         case = Case(pj.N, pj.K, 32, pj.seed)
         _sampled(case, plan, 32, seed=pj.seed)
@@ -419,9 +440,17 @@ def test_argument_errors():
 @kernel_param
 def test_plan_info_independent_of_M(kernel):
     for N, K in [(5120, 5120), (152064, 5120), (256, 512), (5120, 17408)]:
+        if kernel == "cluster" and not cluster_takes(N, K):
+            continue
         info = nb.nvfp4_plan_get_info(_plan(N, K, kernel=kernel))
         assert info["N"] == N and info["K"] == K
-        assert info["kernel"] == (nb.NVFP4_KERNEL_TCGEN05 if kernel == "tcgen05" else nb.NVFP4_KERNEL_MMA_SYNC)
+        assert info["kernel"] == KERNEL_IDS[kernel]
+        if kernel == "cluster":  # clusters of C blocks over 16-row tiles, K / C per block
+            C = info["cluster_size"]
+            assert C in (2, 4, 8) and info["grid"] % C == 0 and info["grid"] <= 2 * info["sm_count"]
+            assert info["rows_per_block"] == 16 and info["row_blocks"] == -(-N // 16)
+            assert info["k_steps"] * info["k_step"] == K and info["launches_per_call"] == 1
+            continue
         assert info["row_blocks"] == -(-N // info["rows_per_block"])
         assert info["units"] == info["row_blocks"] * (K // info["k_step"])
         blocks_per_sm = 1 if kernel == "tcgen05" else 2  # the register-direct kernel runs two per SM
