@@ -369,7 +369,9 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM) gemv_kernel(const __gr
   if (p.weights_after_wait) prefetch();
 
   // The activation fragments of the unit at k-step ks into L1 (lane L: line L of each 4 KB
-  // n-tile run), so that the first warp to multiply it does not wait on L2 for each load.
+  // n-tile run), so that the first warp to multiply it does not wait on L2 for each load.  Only
+  // up to two n-tiles: with three or four, two units' runs of every k-slice outgrow the L1 left
+  // beside two blocks' stages and the prefetch evicts lines still in use (measured slower).
   constexpr int nt_stride = NT * 8 * 32;  // uint4 per 256-k step of x16
   auto prefetch_x = [&](int ks) {
     const uint8_t* base = reinterpret_cast<const uint8_t*>(p.x16 + (int64_t)(ks * p.wk + wk_i) * nt_stride);
@@ -378,8 +380,8 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM) gemv_kernel(const __gr
   };
   {
     const int ks0 = (int)(u_begin - (int64_t)rb_first * S);
-    if (n_local > 0) prefetch_x(ks0);
-    if (n_local > 1) prefetch_x((ks0 + 1) % S32);
+    if (n_local > 0 && NT <= 2) prefetch_x(ks0);
+    if (n_local > 1 && NT <= 2) prefetch_x((ks0 + 1) % S32);
   }
 
   float acc[kTilesPerWarp][NT][4];
@@ -546,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM) gemv_kernel(const __gr
     mma_unit<NT>(acc, stage + (uint32_t)(lane * 16), stage + kStageCodeBytes + s_off, s_sh, xq);
     __syncwarp();              // every lane has read the stage (a quad shares its scale words)
     issue_next(i + depth);     // into the stage just read
-    if (i + 2 < n_local) prefetch_x((c_ks + 2) % S32);
+    if (NT <= 2 && i + 2 < n_local) prefetch_x((c_ks + 2) % S32);
     if (pend_rb >= 0) finish_pending();
     if (c_ks == S32 - 1 || i == n_local - 1) {
       flush(c_rb, seg_ks0 == 0 && c_ks == S32 - 1);
