@@ -49,6 +49,20 @@ int nvfp4_unpack_codes(const uint8_t* packed, int64_t N, int64_t K, uint8_t* cod
  * saturates to 448 like any value above it. */
 int nvfp4_e4m3_encode(const float* s, int64_t n, uint8_t* out, int64_t* bad_index);
 
+/* Quantize a BF16 weight w[rows, ldw] (its first K columns, bfloat16 bits) to NVFP4 on the host:
+ * codes[rows, K/2] (E2M1, low nibble = even k) and scales[rows, K/16] (E4M3), with per-tensor
+ * scale w_global_scale ("Module ops", quantize_bf16_to_nvfp4: packed E2M1 [M, K/2] and one E4M3
+ * scale per 16 elements [M, K/16]; the pages fix scale2 = 1.0 there and print no rounding rule).
+ * The rule is the plainest reading, the same as nvfp4_quantize_bf16 on the device, bit for bit:
+ * per 16-element block, scale = E4M3(amax / 6 / gs), then code = E2M1(x / (scale_value * gs)),
+ * each to the nearest value with ties to even, saturating at 448 and 6; every step an fp32
+ * operation rounded to nearest; a zero scale gives codes 0 and a code of magnitude 0 is +0.
+ * K must be a positive multiple of 16 and ldw >= K.  Returns NVFP4_PACK_ERR_ARG for a null
+ * pointer or a bad shape, NVFP4_PACK_ERR_VALUE unless 0 < w_global_scale < inf; the outputs are
+ * untouched then. */
+int nvfp4_quantize_bf16_host(const uint16_t* w, int64_t rows, int64_t K, int64_t ldw, float w_global_scale,
+                             uint8_t* codes, uint8_t* scales);
+
 #ifdef __cplusplus
 }
 #endif

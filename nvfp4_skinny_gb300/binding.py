@@ -50,7 +50,7 @@ CUDA_SYMBOLS = ("nvfp4_status_string", "nvfp4_abi_version", "nvfp4_plan_create",
 PREFILL_SYMBOLS = ("nvfp4_prefill_geometry", "nvfp4_prefill_plan_create", "nvfp4_prefill_plan_destroy",
                    "nvfp4_prefill_linear", "nvfp4_prefill_linear_ex", "nvfp4_prefill_plan_check",
                    "nvfp4_prefill_plan_get_info")
-PACK_SYMBOLS = ("nvfp4_pack_codes", "nvfp4_unpack_codes", "nvfp4_e4m3_encode")
+PACK_SYMBOLS = ("nvfp4_pack_codes", "nvfp4_unpack_codes", "nvfp4_e4m3_encode", "nvfp4_quantize_bf16_host")
 NVFP4_PREFILL_MAX_ROWS = 65536
 
 
@@ -164,6 +164,8 @@ def pack_lib():
         lib.nvfp4_unpack_codes.argtypes = [p, i64, i64, p]
         lib.nvfp4_e4m3_encode.restype = ctypes.c_int
         lib.nvfp4_e4m3_encode.argtypes = [p, i64, p, ctypes.POINTER(i64)]
+        lib.nvfp4_quantize_bf16_host.restype = ctypes.c_int
+        lib.nvfp4_quantize_bf16_host.argtypes = [p, i64, i64, i64, ctypes.c_float, p, p]
         _pack = lib
     return _pack
 
@@ -460,3 +462,21 @@ def nvfp4_e4m3_encode(scales):
     if st != NVFP4_PACK_OK:
         raise ValueError("nvfp4_e4m3_encode refused element %d (status %d)" % (bad.value, st))
     return out
+
+
+def nvfp4_quantize_bf16_host(w_bits, K=None, w_global_scale=1.0):
+    """uint16 [rows, ldw] bfloat16 bits (the first K columns are the weight) -> (codes uint8
+    [rows, K/2], scales uint8 [rows, K/16]) on the host.  A refused call raises ValueError with
+    the library's status in its `status` attribute."""
+    w = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    rows, ldw = w.shape
+    K = ldw if K is None else int(K)
+    codes = np.zeros((rows, max(K, 0) // 2), np.uint8)
+    scales = np.zeros((rows, max(K, 0) // 16), np.uint8)
+    st = pack_lib().nvfp4_quantize_bf16_host(w.ctypes.data, rows, K, ldw, float(w_global_scale), codes.ctypes.data,
+                                              scales.ctypes.data)
+    if st != NVFP4_PACK_OK:
+        err = ValueError("nvfp4_quantize_bf16_host refused the call (status %d)" % st)
+        err.status = st
+        raise err
+    return codes, scales

@@ -59,7 +59,7 @@ def build_pack(force=False):
         return PACK_LIB
     os.makedirs(OUT, exist_ok=True)
     tmp = PACK_LIB + ".tmp%d" % os.getpid()
-    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-I", INCLUDE,
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-I", INCLUDE,
                     os.path.join(CSRC, "nvfp4_pack.c"), "-o", tmp, "-lm"], check=True)
     os.replace(tmp, PACK_LIB)
     return PACK_LIB

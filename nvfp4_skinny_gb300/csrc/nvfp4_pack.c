@@ -1,6 +1,9 @@
 /*
- * Host-side NVFP4 packer: E2M1 nibble packing and E4M3 block-scale encoding.
- * The layout and the refusals are described in include/nvfp4_pack.h.
+ * Host-side NVFP4 packer: E2M1 nibble packing, E4M3 block-scale encoding and the BF16 -> NVFP4
+ * weight quantizer.  The layout, the rounding rules and the refusals are described in
+ * include/nvfp4_pack.h.  Every floating-point step is one IEEE fp32 operation rounded to
+ * nearest (no step has the form a * b + c, so no contraction to a fused multiply-add can change
+ * a result), the same sequence the device quantizer runs.
  */
 #include "nvfp4_pack.h"
 
@@ -56,6 +59,58 @@ int nvfp4_e4m3_encode(const float* s, int64_t n, uint8_t* out, int64_t* bad_inde
       return NVFP4_PACK_ERR_VALUE;
     }
     out[i] = e4m3_from_nonneg(f);
+  }
+  return NVFP4_PACK_OK;
+}
+
+/* E4M3FN byte 0x00..0x7E -> its value, exactly: m 2^-9 for e = 0, (8 + m) 2^(e - 10) otherwise. */
+static float e4m3_value(uint8_t c) {
+  const int e = c >> 3, m = c & 7;
+  return e == 0 ? ldexpf((float)m, -9) : ldexpf((float)(8 + m), e - 10);
+}
+
+/* E2M1 magnitude code of v >= 0 (or NaN: code 0): nearest of {0, 0.5, 1, 1.5, 2, 3, 4, 6}, ties
+ * to the even code, saturating at 6.  Each comparison is the decision at one midpoint: 0.25, 1.25,
+ * 2.5 and 5 go down to the even code below, 0.75, 1.75 and 3.5 up to the even code above. */
+static uint8_t e2m1_magnitude(float v) {
+  return (uint8_t)((v > 0.25f) + (v >= 0.75f) + (v > 1.25f) + (v >= 1.75f) + (v > 2.5f) + (v >= 3.5f) + (v > 5.0f));
+}
+
+int nvfp4_quantize_bf16_host(const uint16_t* w, int64_t rows, int64_t K, int64_t ldw, float w_global_scale,
+                             uint8_t* codes, uint8_t* scales) {
+  if (!w || !codes || !scales || rows < 1 || K < 16 || K % 16 != 0 || ldw < K) return NVFP4_PACK_ERR_ARG;
+  if (!(w_global_scale > 0.0f) || !(w_global_scale < INFINITY)) return NVFP4_PACK_ERR_VALUE;
+  const int64_t nb = K / 16;
+  for (int64_t n = 0; n < rows; ++n) {
+    for (int64_t b = 0; b < nb; ++b) {
+      const uint16_t* src = w + n * ldw + b * 16;
+      float x[16];
+      float amax = 0.0f;
+      for (int i = 0; i < 16; ++i) {
+        union {
+          uint32_t u;
+          float f;
+        } cv;
+        cv.u = (uint32_t)src[i] << 16;
+        x[i] = cv.f;
+        amax = fmaxf(amax, fabsf(x[i]));
+      }
+      const float s = (amax / 6.0f) / w_global_scale;
+      const uint8_t sc = e4m3_from_nonneg(s);
+      const float d = e4m3_value(sc) * w_global_scale;
+      uint8_t* out = codes + n * (K / 2) + b * 8;
+      for (int i = 0; i < 16; i += 2) out[i / 2] = 0;
+      for (int i = 0; i < 16; ++i) {
+        uint8_t c = 0;
+        if (d > 0.0f) {
+          const float q = x[i] / d;
+          c = e2m1_magnitude(fabsf(q));
+          if (c != 0 && q < 0.0f) c |= 8; /* a magnitude that rounds to zero is +0 */
+        }
+        out[i / 2] |= (uint8_t)(c << (4 * (i & 1)));
+      }
+      scales[n * nb + b] = sc;
+    }
   }
   return NVFP4_PACK_OK;
 }

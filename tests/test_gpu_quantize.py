@@ -53,6 +53,19 @@ def test_quantizer_matches_oracle_bitwise(gs, ldw_pad):
     assert np.array_equal(codes, codes_ref)
 
 
+@pytest.mark.parametrize("gs", [1.0, 0.0625, 7.5])
+def test_device_and_host_quantizers_agree_bitwise(gs):
+    """The device kernel and the packer library's host quantizer take every rounding decision
+    alike: the same codes and scales, byte for byte, on the special blocks and on random ones."""
+    w = _weights(257, 2048, seed=int(gs * 32) + 5)
+    codes, scales = _device_quantize(w, gs)
+    from nvfp4_skinny_gb300 import build
+    build.build_pack()
+    codes_h, scales_h = nb.nvfp4_quantize_bf16_host(bf16_bits(w), w_global_scale=gs)
+    assert np.array_equal(scales, scales_h)
+    assert np.array_equal(codes, codes_h)
+
+
 def test_quantizer_round_trip_of_representable_blocks():
     rng = np.random.default_rng(33)
     rows, K = 64, 512
