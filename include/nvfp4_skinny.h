@@ -130,6 +130,10 @@ int nvfp4_abi_version(void);
 #define NVFP4_PLAN_KERNEL_CLUSTER 8u        /* force the cluster-split mma.sync kernel; refused with
                                                NVFP4_ERR_SHAPE when K / 128 has no split over a
                                                cluster of 2, 4 or 8 blocks into at most 6 units each */
+#define NVFP4_PLAN_DUAL 16u                 /* two [N, K] weights over one input (nvfp4_skinny_linear_dual
+                                               only): the work split covers 2 N rows; runs the cluster
+                                               kernel where it takes (2 N, K), else the register-direct
+                                               one; refused with NVFP4_PLAN_KERNEL_TCGEN05 */
 
 /* Create a plan for an [N, K] weight with bfloat16 output.  The launch
  * configuration (kernel, rows per block, k-step, split of K across blocks, grid) is a
@@ -212,10 +216,56 @@ typedef struct {
  * nvfp4_skinny_linear on the same arguments. */
 nvfp4_status nvfp4_skinny_linear_grouped(nvfp4_plan_t plan, const nvfp4_group_item* items, int count, void* stream);
 
+/* Two projections of one input in one launch ("Module ops", w4a16_gemv_dual: two W4A16 GEMVs
+ * over the same BF16 input, each with n outputs): y0 = x . dequant(W0)^T * gs0 and
+ * y1 = x . dequant(W1)^T * gs1, each weight [N, K] in the layout above and each y [M, N] of the
+ * plan's output type.  Needs a plan created with NVFP4_PLAN_DUAL (and only such a plan takes it:
+ * the other entry points refuse dual plans with NVFP4_ERR_ARG).  The activations are prepared
+ * once; each output row's bits are a function of its weight row and x alone, so they do not
+ * depend on M or on the other weight. */
+nvfp4_status nvfp4_skinny_linear_dual(nvfp4_plan_t plan, const void* x, int M, const uint8_t* w0_codes,
+                                      const uint8_t* w0_block_scales, float w0_global_scale, void* y0,
+                                      const uint8_t* w1_codes, const uint8_t* w1_block_scales, float w1_global_scale,
+                                      void* y1, void* stream);
+
+/* nvfp4_skinny_linear for a weight whose rows interleave `parts` (2..4) parts per group, part q
+ * having part_rows[q] rows ("Module ops", w4a16_gemv_qg: Q and gate rows per head, output
+ * [Q of all heads | gate of all heads]; w4a16_gemv_qkvz: Q, K, V and Z rows per group, output
+ * [Q | K | V | Z]): weight row g * S + off_q + r (S = the sum of part_rows, off_q the rows of
+ * the parts before q, r < part_rows[q]) is stored at output column (N / S) * off_q +
+ * g * part_rows[q] + r.  N must be a multiple of S (else NVFP4_ERR_SHAPE); part_rows[q] >= 1
+ * (else NVFP4_ERR_ARG).  The values are those of the plain call, only stored elsewhere. */
+nvfp4_status nvfp4_skinny_linear_deinterleaved(nvfp4_plan_t plan, const void* x, int M, const uint8_t* w_codes,
+                                               const uint8_t* w_block_scales, float w_global_scale, void* y, int parts,
+                                               const int32_t* part_rows, void* stream);
+
+/* Grouped experts over device tables ("Module ops", Nvfp4ExpertTables: device tables of each
+ * expert's packed and block-scale pointers, and its per-tensor scales as f32).  Every member
+ * is a DEVICE array of `count` entries (the struct itself is read on the host); the tables may be
+ * written by kernels earlier on the stream (they are read after those finish). */
+typedef struct {
+  const uint8_t* const* w_codes;        /* [count] device pointers to [N, K/2] codes */
+  const uint8_t* const* w_block_scales; /* [count] device pointers to [N, K/16] E4M3 scales */
+  const float* w_global_scales;         /* [count] per-tensor scales */
+  const void* const* x;                 /* [count] device pointers to bf16 [M_e, K] activations */
+  const int32_t* M;                     /* [count] activation rows M_e, 0..max_M */
+  void* const* y;                       /* [count] device pointers to [M_e, N] outputs (plan's type) */
+} nvfp4_expert_tables;
+
+/* y_e = x_e . dequant(W_e)^T * gs_e for every entry e of `tables`, all experts in ONE launch
+ * (one grid row per entry, each computed exactly as a single call of this plan, so its bits
+ * equal nvfp4_skinny_linear's).  Needs a cluster-kernel plan (NVFP4_PLAN_KERNEL_CLUSTER; others:
+ * NVFP4_ERR_ARG), 1 <= count <= 65535 and 1 <= max_M <= 32.  Every pointer in the tables must be
+ * 16-byte aligned (not checked: the tables live on the device).  An entry whose M_e is outside
+ * 0..max_M is skipped (its y untouched) and nvfp4_plan_check then returns NVFP4_ERR_M_RANGE; an
+ * entry with M_e = 0 writes nothing. */
+nvfp4_status nvfp4_skinny_linear_grouped_tables(nvfp4_plan_t plan, const nvfp4_expert_tables* tables, int count,
+                                                int max_M, void* stream);
+
 /* Synchronize `stream`, then read and clear the plan's device error word.
- * Returns NVFP4_OK, NVFP4_ERR_TIMEOUT, or NVFP4_ERR_CUDA if the stream
- * reported an error.  (The mma.sync kernel has no in-kernel wait, so its plans
- * only ever report NVFP4_OK or NVFP4_ERR_CUDA.) */
+ * Returns NVFP4_OK, NVFP4_ERR_TIMEOUT (a bounded in-kernel wait ran out), NVFP4_ERR_M_RANGE (a
+ * grouped-table entry's M was outside 0..max_M), or NVFP4_ERR_CUDA if the stream reported an
+ * error.  (The mma.sync kernels have no in-kernel wait: their plans never report a timeout.) */
 nvfp4_status nvfp4_plan_check(nvfp4_plan_t plan, void* stream);
 
 /* Description of a plan's launch configuration (for tests and benchmarks). */

@@ -37,6 +37,7 @@ NVFP4_PLAN_KERNEL_TCGEN05 = 1
 NVFP4_PLAN_KERNEL_MMA_SYNC = 2
 NVFP4_PLAN_WEIGHTS_AFTER_WAIT = 4
 NVFP4_PLAN_KERNEL_CLUSTER = 8
+NVFP4_PLAN_DUAL = 16
 
 NVFP4_PACK_OK = 0
 NVFP4_PACK_ERR_ARG = -1
@@ -46,7 +47,8 @@ NVFP4_PACK_ERR_VALUE = -2
 CUDA_SYMBOLS = ("nvfp4_status_string", "nvfp4_abi_version", "nvfp4_plan_create", "nvfp4_plan_create_ex",
                 "nvfp4_plan_create_flags", "nvfp4_plan_destroy", "nvfp4_skinny_linear", "nvfp4_plan_check", "nvfp4_plan_get_info",
                 "nvfp4_skinny_linear_noalloc", "nvfp4_noalloc_check", "nvfp4_skinny_linear_strided", "nvfp4_skinny_linear_silu_mul",
-                "nvfp4_quantize_bf16", "nvfp4_skinny_linear_grouped")
+                "nvfp4_quantize_bf16", "nvfp4_skinny_linear_grouped", "nvfp4_skinny_linear_dual",
+                "nvfp4_skinny_linear_deinterleaved", "nvfp4_skinny_linear_grouped_tables")
 PREFILL_SYMBOLS = ("nvfp4_prefill_geometry", "nvfp4_prefill_plan_create", "nvfp4_prefill_plan_destroy",
                    "nvfp4_prefill_linear", "nvfp4_prefill_linear_ex", "nvfp4_prefill_plan_check",
                    "nvfp4_prefill_plan_get_info")
@@ -76,6 +78,12 @@ class PlanInfo(ctypes.Structure):
                 ("units", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64), ("smem_bytes", ctypes.c_int64),
                 ("launches_per_call", ctypes.c_int32), ("kernel", ctypes.c_int32), ("warps_rows", ctypes.c_int32),
                 ("warps_k", ctypes.c_int32), ("flags", ctypes.c_uint32), ("cluster_size", ctypes.c_int32)]
+
+
+class ExpertTables(ctypes.Structure):
+    """nvfp4_expert_tables: six DEVICE arrays of `count` entries each."""
+    _fields_ = [("w_codes", ctypes.c_void_p), ("w_block_scales", ctypes.c_void_p), ("w_global_scales", ctypes.c_void_p),
+                ("x", ctypes.c_void_p), ("M", ctypes.c_void_p), ("y", ctypes.c_void_p)]
 
 
 class PrefillInfo(ctypes.Structure):
@@ -128,6 +136,13 @@ def cuda_lib():
         lib.nvfp4_skinny_linear_silu_mul.argtypes = [p, p, i64, i32, p, p, ctypes.c_float, p, i64, p]
         lib.nvfp4_skinny_linear_grouped.restype = i32
         lib.nvfp4_skinny_linear_grouped.argtypes = [p, ctypes.POINTER(GroupItem), i32, p]
+        lib.nvfp4_skinny_linear_dual.restype = i32
+        lib.nvfp4_skinny_linear_dual.argtypes = [p, p, i32, p, p, ctypes.c_float, p, p, p, ctypes.c_float, p, p]
+        lib.nvfp4_skinny_linear_deinterleaved.restype = i32
+        lib.nvfp4_skinny_linear_deinterleaved.argtypes = [p, p, i32, p, p, ctypes.c_float, p, i32,
+                                                          ctypes.POINTER(ctypes.c_int32), p]
+        lib.nvfp4_skinny_linear_grouped_tables.restype = i32
+        lib.nvfp4_skinny_linear_grouped_tables.argtypes = [p, ctypes.POINTER(ExpertTables), i32, i32, p]
         lib.nvfp4_quantize_bf16.restype = i32
         lib.nvfp4_quantize_bf16.argtypes = [p, i64, i64, i64, ctypes.c_float, p, p, p]
         lib.nvfp4_skinny_linear_noalloc.restype = i32
@@ -304,6 +319,43 @@ def nvfp4_skinny_linear_grouped(plan, items, stream=None, check=True):
                                                 len(items), _stream(stream))
     if check:
         _check(st, "nvfp4_skinny_linear_grouped")
+    return st
+
+
+def nvfp4_skinny_linear_dual(plan, x, M, w0, w1, y0, y1, stream=None, check=True):
+    """Two projections of one input in one launch on a NVFP4_PLAN_DUAL plan: w0 and w1 are
+    (codes, block_scales, global_scale) triples, y0 and y1 their [M, N] outputs."""
+    (c0, s0, g0), (c1, s1, g1) = w0, w1
+    st = cuda_lib().nvfp4_skinny_linear_dual(plan.as_parameter if isinstance(plan, Plan) else plan, _ptr(x), int(M),
+                                             _ptr(c0), _ptr(s0), float(g0), _ptr(y0), _ptr(c1), _ptr(s1), float(g1),
+                                             _ptr(y1), _stream(stream))
+    if check:
+        _check(st, "nvfp4_skinny_linear_dual")
+    return st
+
+
+def nvfp4_skinny_linear_deinterleaved(plan, x, M, w_codes, w_block_scales, w_global_scale, y, part_rows, stream=None,
+                                      check=True):
+    """The projection of a weight whose rows interleave len(part_rows) parts per group, stored
+    part-major (Q | gate, or Q | K | V | Z)."""
+    rows = (ctypes.c_int32 * len(part_rows))(*[int(r) for r in part_rows])
+    st = cuda_lib().nvfp4_skinny_linear_deinterleaved(plan.as_parameter if isinstance(plan, Plan) else plan, _ptr(x),
+                                                      int(M), _ptr(w_codes), _ptr(w_block_scales),
+                                                      float(w_global_scale), _ptr(y), len(part_rows), rows,
+                                                      _stream(stream))
+    if check:
+        _check(st, "nvfp4_skinny_linear_deinterleaved")
+    return st
+
+
+def nvfp4_skinny_linear_grouped_tables(plan, tables, count, max_M, stream=None, check=True):
+    """Grouped experts in one launch; `tables` maps the six field names of nvfp4_expert_tables to
+    device tensors (int64 pointer arrays, float32 scales, int32 row counts)."""
+    t = ExpertTables(*[_ptr(tables[f]) for f, _ in ExpertTables._fields_])
+    st = cuda_lib().nvfp4_skinny_linear_grouped_tables(plan.as_parameter if isinstance(plan, Plan) else plan,
+                                                       ctypes.byref(t), int(count), int(max_M), _stream(stream))
+    if check:
+        _check(st, "nvfp4_skinny_linear_grouped_tables")
     return st
 
 

@@ -70,9 +70,28 @@ struct Params {
   int64_t lda;
   void* y;                // [M, ldc] bf16 or f32
   int64_t ldc;
-  int64_t N, K;
+  int64_t N, K;           // N: every row of the launch (both weights of a dual call)
   float gs;
   int M;
+  // a second weight over the same activations ("Module ops", w4a16_gemv_dual): rows n >= n1
+  // are its rows n - n1, with their own scale and output (n1 >= N: none)
+  const uint8_t* codes1;
+  const uint8_t* scales1;
+  void* y1;
+  float gs1;
+  int64_t n1;
+  RowMap rmap;            // where each output row is stored (deinterleaved weights)
+  // grouped experts over device tables ("Module ops", Nvfp4ExpertTables): blockIdx.y picks
+  // entry e; its weight, scale, activations, rows and output replace the fields above
+  int grouped;
+  int group_count;        // gridDim.y of a grouped launch
+  int* err;               // the plan's error word: kErrMRange when an entry's rows are not in 0..M
+  const uint8_t* const* g_codes;
+  const uint8_t* const* g_scales;
+  const float* g_gs;
+  const uint16_t* const* g_x;
+  void* const* g_y;
+  const int* g_M;
   int out_f32;
   int silu_mul;
   int weights_after_wait;  // 1: no weight byte is read before the dependency wait
@@ -143,6 +162,14 @@ __global__ void __launch_bounds__(kThreads, 2) cluster_kernel(const __grid_const
 
   const int64_t code_row = p.K / 2, scale_row = p.K / 16;
   const uint64_t pol = ptx::policy_evict_first();
+  // this launch row's weight, activations and output (a grouped call reads them from its tables,
+  // which may be written upstream: after the dependency wait)
+  const uint8_t* codes = p.codes;
+  const uint8_t* scales = p.scales;
+  const uint16_t* xg = p.x;
+  void* yg = p.y;
+  float gs = p.gs;
+  int M = p.M;
 
   // tile-unit l_v (local tile l_v / Uk, k-unit l_v % Uk) into stage l_st: rows past N read
   // nothing (zeros); one commit group per call either way
@@ -155,11 +182,12 @@ __global__ void __launch_bounds__(kThreads, 2) cluster_kernel(const __grid_const
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int64_t n = (int64_t)(T0 + j) * 16 + g + 8 * h;
-        const bool ok = n < p.N;
-        const uint8_t* cs = ok ? p.codes + n * code_row + kb / 2 + t * 16 : p.codes;
+        const bool ok = n < p.N, sec = n >= p.n1;
+        const int64_t nr = sec ? n - p.n1 : n;  // the row within its weight
+        const uint8_t* cs = ok ? (sec ? p.codes1 : codes) + nr * code_row + kb / 2 + t * 16 : codes;
         gemv::cp_async16_z(st + (uint32_t)(h * 512 + lane * 16), cs, ok ? 16u : 0u, pol);
         if (t == 0) {
-          const uint8_t* ss = ok ? p.scales + n * scale_row + kb / 16 : p.scales;
+          const uint8_t* ss = ok ? (sec ? p.scales1 : scales) + nr * scale_row + kb / 16 : scales;
           cp_async8_z(st + (uint32_t)(kStageCodeBytes + h * 64 + g * 8), ss, ok ? 8u : 0u, pol);
         }
       }
@@ -169,11 +197,25 @@ __global__ void __launch_bounds__(kThreads, 2) cluster_kernel(const __grid_const
     ptx::cp_async_commit();
   };
 
-  if (!p.weights_after_wait)
+  const bool early = !p.weights_after_wait && !p.grouped;  // weights before the wait
+  if (early)
     for (int j = 0; j < depth; ++j) issue_next();
   ptx::grid_launch_dependents();
-  ptx::grid_dependency_wait();  // the activations are produced upstream
-  if (p.weights_after_wait)
+  ptx::grid_dependency_wait();  // the activations (and a grouped call's tables) are produced upstream
+  if (p.grouped) {
+    const int e = blockIdx.y;
+    codes = p.g_codes[e];
+    scales = p.g_scales[e];
+    xg = p.g_x[e];
+    yg = p.g_y[e];
+    gs = p.g_gs[e];
+    M = p.g_M[e];
+    if (M < 0 || M > p.M) {  // p.M: the launch's most rows; the entry is skipped and reported
+      if (threadIdx.x == 0 && rank == 0) atomicOr(p.err, kErrMRange);
+      M = 0;
+    }
+  }
+  if (!early)
     for (int j = 0; j < depth; ++j) issue_next();
 
   // ---- activations: warp w owns rows m = w + 8 j (n-tile j); lane l holds chunks l, l + 32, l + 64
@@ -190,13 +232,13 @@ __global__ void __launch_bounds__(kThreads, 2) cluster_kernel(const __grid_const
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int m = nt * 8 + warp;
-      const uint4* row = reinterpret_cast<const uint4*>(p.x + (int64_t)(m < p.M ? m : 0) * p.lda + k0);
-      const uint4* urow = reinterpret_cast<const uint4*>(p.x + (int64_t)(m < p.M ? m : 0) * p.lda + p.K + k0);
+      const uint4* row = reinterpret_cast<const uint4*>(xg + (int64_t)(m < M ? m : 0) * p.lda + k0);
+      const uint4* urow = reinterpret_cast<const uint4*>(xg + (int64_t)(m < M ? m : 0) * p.lda + p.K + k0);
 #pragma unroll
       for (int q = 0; q < kXPerLane; ++q) {
         const int c = lane + 32 * q;
         xv[nt][q] = make_uint4(0u, 0u, 0u, 0u);
-        if (m < p.M && c < chunks)
+        if (m < M && c < chunks)
           xv[nt][q] = p.silu_mul ? bf16x8_silu_mul(__ldg(row + c), __ldg(urow + c)) : __ldg(row + c);
       }
     }
@@ -208,14 +250,14 @@ __global__ void __launch_bounds__(kThreads, 2) cluster_kernel(const __grid_const
       for (int q = 0; q < kXPerLane; ++q) mx = max(mx, bf16x8_maxmag(xv[nt][q]));
       mx = warp_max_u32(mx);
       const int e = x_exponent(__uint_as_float(mx << 16));  // -112 <= e <= 148 for bf16 data
-      if (lane == 0) xs[m] = m < p.M ? pow2i(-(e / 2)) * pow2i(-(e - e / 2)) : 0.f;  // 2^-e, exact
+      if (lane == 0) xs[m] = m < M ? pow2i(-(e / 2)) * pow2i(-(e - e / 2)) : 0.f;  // 2^-e, exact
       const float f1 = pow2i(e <= 127 ? e : e / 2), f2 = pow2i(e <= 127 ? 0 : e - e / 2);
 #pragma unroll
       for (int q = 0; q < kXPerLane; ++q) {
         const int c = lane + 32 * q;
         if (c < chunks)  // rows past M stay zero
           *reinterpret_cast<uint4*>(x_slot(nt, c)) =
-              m >= p.M ? xv[nt][q] : (e <= 127 ? bf16x8_to_f16x8(xv[nt][q], f1) : bf16x8_to_f16x8(xv[nt][q], f1, f2));
+              m >= M ? xv[nt][q] : (e <= 127 ? bf16x8_to_f16x8(xv[nt][q], f1) : bf16x8_to_f16x8(xv[nt][q], f1, f2));
       }
     }
   }
@@ -335,18 +377,22 @@ __global__ void __launch_bounds__(kThreads, 2) cluster_kernel(const __grid_const
     for (int h = 0; h < 2; ++h) {
       const int64_t n = (int64_t)(T0 + j) * 16 + g + 8 * h;
       if (n >= p.N) continue;
+      const bool sec = n >= p.n1;
+      const int64_t no = map_row(p.rmap, sec ? n - p.n1 : n);  // the row's place in its output
+      void* yb = sec ? p.y1 : yg;
+      const float gsr = sec ? p.gs1 : gs;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const int m = nt * 8 + 2 * t + c;
-          if (m >= p.M) continue;
+          if (m >= M) continue;
           const float s = h == 0 ? (c == 0 ? sum[nt].x : sum[nt].y) : (c == 0 ? sum[nt].z : sum[nt].w);
-          const float val = __fmul_rn(s, p.gs);
+          const float val = __fmul_rn(s, gsr);
           if (p.out_f32)
-            static_cast<float*>(p.y)[(int64_t)m * p.ldc + n] = val;
+            static_cast<float*>(yb)[(int64_t)m * p.ldc + no] = val;
           else
-            static_cast<uint16_t*>(p.y)[(int64_t)m * p.ldc + n] = ptx::f32_to_bf16_rn(val);
+            static_cast<uint16_t*>(yb)[(int64_t)m * p.ldc + no] = ptx::f32_to_bf16_rn(val);
         }
     }
   }

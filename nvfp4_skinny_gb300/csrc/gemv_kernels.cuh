@@ -99,6 +99,14 @@ struct Params {
   int wr, wk, wk_shift;
   int depth;               // shared-memory stages per warp, 2..kMaxDepth
   int weights_after_wait;  // 1: no weight byte is read before the dependency wait
+  // a second weight over the same activations ("Module ops", w4a16_gemv_dual): rows n >= n1 are
+  // its rows n - n1, with their own scale and output (n1 >= N: none)
+  const uint8_t* codes1;
+  const uint8_t* scales1;
+  void* y1;
+  float gs1;
+  int64_t n1;
+  RowMap rmap;             // where each output row is stored (deinterleaved weights)
 };
 
 // ------------------------------------------------------------------ copies into the stage ring
@@ -297,31 +305,35 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM) gemv_kernel(const __gr
   // Unit (rb, ks) of the lane's rows into stage st: [row][half][lane] codes and [row][lane]
   // scale words.  A row block is full unless it is the last one and N is not a multiple of its
   // rows; only then are the rows checked (rows past N are zero-filled and read nothing).
-  const int64_t row8_codes = 8 * code_row, row8_scales = 8 * scale_row;
   const int64_t last_full = (p.N / row_block_rows) - 1;  // row blocks up to this one are full
+  // the first code and scale byte of launch row n (a dual call's second weight from row n1 on)
+  auto code_row_ptr = [&](int64_t n) { return n >= p.n1 ? p.codes1 + (n - p.n1) * code_row : p.codes + n * code_row; };
+  auto scale_row_ptr = [&](int64_t n) {
+    return n >= p.n1 ? p.scales1 + (n - p.n1) * scale_row : p.scales + n * scale_row;
+  };
   auto issue_unit = [&](int rb, int ks, int st) {
     const int q = ks * p.wk + wk_i;  // 256-k step
     const int64_t n0 = (int64_t)rb * row_block_rows + n_lane;
-    const uint8_t* cp = p.codes + n0 * code_row + q * kUnitCodeBytes + t * 16;
-    const uint8_t* sp = p.scales + n0 * scale_row + q * kUnitScaleBytes;
     const uint32_t cd = ring + (uint32_t)(st * kStageBytes) + (uint32_t)(lane * 16);
     const uint32_t sd = ring + (uint32_t)(st * kStageBytes + kStageCodeBytes) + (uint32_t)(g * 16);
     if (rb <= last_full) {
 #pragma unroll
       for (int rh = 0; rh < 4; ++rh) {  // (tile, half) = (rh / 2, rh % 2): row n0 + 8 rh
-        const uint8_t* c = cp + rh * row8_codes;
+        const uint8_t* c = code_row_ptr(n0 + 8 * rh) + q * kUnitCodeBytes + t * 16;
         cp_async16_z(cd + rh * 1024, c, 16u, pol);
         cp_async16_z(cd + rh * 1024 + 512, c + 64, 16u, pol);
-        if (t == 0) cp_async16_z(sd + rh * 128, sp + rh * row8_scales, 16u, pol);
+        if (t == 0) cp_async16_z(sd + rh * 128, scale_row_ptr(n0 + 8 * rh) + q * kUnitScaleBytes, 16u, pol);
       }
     } else {
 #pragma unroll
       for (int rh = 0; rh < 4; ++rh) {
         const bool ok = n0 + 8 * rh < p.N;
-        const uint8_t* c = ok ? cp + rh * row8_codes : p.codes;
+        const uint8_t* c = ok ? code_row_ptr(n0 + 8 * rh) + q * kUnitCodeBytes + t * 16 : p.codes;
         cp_async16_z(cd + rh * 1024, c, ok ? 16u : 0u, pol);
         cp_async16_z(cd + rh * 1024 + 512, c + 64, ok ? 16u : 0u, pol);
-        if (t == 0) cp_async16_z(sd + rh * 128, ok ? sp + rh * row8_scales : p.scales, ok ? 16u : 0u, pol);
+        if (t == 0)
+          cp_async16_z(sd + rh * 128, ok ? scale_row_ptr(n0 + 8 * rh) + q * kUnitScaleBytes : p.scales,
+                       ok ? 16u : 0u, pol);
       }
     }
   };
@@ -350,8 +362,8 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM) gemv_kernel(const __gr
     const int64_t n = (int64_t)rb * row_block_rows + (int64_t)wr_i * kWarpRows + lane;
     if (n >= p.N) return;
     const int cnt = min(j1 - j0, S32 - ks);  // units of this row block
-    const uint8_t* crow = p.codes + n * code_row;
-    const uint8_t* srow = p.scales + n * scale_row;
+    const uint8_t* crow = code_row_ptr(n);
+    const uint8_t* srow = scale_row_ptr(n);
     if (p.wk == 1) {
       prefetch_l2_bulk(crow + (int64_t)ks * kUnitCodeBytes, (uint32_t)(cnt * kUnitCodeBytes));
       prefetch_l2_bulk(srow + (int64_t)ks * kUnitScaleBytes, (uint32_t)(cnt * kUnitScaleBytes));
@@ -404,17 +416,21 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM) gemv_kernel(const __gr
       for (int h = 0; h < 2; ++h) {
         const int64_t n = n0 + 16 * r + 8 * h;
         if (n >= p.N) continue;
+        const bool sec = n >= p.n1;
+        const int64_t no = map_row(p.rmap, sec ? n - p.n1 : n);  // the row's place in its output
+        void* yb = sec ? p.y1 : p.y;
+        const float gsr = sec ? p.gs1 : p.gs;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             const int m = nt * 8 + 2 * t + c;
             if (m >= p.M) continue;
-            const float val = __fmul_rn(v[r][nt][2 * h + c], p.gs);
+            const float val = __fmul_rn(v[r][nt][2 * h + c], gsr);
             if (p.out_f32)
-              static_cast<float*>(p.y)[(int64_t)m * p.ldc + n] = val;
+              static_cast<float*>(yb)[(int64_t)m * p.ldc + no] = val;
             else
-              static_cast<uint16_t*>(p.y)[(int64_t)m * p.ldc + n] = ptx::f32_to_bf16_rn(val);
+              static_cast<uint16_t*>(yb)[(int64_t)m * p.ldc + no] = ptx::f32_to_bf16_rn(val);
           }
       }
   };

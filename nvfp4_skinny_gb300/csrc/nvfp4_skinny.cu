@@ -21,7 +21,7 @@ namespace {
 
 constexpr int kAbiVersion = 4;
 constexpr uint32_t kKernelFlags = NVFP4_PLAN_KERNEL_TCGEN05 | NVFP4_PLAN_KERNEL_MMA_SYNC | NVFP4_PLAN_KERNEL_CLUSTER;
-constexpr uint32_t kKnownFlags = kKernelFlags | NVFP4_PLAN_WEIGHTS_AFTER_WAIT;
+constexpr uint32_t kKnownFlags = kKernelFlags | NVFP4_PLAN_WEIGHTS_AFTER_WAIT | NVFP4_PLAN_DUAL;
 
 struct Workspace {
   float* partials = nullptr; // tcgen05: [2 * grid][32][256]; mma.sync: [2 * grid][wr] parts of 4 KB
@@ -49,6 +49,27 @@ struct ClusterGeometry {
   bool ok = false;
   int C = 0, clusters = 0, units_k = 0, tiles = 0, tiles_max = 0;
   int depth[nvfp4::cluster::kMaxNT + 1] = {0};  // stages per warp by n-tiles (1..4): scheduling only
+};
+
+// What a call adds to the plain projection: a second weight over the same activations (rows N..2N-1
+// of a dual plan's launch) and the order in which output rows are stored.
+struct CallExtras {
+  const uint8_t* codes1 = nullptr;
+  const uint8_t* scales1 = nullptr;
+  void* y1 = nullptr;
+  float gs1 = 0.f;
+  nvfp4::RowMap rmap = {0, 1, {0, 0, 0, 0}, 0};
+};
+
+// Grouped experts over device tables (the cluster kernel only): blockIdx.y picks an entry.
+struct GroupTables {
+  const uint8_t* const* codes = nullptr;
+  const uint8_t* const* scales = nullptr;
+  const float* gs = nullptr;
+  const uint16_t* const* x = nullptr;
+  void* const* y = nullptr;
+  const int* M = nullptr;
+  int count = 0;
 };
 
 // The fewest k-slices per block (wk) for which the blocks sharing a row block are, on average,
@@ -95,6 +116,7 @@ struct nvfp4_plan {
   int64_t row_blocks = 0, k_steps = 0, units = 0;
   GemvGeometry gg;     // mma.sync kernel
   ClusterGeometry cg;  // cluster kernel
+  bool dual = false;   // two [N, K] weights over one input: every launch covers 2 N rows
   Workspace ws;
 };
 
@@ -295,8 +317,14 @@ cudaError_t launch_gemv_nt(const nvfp4::gemv::Params& p, const void* x, int64_t 
 nvfp4_status launch_gemv(const GemvGeometry& gg, const void* x, int64_t lda, int M, const uint8_t* codes,
                          const uint8_t* scales, float gs, void* y, int64_t ldc, float* partials, int* counters,
                          uint8_t* x16, float* xs, int out_f32, int64_t N, int64_t K, int weights_after_wait,
-                         cudaStream_t stream, int silu_mul = 0) {
+                         cudaStream_t stream, int silu_mul, const CallExtras& ex, int64_t n1) {
   nvfp4::gemv::Params p;
+  p.codes1 = ex.codes1;
+  p.scales1 = ex.scales1;
+  p.y1 = ex.y1;
+  p.gs1 = ex.gs1;
+  p.n1 = n1;
+  p.rmap = ex.rmap;
   p.codes = codes;
   p.scales = scales;
   p.x16 = reinterpret_cast<const uint4*>(x16);
@@ -334,7 +362,8 @@ nvfp4_status launch_gemv(const GemvGeometry& gg, const void* x, int64_t lda, int
 nvfp4_status launch_main(const CUtensorMap& tm_codes, const CUtensorMap& tm_scales, const void* x, int64_t lda, int M,
                          float gs, void* y, int64_t ldc, float* partials, int* counters, int* err, uint8_t* x16,
                          float* xs, int out_f32, int grid, int64_t N, int64_t K, int64_t row_blocks,
-                         cudaStream_t stream, int silu_mul = 0, int weights_after_wait = 0) {
+                         cudaStream_t stream, int silu_mul = 0, int weights_after_wait = 0,
+                         const nvfp4::RowMap& rmap = nvfp4::RowMap{0, 1, {0, 0, 0, 0}, 0}) {
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -372,6 +401,7 @@ nvfp4_status launch_main(const CUtensorMap& tm_codes, const CUtensorMap& tm_scal
   p.M = M;
   p.out_f32 = out_f32;
   p.weights_after_wait = weights_after_wait;
+  p.rmap = rmap;
   p.grid = grid;
   p.N = N;
   p.K = K;
@@ -403,7 +433,7 @@ cudaError_t launch_cluster_nt(const nvfp4::cluster::Params& p, cudaStream_t stre
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(p.clusters * p.C));
+  cfg.gridDim = dim3((unsigned)(p.clusters * p.C), (unsigned)(p.grouped ? p.group_count : 1));
   cfg.blockDim = dim3(nvfp4::cluster::kThreads);
   cfg.dynamicSmemBytes = (size_t)nvfp4::cluster::smem_bytes(p.depth, p.units_k, NT, p.tiles_max);
   cfg.stream = stream;
@@ -414,8 +444,24 @@ cudaError_t launch_cluster_nt(const nvfp4::cluster::Params& p, cudaStream_t stre
 
 nvfp4_status launch_cluster(const ClusterGeometry& cg, const void* x, int64_t lda, int M, const uint8_t* codes,
                             const uint8_t* scales, float gs, void* y, int64_t ldc, int out_f32, int64_t N, int64_t K,
-                            int weights_after_wait, cudaStream_t stream, int silu_mul = 0) {
+                            int weights_after_wait, cudaStream_t stream, int silu_mul, const CallExtras& ex, int64_t n1,
+                            int* err, const GroupTables& gt = GroupTables{}) {
   nvfp4::cluster::Params p;
+  p.codes1 = ex.codes1;
+  p.scales1 = ex.scales1;
+  p.y1 = ex.y1;
+  p.gs1 = ex.gs1;
+  p.n1 = n1;
+  p.rmap = ex.rmap;
+  p.err = err;
+  p.grouped = gt.count > 0 ? 1 : 0;
+  p.g_codes = gt.codes;
+  p.g_scales = gt.scales;
+  p.g_gs = gt.gs;
+  p.g_x = gt.x;
+  p.g_y = gt.y;
+  p.g_M = gt.M;
+  p.group_count = gt.count;
   p.codes = codes;
   p.scales = scales;
   p.x = static_cast<const uint16_t*>(x);
@@ -447,19 +493,21 @@ nvfp4_status launch_cluster(const ClusterGeometry& cg, const void* x, int64_t ld
 
 nvfp4_status launch_call(nvfp4_plan* plan, const void* x, int64_t lda, int M, const uint8_t* codes,
                          const uint8_t* scales, float gs, void* y, int64_t ldc, cudaStream_t stream,
-                         int silu_mul = 0) {
+                         int silu_mul = 0, const CallExtras& ex = CallExtras{}) {
+  const int waw = (plan->flags & NVFP4_PLAN_WEIGHTS_AFTER_WAIT) ? 1 : 0;
+  const int out_f32 = plan->out == NVFP4_OUT_F32 ? 1 : 0;
+  // rows of the launch: both weights of a dual plan, the second from row N on
+  const int64_t rows = plan->dual ? 2 * plan->N : plan->N, n1 = plan->dual ? plan->N : rows;
   if (plan->kernel == NVFP4_KERNEL_CLUSTER)
-    return launch_cluster(plan->cg, x, lda, M, codes, scales, gs, y, ldc, plan->out == NVFP4_OUT_F32 ? 1 : 0,
-                          plan->N, plan->K, (plan->flags & NVFP4_PLAN_WEIGHTS_AFTER_WAIT) ? 1 : 0, stream, silu_mul);
+    return launch_cluster(plan->cg, x, lda, M, codes, scales, gs, y, ldc, out_f32, rows, plan->K, waw, stream,
+                          silu_mul, ex, n1, plan->ws.err);
   if (plan->kernel == NVFP4_KERNEL_MMA_SYNC)
     return launch_gemv(plan->gg, x, lda, M, codes, scales, gs, y, ldc, plan->ws.partials, plan->ws.counters,
-                       plan->ws.x16, plan->ws.xs, plan->out == NVFP4_OUT_F32 ? 1 : 0, plan->N, plan->K,
-                       (plan->flags & NVFP4_PLAN_WEIGHTS_AFTER_WAIT) ? 1 : 0, stream, silu_mul);
+                       plan->ws.x16, plan->ws.xs, out_f32, rows, plan->K, waw, stream, silu_mul, ex, n1);
   if (!prepare_tensor_maps(plan, codes, scales)) return NVFP4_ERR_CUDA;  // before anything is enqueued
   return launch_main(plan->tm_codes, plan->tm_scales, x, lda, M, gs, y, ldc, plan->ws.partials, plan->ws.counters,
-                     plan->ws.err, plan->ws.x16, plan->ws.xs, plan->out == NVFP4_OUT_F32 ? 1 : 0, plan->grid,
-                     plan->N, plan->K, plan->row_blocks, stream, silu_mul,
-                     (plan->flags & NVFP4_PLAN_WEIGHTS_AFTER_WAIT) ? 1 : 0);
+                     plan->ws.err, plan->ws.x16, plan->ws.xs, out_f32, plan->grid, plan->N, plan->K, plan->row_blocks,
+                     stream, silu_mul, waw, ex.rmap);
 }
 
 }  // namespace
@@ -515,13 +563,24 @@ nvfp4_status nvfp4_plan_create_flags(int64_t N, int64_t K, nvfp4_out_dtype out_d
   plan->kernel = (flags & NVFP4_PLAN_KERNEL_MMA_SYNC) ? NVFP4_KERNEL_MMA_SYNC : NVFP4_KERNEL_TCGEN05;
   plan->device = dev;
   plan->sm_count = sms;
-  if (flags & NVFP4_PLAN_KERNEL_CLUSTER) {
-    plan->cg = cluster_geometry(N, K, sms);
-    if (!plan->cg.ok) {
+  // A dual plan covers two [N, K] weights, 2 N launch rows, on one of the mma.sync kernels: the
+  // cluster kernel where it takes the shape, else the register-direct one.
+  plan->dual = (flags & NVFP4_PLAN_DUAL) != 0;
+  const int64_t rows = plan->dual ? 2 * N : N;
+  if (plan->dual && (flags & NVFP4_PLAN_KERNEL_TCGEN05)) {
+    delete plan;
+    return NVFP4_ERR_ARG;
+  }
+  if ((flags & NVFP4_PLAN_KERNEL_CLUSTER) || (plan->dual && !(flags & NVFP4_PLAN_KERNEL_MMA_SYNC))) {
+    plan->cg = cluster_geometry(rows, K, sms);
+    if (plan->cg.ok)
+      plan->kernel = NVFP4_KERNEL_CLUSTER;
+    else if (flags & NVFP4_PLAN_KERNEL_CLUSTER) {
       delete plan;
       return NVFP4_ERR_SHAPE;
+    } else {
+      plan->kernel = NVFP4_KERNEL_MMA_SYNC;
     }
-    plan->kernel = NVFP4_KERNEL_CLUSTER;
   }
 
   size_t part_bytes, cnt_bytes, x16b, cnt_count;
@@ -534,7 +593,7 @@ nvfp4_status nvfp4_plan_create_flags(int64_t N, int64_t K, nvfp4_out_dtype out_d
     cnt_count = 0;
     x16b = 0;
   } else if (plan->kernel == NVFP4_KERNEL_MMA_SYNC) {
-    plan->gg = gemv_geometry(N, K, sms);
+    plan->gg = gemv_geometry(rows, K, sms);
     plan->row_blocks = plan->gg.row_blocks;
     plan->k_steps = plan->gg.S;
     plan->units = plan->gg.units;
@@ -599,7 +658,7 @@ void nvfp4_plan_destroy(nvfp4_plan_t plan) {
 
 nvfp4_status nvfp4_skinny_linear(nvfp4_plan_t plan, const void* x, int M, const uint8_t* w_codes,
                                  const uint8_t* w_block_scales, float w_global_scale, void* y, void* stream) {
-  if (!plan || !x || !w_codes || !w_block_scales || !y) return NVFP4_ERR_ARG;
+  if (!plan || !x || !w_codes || !w_block_scales || !y || plan->dual) return NVFP4_ERR_ARG;
   if (M < 1 || M > NVFP4_MAX_M) return NVFP4_ERR_M_RANGE;
   if (!aligned16(x) || !aligned16(y) || !aligned16(w_codes) || !aligned16(w_block_scales)) return NVFP4_ERR_ALIGN;
   return launch_call(plan, x, plan->K, M, w_codes, w_block_scales, w_global_scale, y, plan->N,
@@ -609,7 +668,7 @@ nvfp4_status nvfp4_skinny_linear(nvfp4_plan_t plan, const void* x, int M, const 
 nvfp4_status nvfp4_skinny_linear_strided(nvfp4_plan_t plan, const void* x, int64_t lda, int M, const uint8_t* w_codes,
                                          const uint8_t* w_block_scales, float w_global_scale, void* y, int64_t ldc,
                                          void* stream) {
-  if (!plan || !x || !w_codes || !w_block_scales || !y) return NVFP4_ERR_ARG;
+  if (!plan || !x || !w_codes || !w_block_scales || !y || plan->dual) return NVFP4_ERR_ARG;
   if (M < 1 || M > NVFP4_MAX_M) return NVFP4_ERR_M_RANGE;
   if (lda < plan->K || ldc < plan->N) return NVFP4_ERR_SHAPE;
   if (!aligned16(x) || !aligned16(y) || !aligned16(w_codes) || !aligned16(w_block_scales) || lda % 8 != 0 ||
@@ -620,7 +679,7 @@ nvfp4_status nvfp4_skinny_linear_strided(nvfp4_plan_t plan, const void* x, int64
 }
 
 nvfp4_status nvfp4_skinny_linear_grouped(nvfp4_plan_t plan, const nvfp4_group_item* items, int count, void* stream) {
-  if (!plan || !items || count < 1) return NVFP4_ERR_ARG;
+  if (!plan || !items || count < 1 || plan->dual) return NVFP4_ERR_ARG;
   for (int e = 0; e < count; ++e) {
     const nvfp4_group_item& it = items[e];
     if (!it.x || !it.w_codes || !it.w_block_scales || !it.y) return NVFP4_ERR_ARG;
@@ -640,7 +699,7 @@ nvfp4_status nvfp4_skinny_linear_grouped(nvfp4_plan_t plan, const nvfp4_group_it
 nvfp4_status nvfp4_skinny_linear_silu_mul(nvfp4_plan_t plan, const void* gate_up, int64_t ld_gate_up, int M,
                                           const uint8_t* w_codes, const uint8_t* w_block_scales, float w_global_scale,
                                           void* y, int64_t ldc, void* stream) {
-  if (!plan || !gate_up || !w_codes || !w_block_scales || !y) return NVFP4_ERR_ARG;
+  if (!plan || !gate_up || !w_codes || !w_block_scales || !y || plan->dual) return NVFP4_ERR_ARG;
   if (M < 1 || M > NVFP4_MAX_M) return NVFP4_ERR_M_RANGE;
   if (ld_gate_up < 2 * plan->K || ldc < plan->N) return NVFP4_ERR_SHAPE;
   if (!aligned16(gate_up) || !aligned16(y) || !aligned16(w_codes) || !aligned16(w_block_scales) ||
@@ -648,6 +707,70 @@ nvfp4_status nvfp4_skinny_linear_silu_mul(nvfp4_plan_t plan, const void* gate_up
     return NVFP4_ERR_ALIGN;
   return launch_call(plan, gate_up, ld_gate_up, M, w_codes, w_block_scales, w_global_scale, y, ldc,
                      static_cast<cudaStream_t>(stream), 1);
+}
+
+nvfp4_status nvfp4_skinny_linear_dual(nvfp4_plan_t plan, const void* x, int M, const uint8_t* w0_codes,
+                                      const uint8_t* w0_block_scales, float w0_global_scale, void* y0,
+                                      const uint8_t* w1_codes, const uint8_t* w1_block_scales, float w1_global_scale,
+                                      void* y1, void* stream) {
+  if (!plan || !plan->dual || !x || !w0_codes || !w0_block_scales || !y0 || !w1_codes || !w1_block_scales || !y1)
+    return NVFP4_ERR_ARG;
+  if (M < 1 || M > NVFP4_MAX_M) return NVFP4_ERR_M_RANGE;
+  if (!aligned16(x) || !aligned16(y0) || !aligned16(w0_codes) || !aligned16(w0_block_scales) || !aligned16(y1) ||
+      !aligned16(w1_codes) || !aligned16(w1_block_scales))
+    return NVFP4_ERR_ALIGN;
+  CallExtras ex;
+  ex.codes1 = w1_codes;
+  ex.scales1 = w1_block_scales;
+  ex.y1 = y1;
+  ex.gs1 = w1_global_scale;
+  return launch_call(plan, x, plan->K, M, w0_codes, w0_block_scales, w0_global_scale, y0, plan->N,
+                     static_cast<cudaStream_t>(stream), 0, ex);
+}
+
+nvfp4_status nvfp4_skinny_linear_deinterleaved(nvfp4_plan_t plan, const void* x, int M, const uint8_t* w_codes,
+                                               const uint8_t* w_block_scales, float w_global_scale, void* y, int parts,
+                                               const int32_t* part_rows, void* stream) {
+  if (!plan || !x || !w_codes || !w_block_scales || !y || !part_rows || plan->dual) return NVFP4_ERR_ARG;
+  if (M < 1 || M > NVFP4_MAX_M) return NVFP4_ERR_M_RANGE;
+  if (parts < 2 || parts > 4) return NVFP4_ERR_ARG;
+  CallExtras ex;
+  int64_t group = 0;
+  for (int q = 0; q < parts; ++q) {
+    if (part_rows[q] < 1) return NVFP4_ERR_ARG;
+    ex.rmap.rows[q] = part_rows[q];
+    group += part_rows[q];
+  }
+  if (group > plan->N || plan->N % group != 0) return NVFP4_ERR_SHAPE;
+  ex.rmap.parts = parts;
+  ex.rmap.group = (int)group;
+  ex.rmap.groups = plan->N / group;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(w_codes) || !aligned16(w_block_scales)) return NVFP4_ERR_ALIGN;
+  return launch_call(plan, x, plan->K, M, w_codes, w_block_scales, w_global_scale, y, plan->N,
+                     static_cast<cudaStream_t>(stream), 0, ex);
+}
+
+nvfp4_status nvfp4_skinny_linear_grouped_tables(nvfp4_plan_t plan, const nvfp4_expert_tables* tables, int count,
+                                                int max_M, void* stream) {
+  if (!plan || !tables || plan->dual || plan->kernel != NVFP4_KERNEL_CLUSTER) return NVFP4_ERR_ARG;
+  if (!tables->w_codes || !tables->w_block_scales || !tables->w_global_scales || !tables->x || !tables->M ||
+      !tables->y)
+    return NVFP4_ERR_ARG;
+  if (count < 1 || count > 65535) return NVFP4_ERR_ARG;
+  if (max_M < 1 || max_M > NVFP4_MAX_M) return NVFP4_ERR_M_RANGE;
+  GroupTables gt;
+  gt.codes = tables->w_codes;
+  gt.scales = tables->w_block_scales;
+  gt.gs = tables->w_global_scales;
+  gt.x = reinterpret_cast<const uint16_t* const*>(tables->x);
+  gt.y = tables->y;
+  gt.M = tables->M;
+  gt.count = count;
+  // the per-entry pointers come from the tables on the device; these stand-ins are never read
+  const nvfp4_status st = launch_cluster(plan->cg, nullptr, plan->K, max_M, nullptr, nullptr, 0.f, nullptr, plan->N,
+                                         plan->out == NVFP4_OUT_F32 ? 1 : 0, plan->N, plan->K, 1,
+                                         static_cast<cudaStream_t>(stream), 0, CallExtras{}, plan->N, plan->ws.err, gt);
+  return st;
 }
 
 nvfp4_status nvfp4_plan_check(nvfp4_plan_t plan, void* stream) {
@@ -666,7 +789,7 @@ nvfp4_status nvfp4_plan_check(nvfp4_plan_t plan, void* stream) {
                          s) != cudaSuccess) ||
         cudaStreamSynchronize(s) != cudaSuccess)
       return NVFP4_ERR_CUDA;
-    return NVFP4_ERR_TIMEOUT;
+    return (err & nvfp4::kErrTimeout) ? NVFP4_ERR_TIMEOUT : NVFP4_ERR_M_RANGE;
   }
   return NVFP4_OK;
 }

@@ -127,7 +127,30 @@ __host__ __device__ constexpr uint32_t idesc() {
 
 constexpr long long kWaitLimitCycles = 4000000000LL;  // ~2 s at 2 GHz: a bounded wait
 
-enum : int { kErrTimeout = 1 };
+enum : int { kErrTimeout = 1, kErrMRange = 2 };  // bits of a plan's device error word
+
+// ------------------------------------------------------------------ output row order
+// Weights whose rows interleave up to four parts per group ("Module ops", w4a16_gemv_qg: Q and
+// gate rows per head; w4a16_gemv_qkvz: Q, K, V and Z rows per group) with the output stored
+// deinterleaved, part-major: [part 0 of every group | part 1 of every group | ...].  parts = 0 is
+// the plain order.  Only where a result is stored changes, never how it is computed.
+struct RowMap {
+  int parts;        // 0, or 2..4
+  int group;        // rows per group: rows[0] + ... + rows[parts - 1]
+  int rows[4];      // rows of each part in a group
+  int64_t groups;   // weight rows / group
+};
+__host__ __device__ __forceinline__ int64_t map_row(const RowMap& r, int64_t n) {
+  if (r.parts == 0) return n;
+  const int64_t grp = n / r.group;
+  int o = (int)(n - grp * r.group), off = 0;
+  for (int q = 0; q + 1 < r.parts; ++q) {
+    if (o < r.rows[q]) return r.groups * off + grp * r.rows[q] + o;
+    o -= r.rows[q];
+    off += r.rows[q];
+  }
+  return r.groups * off + grp * r.rows[r.parts - 1] + o;
+}
 
 struct MainParams {
   CUtensorMap tm_codes;   // uint8 [N rows, K/2 bytes], box 128 B x 256 rows, 128-byte swizzle
@@ -145,6 +168,7 @@ struct MainParams {
   int M;
   int out_f32;
   int weights_after_wait;  // 1: thread 0 waits for the kernels before this one before its first weight copy
+  RowMap rmap;             // where each output row is stored (deinterleaved weights)
   int grid;
   int64_t N, K;
   int64_t S;      // k-steps = K / 256
@@ -638,11 +662,12 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
       const bool bf16_out = whole && !p.out_f32;
       const float mul = whole ? gs : 1.f;
       const int64_t fstride = whole ? p.ldc : kRowsPerBlock;
-      float* f0 = whole ? static_cast<float*>(p.y) + n0 : p.partials + (int64_t)slot * (kNmma * kRowsPerBlock) + r0;
-      float* f1 = whole ? static_cast<float*>(p.y) + n1 : p.partials + (int64_t)slot * (kNmma * kRowsPerBlock) + r1;
-      uint16_t* h0 = static_cast<uint16_t*>(p.y) + n0;
-      uint16_t* h1 = static_cast<uint16_t*>(p.y) + n1;
       const bool in0 = !whole || n0 < p.N, in1 = !whole || n1 < p.N;
+      const int64_t o0 = in0 && whole ? map_row(p.rmap, n0) : n0, o1 = in1 && whole ? map_row(p.rmap, n1) : n1;
+      float* f0 = whole ? static_cast<float*>(p.y) + o0 : p.partials + (int64_t)slot * (kNmma * kRowsPerBlock) + r0;
+      float* f1 = whole ? static_cast<float*>(p.y) + o1 : p.partials + (int64_t)slot * (kNmma * kRowsPerBlock) + r1;
+      uint16_t* h0 = static_cast<uint16_t*>(p.y) + o0;
+      uint16_t* h1 = static_cast<uint16_t*>(p.y) + o1;
 #pragma unroll 1
       for (int cb = 0; cb < NC / 16; ++cb) {
         float v0[16], v1[16];
@@ -710,23 +735,24 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
     auto store4 = [&](int m, int r, float4 acc) {
       const float v[4] = {__fmul_rn(acc.x, gs), __fmul_rn(acc.y, gs), __fmul_rn(acc.z, gs), __fmul_rn(acc.w, gs)};
       const int64_t n = rb * kRowsPerBlock + r;
+      const bool vec = n + 3 < p.N && (p.ldc & 3) == 0 && p.rmap.parts == 0;  // four adjacent output rows
       if (p.out_f32) {
         float* yrow = static_cast<float*>(p.y) + (int64_t)m * p.ldc;
-        if (n + 3 < p.N && (p.ldc & 3) == 0) {
+        if (vec) {
           *reinterpret_cast<float4*>(yrow + n) = make_float4(v[0], v[1], v[2], v[3]);
         } else {
           for (int c = 0; c < 4; ++c)
-            if (n + c < p.N) yrow[n + c] = v[c];
+            if (n + c < p.N) yrow[map_row(p.rmap, n + c)] = v[c];
         }
       } else {
         uint16_t* yrow = static_cast<uint16_t*>(p.y) + (int64_t)m * p.ldc;
-        if (n + 3 < p.N && (p.ldc & 3) == 0) {
+        if (vec) {
           const uint32_t lo = (uint32_t)ptx::f32_to_bf16_rn(v[0]) | ((uint32_t)ptx::f32_to_bf16_rn(v[1]) << 16);
           const uint32_t hi = (uint32_t)ptx::f32_to_bf16_rn(v[2]) | ((uint32_t)ptx::f32_to_bf16_rn(v[3]) << 16);
           *reinterpret_cast<uint2*>(yrow + n) = make_uint2(lo, hi);
         } else {
           for (int c = 0; c < 4; ++c)
-            if (n + c < p.N) yrow[n + c] = ptx::f32_to_bf16_rn(v[c]);
+            if (n + c < p.N) yrow[map_row(p.rmap, n + c)] = ptx::f32_to_bf16_rn(v[c]);
         }
       }
     };
