@@ -17,8 +17,8 @@ scaling); the time is the max over ranks and `value` sums all ranks' bytes.
 
 `other_workloads` adds the other projection shapes, the 64-layer decode round and the prefill
 projection (M = 64 / 256 / 1024, TFLOP/s against the dense bf16 tensor peak); `kernel_ab` times
-the register-direct mma.sync kernel on the same large shapes and on the round (the plans' default
-is the tcgen05 kernel).
+the two mma.sync kernels on the same shapes: the register-direct one everywhere and on the
+round, the cluster-split one on the shapes it takes (the plans' default is the tcgen05 kernel).
 """
 import argparse
 import hashlib
@@ -269,12 +269,18 @@ def run_ours(args, rank, world):
 
     # ---------------- other workloads (reported alongside, not the headline)
     others = {} if args.quick else run_other_workloads(stream, rank, peak)
-    # ---------------- the register-direct mma.sync kernel on the same shapes (A/B)
+    # ---------------- the two mma.sync kernels on the same shapes (A/B against the default tcgen05)
     ab = {} if args.quick else {
-        "kernel": "register-direct mma.sync (NVFP4_PLAN_KERNEL_MMA_SYNC); the default plans run tcgen05",
-        "square 5120x5120": run_square_ab(stream, rank, peak),
-        **run_other_workloads(stream, rank, peak, flags=nb.NVFP4_PLAN_KERNEL_MMA_SYNC, Ms=HEAD_MS,
-                              with_prefill=False)}
+        "mma_sync": {
+            "kernel": "register-direct mma.sync (NVFP4_PLAN_KERNEL_MMA_SYNC); the default plans run tcgen05",
+            "square 5120x5120": run_square_ab(stream, rank, peak, nb.NVFP4_PLAN_KERNEL_MMA_SYNC),
+            **run_other_workloads(stream, rank, peak, flags=nb.NVFP4_PLAN_KERNEL_MMA_SYNC, Ms=HEAD_MS,
+                                  with_prefill=False)},
+        "cluster": {
+            "kernel": "cluster-split mma.sync, one launch (NVFP4_PLAN_KERNEL_CLUSTER); only the shapes it takes",
+            "square 5120x5120": run_square_ab(stream, rank, peak, nb.NVFP4_PLAN_KERNEL_CLUSTER),
+            **run_other_workloads(stream, rank, peak, flags=nb.NVFP4_PLAN_KERNEL_CLUSTER, Ms=HEAD_MS,
+                                  with_prefill=False, with_round=False)}}
 
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -354,14 +360,15 @@ def run_e2e(args, proj, x_all, stream, world):
                       "how": "the same step issued eagerly from Python, call by call"}}
 
 
-def run_square_ab(stream, rank, peak):
-    """The headline square projection on register-direct plans, each M as in other_workloads."""
+def run_square_ab(stream, rank, peak, flags):
+    """The headline square projection on plans made with `flags` (another kernel), each M as in
+    other_workloads."""
     import torch
     from nvfp4_skinny_gb300 import binding as nb
     from nvfp4_skinny_gb300 import synth
     sq = synth.WORKLOADS["square"].projections[0]
     copies = max(2, -(-3 * L2_BYTES // call_bytes(sq.N, sq.K, 1)))
-    proj = Projection(sq.N, sq.K, sq.seed + 1000 * rank, copies, False, nb.NVFP4_PLAN_KERNEL_MMA_SYNC)
+    proj = Projection(sq.N, sq.K, sq.seed + 1000 * rank, copies, False, flags)
     x_all = synth.activations(32, sq.K, sq.seed, device="cuda")
     entry = {}
     for M in HEAD_MS:
@@ -393,9 +400,10 @@ def _time_graph(g, stream, reps, warm=3):
     return a.elapsed_time(b) / reps
 
 
-def run_other_workloads(stream, rank, peak, flags=0, Ms=None, with_prefill=True):
+def run_other_workloads(stream, rank, peak, flags=0, Ms=None, with_prefill=True, with_round=True):
     """QKV / down, wide gate|up / head (fp32 out), and the full 64-layer decode round (on plans
-    made with `flags`; each shape at its workload's Ms, or at `Ms`)."""
+    made with `flags`; each shape at its workload's Ms, or at `Ms`).  A shape the flags' kernel
+    does not take is reported as such."""
     import torch
     from nvfp4_skinny_gb300 import binding as nb
     from nvfp4_skinny_gb300 import synth
@@ -405,6 +413,12 @@ def run_other_workloads(stream, rank, peak, flags=0, Ms=None, with_prefill=True)
         for pj in w.projections:
             per_copy = call_bytes(pj.N, pj.K, 1, 4 if pj.f32_out else 2)
             copies = max(2, -(-3 * L2_BYTES // per_copy))
+            name = "%s %dx%d%s" % (pj.name, pj.N, pj.K, " f32-out" if pj.f32_out else "")
+            try:
+                nb.nvfp4_plan_create_flags(pj.N, pj.K, nb.NVFP4_OUT_BF16, flags).destroy()
+            except nb.Nvfp4Error as e:
+                res[name] = {"not_planned": str(e)}
+                continue
             proj = Projection(pj.N, pj.K, pj.seed + 1000 * rank, copies, pj.f32_out, flags)
             x_all = synth.activations(32, pj.K, pj.seed, device="cuda", outlier_frac=w.outlier_frac)
             entry = {}
@@ -420,11 +434,12 @@ def run_other_workloads(stream, rank, peak, flags=0, Ms=None, with_prefill=True)
                 entry[str(M)] = {"us_per_call": round(t_call * 1e3, 3), "GBps": round(gbs, 1),
                                  "frac_of_peak": round(gbs / peak, 4),
                                  "GBps_actual_out_bytes": round(byts / (t_call * 1e-3) / 1e9, 1)}
-            res["%s %dx%d%s" % (pj.name, pj.N, pj.K, " f32-out" if pj.f32_out else "")] = entry
+            res[name] = entry
             assert nb.nvfp4_plan_check(proj.plan, stream) == nb.NVFP4_OK
             del proj
             torch.cuda.empty_cache()
-    res["round"] = run_round(stream, rank, peak, flags)
+    if with_round:
+        res["round"] = run_round(stream, rank, peak, flags)
     if with_prefill:
         res["prefill"] = run_prefill(stream, rank)
     return res
@@ -672,6 +687,35 @@ def profile_shape(args):
         N, K, Ms, copies, args.warmup + args.steps, "mma" if args.mma else "tcgen05"))
 
 
+def profile_round(args):
+    """The 64-layer decode round (qkv, o, gate|up, down per layer), --warmup then --steps rounds
+    at one M, issued eagerly, for an ncu launch list (the per-launch times of all 256 calls)."""
+    import torch
+    from nvfp4_skinny_gb300 import binding as nb
+    from nvfp4_skinny_gb300 import build as nbuild
+    from nvfp4_skinny_gb300 import synth
+    nbuild.build()
+    M = int(args.profile_round)
+    w = synth.WORKLOADS["round"]
+    plans = {}
+    weights = []
+    for pj in w.projections:
+        if (pj.N, pj.K) not in plans:
+            plans[(pj.N, pj.K)] = nb.nvfp4_plan_create(pj.N, pj.K)
+        weights.append((pj, synth.weights(pj.N, pj.K, pj.seed, device="cuda")))
+    xs = {K: synth.activations(M, K, 1, device="cuda") for K in (5120, 17408)}
+    ys = {N: torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for N in (5120, 7168, 34816)}
+    torch.cuda.synchronize()
+    for _ in range(args.warmup + args.steps):
+        for pj, (c, sc, gs) in weights:
+            nb.nvfp4_skinny_linear(plans[(pj.N, pj.K)], xs[pj.K], M, c, sc, gs, ys[pj.N])
+    torch.cuda.synchronize()
+    for p in plans.values():
+        if nb.nvfp4_plan_check(p) != nb.NVFP4_OK:
+            raise RuntimeError("kernel reported an error")
+    print("profiled round M=%d calls per round=%d rounds=%d" % (M, len(weights), args.warmup + args.steps))
+
+
 def profile_prefill(args):
     """A few prefill calls of one shape on rotating cold weights (> 2x L2), for ncu captures."""
     import torch
@@ -743,6 +787,8 @@ def main(argv=None):
                     help="profiling driver: for each M, run --warmup then --steps calls of one shape on cold "
                          "weights, no JSON")
     ap.add_argument("--mma", action="store_true", help="--profile-shape on register-direct mma.sync plans")
+    ap.add_argument("--profile-round", default=None, metavar="M",
+                    help="run the 64-layer decode round at one M eagerly (for ncu launch lists), then exit")
     ap.add_argument("--profile-prefill", default=None, metavar="N,K,M",
                     help="run a few prefill calls of one shape (for ncu) and exit")
     args = ap.parse_args(argv)
@@ -750,6 +796,8 @@ def main(argv=None):
         return profile_shape(args)
     if args.profile_prefill:
         return profile_prefill(args)
+    if args.profile_round:
+        return profile_round(args)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world = dist_init()

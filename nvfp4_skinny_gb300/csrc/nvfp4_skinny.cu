@@ -518,7 +518,9 @@ const char* nvfp4_status_string(nvfp4_status status) {
   switch (status) {
     case NVFP4_OK: return "NVFP4_OK";
     case NVFP4_ERR_ARG: return "NVFP4_ERR_ARG: null plan or pointer, or invalid enum";
-    case NVFP4_ERR_SHAPE: return "NVFP4_ERR_SHAPE: need N >= 1 and K a positive multiple of 256";
+    case NVFP4_ERR_SHAPE:
+      return "NVFP4_ERR_SHAPE: a size the call refuses (N >= 1, K a positive multiple of 256, strides, a group of "
+             "rows dividing N) or that the chosen kernel does not take";
     case NVFP4_ERR_ALIGN: return "NVFP4_ERR_ALIGN: x, y, w_codes and w_block_scales must be 16-byte aligned";
     case NVFP4_ERR_M_RANGE: return "NVFP4_ERR_M_RANGE: M must be in 1..32";
     case NVFP4_ERR_CUDA: return "NVFP4_ERR_CUDA: a CUDA runtime call failed";
