@@ -184,3 +184,44 @@ def test_grouped_tables_rows_out_of_range_and_refusals():
     assert nb.nvfp4_skinny_linear_grouped_tables(plan, t, 0, 8, check=False) == nb.NVFP4_ERR_ARG
     assert nb.nvfp4_skinny_linear_grouped_tables(plan, t, 2, 33, check=False) == nb.NVFP4_ERR_M_RANGE
     torch.cuda.synchronize()
+
+
+# ------------------------------------------------------------------ fp32 outputs of the variants
+
+def test_variants_fp32_output():
+    """Dual, deinterleaved and grouped-table calls on fp32-output plans: the same values as the
+    bf16 plans before rounding, within the oracle's tolerance, and the grouped bits equal to
+    single calls."""
+    N, K, M = 768, 1024, 5
+    c0 = Case(N, K, M, seed=71)
+    c1 = Case(N, K, M, seed=72, x=c0.x, gs=0.5)
+    r0, a0 = c0.oracle_full()
+    r1, a1 = c1.oracle_full()
+    dual = nb.nvfp4_plan_create_flags(N, K, nb.NVFP4_OUT_F32, nb.NVFP4_PLAN_DUAL)
+    y0 = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    y1 = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    nb.nvfp4_skinny_linear_dual(dual, c0.d_x, M, (c0.d_codes, c0.d_scales, c0.gs), (c1.d_codes, c1.d_scales, c1.gs),
+                                y0, y1)
+    torch.cuda.synchronize()
+    for y, r, a in ((y0, r0, a0), (y1, r1, a1)):
+        ok, ratio = within_tolerance(to_f64(y), r, a)
+        assert ok, ratio
+    parts = (64, 32, 32, 64)
+    order = torch.from_numpy(_deinterleave_order(N, parts)).cuda()
+    for kernel in (nb.NVFP4_PLAN_KERNEL_TCGEN05, nb.NVFP4_PLAN_KERNEL_MMA_SYNC, nb.NVFP4_PLAN_KERNEL_CLUSTER):
+        plan = nb.nvfp4_plan_create_flags(N, K, nb.NVFP4_OUT_F32, kernel)
+        y = c0.run(plan)
+        yd = torch.empty_like(y)
+        nb.nvfp4_skinny_linear_deinterleaved(plan, c0.d_x, M, c0.d_codes, c0.d_scales, c0.gs, yd, parts)
+        torch.cuda.synchronize()
+        want = torch.empty_like(y)
+        want[:, order] = y
+        assert torch.equal(yd, want), kernel
+        ok, ratio = within_tolerance(to_f64(y), r0, a0)
+        assert ok, (kernel, ratio)
+    plan = nb.nvfp4_plan_create_flags(N, K, nb.NVFP4_OUT_F32, nb.NVFP4_PLAN_KERNEL_CLUSTER)
+    ys = [torch.empty((M, N), dtype=torch.float32, device="cuda") for _ in range(2)]
+    nb.nvfp4_skinny_linear_grouped_tables(plan, _tables([c0, c1], ys), 2, M)
+    torch.cuda.synchronize()
+    assert nb.nvfp4_plan_check(plan) == nb.NVFP4_OK
+    assert torch.equal(ys[0], c0.run(plan)) and torch.equal(ys[1], c1.run(plan))
