@@ -35,7 +35,8 @@
 //
 // Work split ("10 Kernels" 10.1 Row invariance): a unit is (row block of 256 weight rows,
 // k-step of 256).  The units, row-block-major, are split into `grid` contiguous, equal ranges;
-// grid = min(units, SMs).  Which block computes which part of a row's sum, the order of the
+// grid = min(units, SMs), or fewer blocks of u <= 4 units each when such ranges never straddle a
+// row block (chosen on the host).  Which block computes which part of a row's sum, the order of the
 // MMAs and the order in which parts are added all depend on (N, K, grid) only.  Activation
 // row m is column m of every MMA, its exponent e depends on row m alone, and nothing a column
 // computes depends on another column, so a row's bits do not depend on M.

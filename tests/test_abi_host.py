@@ -83,9 +83,15 @@ def _block_of(u, T, G):
 
 @pytest.mark.parametrize("B,S,sms", [(1, 2, 152), (20, 20, 152), (28, 20, 152), (20, 68, 152), (136, 20, 152),
                                      (594, 20, 152), (3, 1, 152), (7, 3, 4), (5, 7, 5), (2, 9, 11), (40, 2, 152)])
-def test_work_split_invariants(B, S, sms):
+@pytest.mark.parametrize("aligned", [False, True])
+def test_work_split_invariants(B, S, sms, aligned):
     T = B * S
     G = min(T, sms)
+    if aligned:  # the tcgen05 plan's grid: fewer blocks of u <= 4 units that never straddle a row block
+        us = [u for u in range(1, 5) if T % u == 0 and S % u == 0 and T // u <= sms]
+        if us:
+            G = T // us[0]
+            assert all((b // S) == ((e - 1) // S) for b, e in _split(T, G))
     ranges = _split(T, G)
     assert ranges[0][0] == 0 and ranges[-1][1] == T
     sizes = [e - b for b, e in ranges]

@@ -453,6 +453,11 @@ def test_plan_info_independent_of_M(kernel):
             continue
         assert info["row_blocks"] == -(-N // info["rows_per_block"])
         assert info["units"] == info["row_blocks"] * (K // info["k_step"])
-        blocks_per_sm = 1 if kernel == "tcgen05" else 2  # the register-direct kernel runs two per SM
-        assert info["grid"] == min(info["units"], blocks_per_sm * info["sm_count"])
+        if kernel == "tcgen05":
+            # min(units, SMs), or fewer blocks of u <= 4 units whose ranges never straddle a row block
+            steps, units, sms = K // info["k_step"], info["units"], info["sm_count"]
+            aligned = [units // u for u in range(1, 5) if units % u == 0 and steps % u == 0 and units // u <= sms]
+            assert info["grid"] == (aligned[0] if aligned else min(units, sms))
+        else:  # the register-direct kernel runs two blocks per SM
+            assert info["grid"] == min(info["units"], 2 * info["sm_count"])
         assert info["warps_rows"] * info["warps_k"] * 32 == (info["threads"] if kernel == "mma" else 32)
