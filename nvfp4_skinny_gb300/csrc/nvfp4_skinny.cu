@@ -172,15 +172,24 @@ size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 size_t x16_bytes(int64_t K) { return (size_t)(K / nvfp4::kKStep) * nvfp4::kXAreaBytes; }
 
-// Blocks of the tcgen05 split: min(units, SMs), unless a smaller grid splits the units into
-// equal ranges of u <= kStages units that never straddle a row block (u divides both the units
-// and the k-steps per row block).  Then every block has one segment, each row block is summed
-// from exactly K / (256 u) parts, and the call keeps its one-launch mode: for the 5120^2 weight
-// 100 blocks of 4 units against 152 of 2-3, with M = 32 calls 1.7 us shorter (measured).
-// A function of (N, K, SM count) only.
+// Blocks of the tcgen05 split, preferring ranges that never straddle a row block:
+// - a grid of u <= kStages units per block, u dividing both the units and the k-steps per row
+//   block: every block has one segment, each row block is summed from exactly K / (256 u) parts,
+//   and the call keeps its one-launch mode (5120^2: 100 blocks of 4 units against 152 of 2-3;
+//   M = 32 calls 1.7 us shorter);
+// - else whole row blocks per block, when that still keeps at least 85 % of the SMs busy: no
+//   split-K at all (34816x5120: 136 blocks of one row block against 152; 2.5-8 % shorter);
+// - else min(units, SMs).
+// A function of (N, K, SM count) only (all measured on eager back-to-back calls).
 int64_t tc_grid(int64_t units, int64_t steps, int sms) {
   for (int64_t u = 1; u <= nvfp4::kStages; ++u)
     if (units % u == 0 && steps % u == 0 && units / u <= sms) return units / u;
+  const int64_t row_blocks = units / steps;
+  for (int64_t k = 1; k <= row_blocks; ++k)
+    if (row_blocks % k == 0 && row_blocks / k <= sms) {
+      if (20 * (row_blocks / k) >= 17 * (int64_t)sms) return row_blocks / k;
+      break;
+    }
   return units < sms ? units : sms;
 }
 

@@ -87,11 +87,15 @@ def _block_of(u, T, G):
 def test_work_split_invariants(B, S, sms, aligned):
     T = B * S
     G = min(T, sms)
-    if aligned:  # the tcgen05 plan's grid: fewer blocks of u <= 4 units that never straddle a row block
+    if aligned:  # the tcgen05 plan's grid: ranges that never straddle a row block, where it can
         us = [u for u in range(1, 5) if T % u == 0 and S % u == 0 and T // u <= sms]
-        if us:
+        ks = [k for k in range(1, B + 1) if B % k == 0 and B // k <= sms][:1]
+        if us:  # u <= 4 units of one row block per range
             G = T // us[0]
             assert all((b // S) == ((e - 1) // S) for b, e in _split(T, G))
+        elif ks and 20 * (B // ks[0]) >= 17 * sms:  # whole row blocks per range
+            G = B // ks[0]
+            assert all(b % S == 0 and e % S == 0 for b, e in _split(T, G))
     ranges = _split(T, G)
     assert ranges[0][0] == 0 and ranges[-1][1] == T
     sizes = [e - b for b, e in ranges]

@@ -457,7 +457,10 @@ def test_plan_info_independent_of_M(kernel):
             # min(units, SMs), or fewer blocks of u <= 4 units whose ranges never straddle a row block
             steps, units, sms = K // info["k_step"], info["units"], info["sm_count"]
             aligned = [units // u for u in range(1, 5) if units % u == 0 and steps % u == 0 and units // u <= sms]
-            assert info["grid"] == (aligned[0] if aligned else min(units, sms))
+            rb = units // steps
+            whole = [rb // k for k in range(1, rb + 1) if rb % k == 0 and rb // k <= sms][:1]
+            whole = [g for g in whole if 20 * g >= 17 * sms]  # whole row blocks, >= 85 % of the SMs
+            assert info["grid"] == (aligned or whole or [min(units, sms)])[0]
         else:  # the register-direct kernel runs two blocks per SM
             assert info["grid"] == min(info["units"], 2 * info["sm_count"])
         assert info["warps_rows"] * info["warps_k"] * 32 == (info["threads"] if kernel == "mma" else 32)
