@@ -32,13 +32,14 @@
  * Ownership and concurrency
  *   The caller owns x, the weight buffers and y.  A plan owns host state and
  *   one device workspace (split-K partials, counters, an error word, the
- *   fp16 activation operand and its per-row scales), allocated by
- *   nvfp4_plan_create* on the device that is current then; all later calls
- *   on the plan must run on that device.  nvfp4_skinny_linear never
- *   allocates, never synchronizes and only enqueues kernels on `stream`, so
- *   it can be captured in a CUDA graph.  A plan runs one of two kernels,
- *   chosen at plan creation from (N, K) and the SM count (or forced with
- *   nvfp4_plan_create_flags); nvfp4_plan_info.kernel says which:
+ *   fp16 activation operand and its per-row scales; the cluster kernel needs
+ *   only the error word), allocated by nvfp4_plan_create* on the device that
+ *   is current then; all later calls on the plan must run on that device.
+ *   nvfp4_skinny_linear never allocates, never synchronizes and only enqueues
+ *   kernels on `stream`, so it can be captured in a CUDA graph.  A plan runs
+ *   one of three kernels, chosen at plan creation from (N, K) and the SM
+ *   count (or forced with nvfp4_plan_create_flags); nvfp4_plan_info.kernel
+ *   says which:
  *   - NVFP4_KERNEL_TCGEN05 (the default): a warp-specialised projection
  *     kernel (weights staged by tensor copies, decoded into tensor memory,
  *     tcgen05.mma), preceded by an activation-preparation kernel unless every
@@ -69,9 +70,10 @@
  * Numerics
  *   Each activation row is converted to fp16 after multiplying it by a power
  *   of two chosen from its largest magnitude (over all of K; or, for the
- *   tcgen05 kernel when one launch does the call, over the k-steps of each
- *   block of the work split, which depends on (N, K) and the SM count only),
- *   exact for every element within 2^-32 of that maximum; weights are decoded
+ *   tcgen05 kernel when one launch does the call and for the cluster kernel,
+ *   over the k-steps of each block of the work split, which depends on (N, K)
+ *   and the SM count only), exact for every element within 2^-32 of that
+ *   maximum; weights are decoded
  *   to fp16 (E2M1 x E4M3 is exact in fp16); products accumulate in fp32 on
  *   the tensor cores over a warp's (or block's) share of a row block's K; that
  *   sum is multiplied back by the inverse power of two (exact); shares are
@@ -96,9 +98,10 @@ typedef struct nvfp4_plan* nvfp4_plan_t; /* opaque, host-owned */
 typedef enum {
   NVFP4_OK = 0,
   NVFP4_ERR_ARG = 1,     /* null plan / pointer, or out-of-range enum */
-  NVFP4_ERR_SHAPE = 2,   /* N < 1, K < 256, K not a multiple of 256, or too large */
+  NVFP4_ERR_SHAPE = 2,   /* N < 1, K < 256, K not a multiple of 256, too large, a stride or row
+                            group that does not fit, or a shape the forced kernel does not take */
   NVFP4_ERR_ALIGN = 3,   /* x, y, w_codes or w_block_scales not 16-byte aligned */
-  NVFP4_ERR_M_RANGE = 4, /* M outside 1..32 */
+  NVFP4_ERR_M_RANGE = 4, /* M outside 1..32 (or a grouped-table entry's rows outside 0..max_M) */
   NVFP4_ERR_CUDA = 5,    /* a CUDA runtime call failed (launch, allocation, query) */
   NVFP4_ERR_NOMEM = 6,   /* host or device allocation failed */
   NVFP4_ERR_TIMEOUT = 7, /* a bounded in-kernel wait ran out (reported by nvfp4_plan_check) */
