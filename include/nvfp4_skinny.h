@@ -48,7 +48,12 @@
  *     register-direct projection kernel (each warp copies its own weight rows
  *     into a private shared-memory ring with cp.async, decodes them into
  *     registers and multiplies them with mma.sync); no in-kernel wait of any
- *     kind.
+ *     kind;
+ *   - NVFP4_KERNEL_CLUSTER: one launch; thread-block clusters of 2, 4 or 8
+ *     blocks split K, each block converting its own activation slice, and
+ *     the blocks' sums are added in rank order through distributed shared
+ *     memory (no split-K in global memory, no atomics).  Only for K that
+ *     splits into whole 128-k units, at most 6 per block.
  *   The kernels are launched with programmatic dependent launch: by default
  *   the projection kernel starts reading the weights before the kernels
  *   before it on the stream have finished (x, y and the workspace are
