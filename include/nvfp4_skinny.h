@@ -284,7 +284,8 @@ typedef struct {
   int32_t k_step;           /* k per unit of work */
   int32_t stages;           /* tcgen05: shared-memory pipeline depth; mma.sync: units of weights
                                each lane holds in flight */
-  int32_t threads;          /* threads per block of the main kernel */
+  int32_t threads;          /* threads per block of the main kernel (tcgen05: calls with M > 12;
+                               calls with M <= 12 use 768: 16 decoder warps, the same results) */
   int32_t grid;             /* blocks of the main kernel (<= SM count) */
   int32_t sm_count;
   int32_t device;

@@ -199,12 +199,21 @@ int fused_mode(int64_t row_blocks, int64_t K, int grid) {
   return (row_blocks * (K / nvfp4::kKStep) + grid - 1) / grid <= nvfp4::kStages ? 1 : 0;
 }
 
+// Decoder warps of the tcgen05 kernel: 16 (one thread per weight row and k-half, 768 threads)
+// for M <= 12, 8 (one thread per weight row, 512 threads) above.  Both compute every MMA, sum and
+// rounding identically, so a row's bits do not depend on the choice.
+constexpr int kSmallM = 12;
+int decoder_warps(int M) { return M <= kSmallM ? 16 : 8; }
+
 cudaError_t set_smem_limits() {
-  cudaError_t e = cudaFuncSetAttribute(nvfp4::skinny_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       nvfp4::kSmemBytes);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(nvfp4::skinny_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, nvfp4::kSmemBytes);
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(nvfp4::skinny_kernel<16, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                nvfp4::kSmemBytes)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(nvfp4::skinny_kernel<32, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                nvfp4::kSmemBytes)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(nvfp4::skinny_kernel<16, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                nvfp4::kSmemBytes)) != cudaSuccess)
+    return e;
   const int gs = nvfp4::gemv::kSmemMaxBytes;
   if ((e = cudaFuncSetAttribute(nvfp4::gemv::gemv_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs)) !=
           cudaSuccess ||
@@ -430,15 +439,20 @@ nvfp4_status launch_main(const CUtensorMap& tm_codes, const CUtensorMap& tm_scal
   p.units = row_blocks * p.S;
   p.row_blocks = row_blocks;
 
+  const int dw = decoder_warps(M);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(nvfp4::kThreads);
+  cfg.blockDim = dim3(dw == 8 ? nvfp4::Roles<8>::kThreads : nvfp4::Roles<16>::kThreads);
   cfg.dynamicSmemBytes = nvfp4::kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = nc == 16 ? cudaLaunchKernelEx(&cfg, nvfp4::skinny_kernel<16>, p)
-                                : cudaLaunchKernelEx(&cfg, nvfp4::skinny_kernel<32>, p);
+  cudaError_t e;
+  if (dw == 8)
+    e = nc == 16 ? cudaLaunchKernelEx(&cfg, nvfp4::skinny_kernel<16, 8>, p)
+                 : cudaLaunchKernelEx(&cfg, nvfp4::skinny_kernel<32, 8>, p);
+  else
+    e = cudaLaunchKernelEx(&cfg, nvfp4::skinny_kernel<16, 16>, p);  // M <= 12
   return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
@@ -827,7 +841,8 @@ nvfp4_status nvfp4_plan_get_info(nvfp4_plan_t plan, nvfp4_plan_info* info) {
   info->rows_per_block = clu ? 16 : mma ? plan->gg.wr * nvfp4::gemv::kWarpRows : nvfp4::kRowsPerBlock;
   info->k_step = clu ? nvfp4::cluster::kUnitK : mma ? plan->gg.wk * nvfp4::gemv::kUnitK : nvfp4::kKStep;
   info->stages = clu ? plan->cg.depth[nvfp4::cluster::kMaxNT] : mma ? plan->gg.depth : nvfp4::kStages;
-  info->threads = clu ? nvfp4::cluster::kThreads : mma ? nvfp4::gemv::kThreads : nvfp4::kThreads;
+  // tcgen05: the block size of calls with M > 12 (calls with M <= 12 use Roles<16>, 768 threads)
+  info->threads = clu ? nvfp4::cluster::kThreads : mma ? nvfp4::gemv::kThreads : nvfp4::Roles<8>::kThreads;
   info->grid = plan->grid;
   info->sm_count = plan->sm_count;
   info->device = plan->device;

@@ -11,24 +11,35 @@
 // into the stages, take each row's largest magnitude over the block's k-steps and convert in
 // place.  Otherwise x_prep_kernel runs first.  The choice depends on (N, K, grid) only.
 //
-// skinny_kernel: persistent and warp-specialised, one block per SM, 16 warps (4 per SM
-// sub-partition, so each thread may hold 128 registers):
-//   warps 0-7    decoders: one weight row per thread; E2M1 x E4M3 -> fp16 with the hardware
-//                converters (exact: at most 6 significant bits), written to tensor memory as the
-//                MMA's A operand, one k-half (128 k) of a unit at a time.  The weights arrive by
-//                2-D tensor copies (TMA) of a 256-row x 256-k block of codes (128-byte swizzle)
-//                and of its block scales into a 4-stage shared-memory ring; the last decoder
-//                warp to take a stage's bytes into registers issues the stage's next copy;
-//   warps 8-11   epilogue: one bulk copy per unit of the unit's fp16 activations into the
+// skinny_kernel<NC, DW>: persistent and warp-specialised, one block per SM, DW decoder warps
+// then 4 epilogue and 4 issuer warps.  DW = 16 (24 warps, 80 registers a thread) for M <= 12,
+// DW = 8 (16 warps, 128 registers) above; the two compute every MMA, sum and rounding
+// identically, so the choice changes no bit:
+//   decoders     DW = 8: one weight row per thread, both k-halves of every unit in turn;
+//                DW = 16: one (weight row, k-half of 128) per thread, warps 0-7 taking half 0
+//                and warps 8-15 half 1, so each sub-partition has four decoder warps whose
+//                shared-memory loads and waits overlap one another's conversions (5-7 % faster
+//                on blocks of 20 or more units).  With 80 registers its split-K reduction keeps
+//                one item's parts in flight per thread, which covers every item in one round
+//                trip only for M <= 12; above, the 8-warp layout's two items per thread are
+//                faster.  One rule for every plan: calls of different layouts back to back
+//                measured 1.5-3.5 us slower at the hand-over.  E2M1 x E4M3 -> fp16 with the hardware
+//                converters (exact: at most 6 significant bits), written to tensor memory as
+//                the MMA's A operand.  The weights arrive by 2-D tensor copies (TMA) of a
+//                256-row x 256-k block of codes (128-byte swizzle) and of its block scales into
+//                a 4-stage shared-memory ring; the last decoder warp to take a stage's bytes
+//                into registers issues the stage's next copy;
+//   epilogue     (4 warps) one bulk copy per unit of the unit's fp16 activations into the
 //                stage (after the MMAs of the unit that last used it completed; fused mode:
 //                the activations are prepared once, before the first MMA); at the end of
 //                a row block's k-range: tensor memory -> registers, times 2^-e, times the
 //                per-tensor scale, rounded and stored, or published for the split-K reduction
 //                at the end of the block's range;
-//   warps 12-15  MMA issuers, one per (128-row tile, k-half): tcgen05.mma M=128, N=NC, K=16,
+//   MMA issuers  (4 warps) one per (128-row tile, k-half): tcgen05.mma M=128, N=NC, K=16,
 //                fp32 accumulation in tensor memory over every unit of a row block's k-range,
 //                8 per unit each.  Four issuers keep the tensor core fed (one issuing thread
-//                sustains about one such MMA per 44 cycles, four reach one per ~16 SM-wide).
+//                sustains about one such MMA per 73 cycles whatever N <= 64; four reach one
+//                per ~18 SM-wide).
 //                An issuer never reads shared memory (a read waits for its MMAs in flight): it
 //                learns that operands are ready from hardware named barriers and reports
 //                completions through tcgen05.commit.
@@ -70,14 +81,20 @@ constexpr int kXOff = kWStageBytes;                 // activation area inside a 
 constexpr int kStageBytes = kWStageBytes + kXAreaBytes;           // 53248
 constexpr int kPrepThreads = 512;
 
-constexpr int kDecodeWarps = 8;
-constexpr int kEpiWarp0 = 8;  // also allocates and frees tensor memory
 constexpr int kEpiWarps = 4;
-constexpr int kMmaWarp0 = 12;
 constexpr int kMmaWarps = 4;
-constexpr int kWarps = 16;
-constexpr int kThreads = kWarps * 32;  // 512
-static_assert(kMmaWarp0 + kMmaWarps == kWarps, "warp roles");
+// Warp roles with DW decoder warps: decoders [k-half (DW = 16 only)][tile][quadrant], then the
+// epilogue warps (the first also allocates and frees tensor memory), then the MMA issuers.
+template <int DW>
+struct Roles {
+  static_assert(DW == 8 || DW == 16, "decoder warps");  // a power of two: stage releases count modulo DW
+  static constexpr int kDecodeWarps = DW;
+  static constexpr int kHalvesPerThread = 16 / DW;  // k-halves of a unit one decoder thread converts
+  static constexpr int kEpiWarp0 = DW;
+  static constexpr int kMmaWarp0 = DW + kEpiWarps;
+  static constexpr int kWarps = kMmaWarp0 + kMmaWarps;
+  static constexpr int kThreads = kWarps * 32;  // 512 or 768
+};
 
 // tensor memory: A slot (half h, tile t) = 64 columns of fp16 pairs (128 k); D buffer d holds
 // one 32-column accumulator per (tile, half)
@@ -117,7 +134,7 @@ static_assert(kSmemBytes <= 232448, "shared memory per block");
 constexpr uint32_t kNbEpi = 1;  // the 4 epilogue warps
 __device__ __forceinline__ uint32_t nb_afull(int h, int t) { return 2u + (uint32_t)(h * kTiles + t); }
 __device__ __forceinline__ uint32_t nb_dfree(int d) { return 6u + (uint32_t)d; }
-constexpr uint32_t kNbAFullThreads = 4 * 32 + 32;    // 4 decoder warps + 1 issuer warp
+constexpr uint32_t kNbAFullThreads = 4 * 32 + 32;    // the 4 decoder warps of a (half, tile) + 1 issuer warp
 constexpr uint32_t kNbDFreeThreads = 4 * 32 + 4 * 32;  // 4 epilogue warps + 4 issuer warps
 
 // instruction descriptor: kind::f16, D = f32, A = B = f16, both K-major, N = NC, M = 128
@@ -273,18 +290,26 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, float f1, float f2) {
   return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
-// v0[j] = (D_a0[j] + D_b0[j]) * xs[j] and v1[j] likewise for the second tile, 16 columns: the
-// two k-half accumulators of each tile, all four loads in flight, one wait.
-__device__ __forceinline__ void drain16(float (&v0)[16], float (&v1)[16], uint32_t a0, uint32_t b0, uint32_t a1,
-                                        uint32_t b1, const float* xs) {
-  uint32_t ra0[16], rb0[16], ra1[16], rb1[16];
-  ptx::tmem_ld16(a0, ra0);
-  ptx::tmem_ld16(b0, rb0);
-  ptx::tmem_ld16(a1, ra1);
-  ptx::tmem_ld16(b1, rb1);
+// v0[j] = (D_a0[j] + D_b0[j]) * xs[j] and v1[j] likewise for the second tile, W = 8 or 16
+// columns: the two k-half accumulators of each tile, all four loads in flight, one wait.
+template <int W>
+__device__ __forceinline__ void drain(float (&v0)[W], float (&v1)[W], uint32_t a0, uint32_t b0, uint32_t a1,
+                                      uint32_t b1, const float* xs) {
+  uint32_t ra0[W], rb0[W], ra1[W], rb1[W];
+  if constexpr (W == 16) {
+    ptx::tmem_ld16(a0, ra0);
+    ptx::tmem_ld16(b0, rb0);
+    ptx::tmem_ld16(a1, ra1);
+    ptx::tmem_ld16(b1, rb1);
+  } else {
+    ptx::tmem_ld8(a0, ra0);
+    ptx::tmem_ld8(b0, rb0);
+    ptx::tmem_ld8(a1, ra1);
+    ptx::tmem_ld8(b1, rb1);
+  }
   ptx::tmem_wait_ld();
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
+  for (int j = 0; j < W; ++j) {
     v0[j] = __fmul_rn(__fadd_rn(__uint_as_float(ra0[j]), __uint_as_float(rb0[j])), xs[j]);
     v1[j] = __fmul_rn(__fadd_rn(__uint_as_float(ra1[j]), __uint_as_float(rb1[j])), xs[j]);
   }
@@ -380,9 +405,10 @@ __global__ void __launch_bounds__(kPrepThreads) x_prep_kernel(const uint16_t* __
 // NC = activation rows of the MMA (16 for M <= 16, else 32).  An N = 16 and an N = 32 MMA give
 // every column the same bits, and every column's epilogue arithmetic is the same sequence of
 // correctly rounded operations, so a row's bits do not depend on NC either.
-template <int NC>
-__global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_constant__ MainParams p) {
+template <int NC, int DW>
+__global__ void __launch_bounds__(Roles<DW>::kThreads, 1) skinny_kernel(const __grid_constant__ MainParams p) {
   static_assert(NC == 16 || NC == 32, "epilogue width");
+  using R = Roles<DW>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSmemBar);
@@ -451,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
     ptx::prefetch_tensormap(&p.tm_scales);
     for (int i = 0; i < kStages && i < n_local; ++i) issue_weights(i);
   }
-  if (warp == kEpiWarp0) {
+  if (warp == R::kEpiWarp0) {
     ptx::tmem_alloc(ptx::smem_addr(tmem_base_smem), kTmemCols);
     ptx::tmem_relinquish();
   }
@@ -518,9 +544,12 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
     ptx::named_bar_sync(kNbPrep, kNbPrepThreads);  // every operand row in place before any MMA
   };
 
-  if (warp < kDecodeWarps) {
+  if (warp < R::kDecodeWarps) {
     // ================================================================ decoders
-    const int tile = warp >> 2, quad = warp & 3;
+    // warp = [k-half (DW = 16)][tile][quadrant]: each thread converts the k-halves h0 ..
+    // h0 + kHW - 1 of one weight row of every unit into A slots (h, tile)
+    constexpr int kHW = R::kHalvesPerThread;
+    const int h0 = kHW == 2 ? 0 : warp >> 3, tile = (warp >> 2) & 1, quad = warp & 3;
     const int row_in_block = tile * kTileRows + quad * 32 + lane;
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
     bool ok = true;
@@ -531,28 +560,37 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
       if (ok) ok = wait_bar(bar(kBarFull + st), (uint32_t)(round & 1), ab);
       ok = __all_sync(0xffffffffu, ok);
       const uint8_t* stage = smem + st * kStageBytes;
-      // 128-byte swizzle: 16-byte chunk q of row r sits at chunk q ^ (r % 8) of the row
+      // 128-byte swizzle: 16-byte chunk q of row r sits at chunk q ^ (r % 8) of the row; half
+      // h's codes are chunks 4 h .. 4 h + 3, its scales bytes 8 h .. 8 h + 7 of the row's 16
       const uint8_t* crow = stage + row_in_block * kCodeRowBytes;
+      const uint8_t* srow = stage + kCodeStageBytes + row_in_block * kScaleRowBytes + 8 * h0;
       const int swz = row_in_block & 7;
-      uint4 c[8];
-      uint4 sc = make_uint4(0u, 0u, 0u, 0u);
+      uint4 c[4 * kHW];
+      uint32_t sw[2 * kHW];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) c[q] = ok ? *reinterpret_cast<const uint4*>(crow + ((q ^ swz) << 4)) : sc;
-      if (ok) sc = *reinterpret_cast<const uint4*>(stage + kCodeStageBytes + row_in_block * kScaleRowBytes);
+      for (int q = 0; q < 4 * kHW; ++q)
+        c[q] = ok ? *reinterpret_cast<const uint4*>(crow + (((4 * h0 + q) ^ swz) << 4)) : make_uint4(0u, 0u, 0u, 0u);
+      if constexpr (kHW == 2) {
+        const uint4 sc = ok ? *reinterpret_cast<const uint4*>(srow) : make_uint4(0u, 0u, 0u, 0u);
+        sw[0] = sc.x, sw[1] = sc.y, sw[2] = sc.z, sw[3] = sc.w;
+      } else {
+        const uint2 sc = ok ? *reinterpret_cast<const uint2*>(srow) : make_uint2(0u, 0u);
+        sw[0] = sc.x, sw[1] = sc.y;
+      }
       __syncwarp();
       if (lane == 0) {
-        // this warp's share of the stage is in registers; the last of the 8 warps refills it.
-        // The count only grows: a round's 8 increments all precede the refill that the next
-        // round's increments wait for, so the last of a round sees a count = 7 mod 8.
+        // this warp's share of the stage is in registers; the last of the DW warps refills it.
+        // The count only grows: a round's DW increments all precede the refill that the next
+        // round's increments wait for, so the last of a round sees a count = DW - 1 mod DW.
         __threadfence_block();
-        if ((atomicAdd(release_cnt + st, 1) & (kDecodeWarps - 1)) == kDecodeWarps - 1) {
+        if ((atomicAdd(release_cnt + st, 1) & (R::kDecodeWarps - 1)) == R::kDecodeWarps - 1) {
           __threadfence_block();
           if (i + kStages < n_local && !*abort_flag) issue_weights(i + kStages);
         }
       }
-      const uint32_t sw4[4] = {sc.x, sc.y, sc.z, sc.w};
 #pragma unroll
-      for (int h = 0; h < kHalves; ++h) {
+      for (int hi = 0; hi < kHW; ++hi) {
+        const int h = h0 + hi;
         // this half's A slot: its MMAs of the previous unit must have completed (and the issuer
         // must have synced) before it is overwritten; the wait ignores the abort flag
         const bool freed = wait_bar(bar(kBarAEmpty + h * kTiles + tile), (uint32_t)((i & 1) ^ 1), ab, false);
@@ -560,20 +598,20 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
         if (store) ptx::tc_fence_after();
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          // k [128 h + 64 hh, +64): code words c[4 h + 2 hh], c[4 h + 2 hh + 1]; 4 scale blocks
-          const uint32_t sw = sw4[2 * h + hh];
-          const uint32_t s0 = ptx::e4m3_pair(sw, 0), s1 = ptx::e4m3_pair(sw, 1);
-          const uint32_t s2 = ptx::e4m3_pair(sw, 2), s3 = ptx::e4m3_pair(sw, 3);
-          const uint4 lo = c[4 * h + 2 * hh], hi = c[4 * h + 2 * hh + 1];
+          // k [128 h + 64 hh, +64): code words c[4 hi + 2 hh], c[4 hi + 2 hh + 1]; 4 scale blocks
+          const uint32_t w = sw[2 * hi + hh];
+          const uint32_t s0 = ptx::e4m3_pair(w, 0), s1 = ptx::e4m3_pair(w, 1);
+          const uint32_t s2 = ptx::e4m3_pair(w, 2), s3 = ptx::e4m3_pair(w, 3);
+          const uint4 lo = c[4 * hi + 2 * hh], hi4 = c[4 * hi + 2 * hh + 1];
           uint32_t o[32];
           ptx::e2m1x8_scaled(lo.x, s0, o[0], o[1], o[2], o[3]);
           ptx::e2m1x8_scaled(lo.y, s0, o[4], o[5], o[6], o[7]);
           ptx::e2m1x8_scaled(lo.z, s1, o[8], o[9], o[10], o[11]);
           ptx::e2m1x8_scaled(lo.w, s1, o[12], o[13], o[14], o[15]);
-          ptx::e2m1x8_scaled(hi.x, s2, o[16], o[17], o[18], o[19]);
-          ptx::e2m1x8_scaled(hi.y, s2, o[20], o[21], o[22], o[23]);
-          ptx::e2m1x8_scaled(hi.z, s3, o[24], o[25], o[26], o[27]);
-          ptx::e2m1x8_scaled(hi.w, s3, o[28], o[29], o[30], o[31]);
+          ptx::e2m1x8_scaled(hi4.x, s2, o[16], o[17], o[18], o[19]);
+          ptx::e2m1x8_scaled(hi4.y, s2, o[20], o[21], o[22], o[23]);
+          ptx::e2m1x8_scaled(hi4.z, s3, o[24], o[25], o[26], o[27]);
+          ptx::e2m1x8_scaled(hi4.w, s3, o[28], o[29], o[30], o[31]);
           if (store) ptx::tmem_st32(t_lane + a_col(h, tile) + (uint32_t)(hh * 32), o);
         }
         if (store) ptx::tmem_wait_st();
@@ -581,18 +619,18 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
         // the unit's activations must be in the stage before its first MMAs are released (after
         // an abort this wait returns at once: the arrivals still pair with the issuers' syncs).
         // In fused mode the issuers wrote them themselves before their first sync.
-        if (h == 0 && !p.fused) (void)wait_bar(bar(kBarXFull + st), (uint32_t)(round & 1), ab);
+        if (hi == 0 && !p.fused) (void)wait_bar(bar(kBarXFull + st), (uint32_t)(round & 1), ab);
         ptx::named_bar_arrive(nb_afull(h, tile), kNbAFullThreads);
       }
     }
-  } else if (warp >= kMmaWarp0) {
+  } else if (warp >= R::kMmaWarp0) {
     // ================================================================ MMA issuers
     // The whole warp walks the schedule (named barriers are warp-wide); lane 0 issues.  No
     // shared-memory reads here: operand readiness comes from named barriers, completions go
     // out through tcgen05.commit.  The issuer has no abort path: MMAs on stale data are
     // harmless, and its commits keep every other role's waits completing.
-    if (p.fused) prep_fused(warp - kEpiWarp0);
-    const int q = warp - kMmaWarp0, t = q >> 1, h = q & 1;
+    if (p.fused) prep_fused(warp - R::kEpiWarp0);
+    const int q = warp - R::kMmaWarp0, t = q >> 1, h = q & 1;
     int sg = -1;  // row-block segment of this block's range; D buffer sg % 2 accumulates it
     for (int i = 0; i < n_local; ++i) {
       const bool first = i == 0 || unit_kstep(i) == 0;
@@ -626,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
     __syncwarp();
   } else {
     // ================================================================ epilogue
-    const int ew = warp - kEpiWarp0, quad = warp & 3;
+    const int ew = warp - R::kEpiWarp0, quad = warp & 3;
     const int etid = ew * 32 + lane;  // 0..127
     ptx::grid_dependency_wait();  // the activation operand, y, partials and counters are ready / free
     const int M = p.M;
@@ -642,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
                     kXBytes, xb, pol_x);
     };
     if (p.fused) {
-      prep_fused(warp - kEpiWarp0);
+      prep_fused(warp - R::kEpiWarp0);
     } else {
       if (etid == 0)
         for (int j = 0; j < kStages && j < n_local; ++j) issue_x(j);
@@ -687,16 +725,17 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
       float* f1 = whole ? static_cast<float*>(p.y) + o1 : p.partials + (int64_t)slot * (kNmma * kRowsPerBlock) + r1;
       uint16_t* h0 = static_cast<uint16_t*>(p.y) + o0;
       uint16_t* h1 = static_cast<uint16_t*>(p.y) + o1;
+      constexpr int kW = DW == 8 ? 16 : 8;  // accumulator columns per drain (fits the registers)
 #pragma unroll 1
-      for (int cb = 0; cb < NC / 16; ++cb) {
-        float v0[16], v1[16];
-        drain16(v0, v1, taddr + d_col(d, 0, 0) + 16 * cb, taddr + d_col(d, 0, 1) + 16 * cb,
-                taddr + d_col(d, 1, 0) + 16 * cb, taddr + d_col(d, 1, 1) + 16 * cb, xs_smem + 16 * cb);
+      for (int cb = 0; cb < NC / kW; ++cb) {
+        float v0[kW], v1[kW];
+        drain<kW>(v0, v1, taddr + d_col(d, 0, 0) + kW * cb, taddr + d_col(d, 0, 1) + kW * cb,
+                  taddr + d_col(d, 1, 0) + kW * cb, taddr + d_col(d, 1, 1) + kW * cb, xs_smem + kW * cb);
         if (!ok) continue;
         if (bf16_out) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int64_t m = 16 * cb + j;
+          for (int j = 0; j < kW; ++j) {
+            const int64_t m = kW * cb + j;
             if (m < M) {
               if (in0) h0[m * p.ldc] = ptx::f32_to_bf16_rn(__fmul_rn(v0[j], gs));
               if (in1) h1[m * p.ldc] = ptx::f32_to_bf16_rn(__fmul_rn(v1[j], gs));
@@ -704,8 +743,8 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
           }
         } else {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int64_t m = 16 * cb + j;
+          for (int j = 0; j < kW; ++j) {
+            const int64_t m = kW * cb + j;
             if (m < M) {
               if (in0) f0[m * fstride] = __fmul_rn(v0[j], mul);
               if (in1) f1[m * fstride] = __fmul_rn(v1[j], mul);
@@ -739,7 +778,8 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
   ptx::tc_fence_before();
   __syncthreads();  // the acquire of the last part's counter (thread 0 of the epilogue) comes first
   ptx::tc_fence_after();
-  for (int k = 0; k < *n_red && !*abort_flag; ++k) {
+  const int n_reduce = *abort_flag ? 0 : *n_red;  // read once after the barrier: the same for every thread
+  for (int k = 0; k < n_reduce; ++k) {
     const int64_t rb = red_rb[k];
     const int64_t pf = block_of_unit(rb * S, T, G), pl = block_of_unit(rb * S + S - 1, T, G);
     const int nseg = (int)(pl - pf + 1);
@@ -748,9 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
     const int pf_bit = unit_begin(pf, T, G) < rb * S ? 1 : 0;
     const float gs = p.gs;
     const int M = p.M;
-    // items of 4 rows x 1 activation row, two per thread and pass; the parts' loads of both
-    // items (up to 8 parts each) are issued before any is used, and the parts are added
-    // strictly in block order
+    // items of 4 rows x 1 activation row: item o = (m, r) is float4 o of a part
     auto store4 = [&](int m, int r, float4 acc) {
       const float v[4] = {__fmul_rn(acc.x, gs), __fmul_rn(acc.y, gs), __fmul_rn(acc.z, gs), __fmul_rn(acc.w, gs)};
       const int64_t n = rb * kRowsPerBlock + r;
@@ -775,44 +813,82 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
         }
       }
     };
+    // The (part, item) pairs of a batch of parts are spread over all threads, at most kLoads
+    // plain L2 loads in flight per thread, stored to the idle stage ring as [part][item]; after
+    // a barrier each thread adds its items' parts in block order.  A batch costs one round trip
+    // to L2: one batch for M <= 16 and up to 5 parts (an asynchronous copy's round trip to
+    // shared memory measured about half a round trip longer with every thread waiting).
     const int n_items = (kRowsPerBlock / 4) * M;
+    if constexpr (DW == 8) {
+      // two items per thread and pass; both items' parts (up to 8 each) are loaded before any is
+      // added, and they are added strictly in block order
 #pragma unroll 1
-    for (int o = threadIdx.x; o < n_items; o += 2 * kThreads) {
-      const int o2 = o + kThreads;
-      const bool two = o2 < n_items;
-      const int m0 = o / (kRowsPerBlock / 4), r0 = 4 * (o % (kRowsPerBlock / 4));
-      const int m1 = two ? o2 / (kRowsPerBlock / 4) : m0, r1 = two ? 4 * (o2 % (kRowsPerBlock / 4)) : r0;
-      const float* base0 = p.partials + m0 * kRowsPerBlock + r0;
-      const float* base1 = p.partials + m1 * kRowsPerBlock + r1;
-      float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
+      for (int o = threadIdx.x; o < n_items; o += 2 * R::kThreads) {
+        const int o2 = o + R::kThreads;
+        const bool two = o2 < n_items;
+        const float* base0 = p.partials + 4 * (int64_t)o;
+        const float* base1 = p.partials + 4 * (int64_t)(two ? o2 : o);
+        float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
 #pragma unroll 1
-      for (int b0 = 0; b0 < nseg; b0 += 8) {
-        float4 t0[8], t1[8];
+        for (int b0 = 0; b0 < nseg; b0 += 8) {
+          float4 t0[8], t1[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (b0 + j < nseg) {
-            const int64_t b = pf + b0 + j;
-            const int64_t off = (2 * b + (b == pf ? pf_bit : 0)) * (int64_t)(kNmma * kRowsPerBlock);
-            t0[j] = __ldcg(reinterpret_cast<const float4*>(base0 + off));
-            if (two) t1[j] = __ldcg(reinterpret_cast<const float4*>(base1 + off));
+          for (int j = 0; j < 8; ++j) {
+            if (b0 + j < nseg) {
+              const int64_t b = pf + b0 + j;
+              const int64_t off = (2 * b + (b == pf ? pf_bit : 0)) * (int64_t)(kNmma * kRowsPerBlock);
+              t0[j] = __ldcg(reinterpret_cast<const float4*>(base0 + off));
+              if (two) t1[j] = __ldcg(reinterpret_cast<const float4*>(base1 + off));
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (b0 + j < nseg) {
+              acc0.x += t0[j].x;
+              acc0.y += t0[j].y;
+              acc0.z += t0[j].z;
+              acc0.w += t0[j].w;
+              acc1.x += t1[j].x;
+              acc1.y += t1[j].y;
+              acc1.z += t1[j].z;
+              acc1.w += t1[j].w;
+            }
           }
         }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (b0 + j < nseg) {
-            acc0.x += t0[j].x;
-            acc0.y += t0[j].y;
-            acc0.z += t0[j].z;
-            acc0.w += t0[j].w;
-            acc1.x += t1[j].x;
-            acc1.y += t1[j].y;
-            acc1.z += t1[j].z;
-            acc1.w += t1[j].w;
-          }
-        }
+        store4(o / (kRowsPerBlock / 4), 4 * (o % (kRowsPerBlock / 4)), acc0);
+        if (two) store4(o2 / (kRowsPerBlock / 4), 4 * (o2 % (kRowsPerBlock / 4)), acc1);
       }
-      store4(m0, r0, acc0);
-      if (two) store4(m1, r1, acc1);
+    } else {
+      // DW = 16 runs only for M <= 12 (the host's rule), so every item has its own thread: its
+      // parts (up to 8 at a time) are all loaded before any is added, in block order
+      static_assert(DW != 16 || NC == 16, "the 16-warp layout runs only for M <= 12");
+      const int o = (int)threadIdx.x;
+      if (o < n_items) {
+        const float* base = p.partials + 4 * (int64_t)o;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+        for (int b0 = 0; b0 < nseg; b0 += 8) {
+          float4 t[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (b0 + j < nseg) {
+              const int64_t b = pf + b0 + j;
+              const int64_t off = (2 * b + (b == pf ? pf_bit : 0)) * (int64_t)(kNmma * kRowsPerBlock);
+              t[j] = __ldcg(reinterpret_cast<const float4*>(base + off));
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (b0 + j < nseg) {
+              acc.x += t[j].x;
+              acc.y += t[j].y;
+              acc.z += t[j].z;
+              acc.w += t[j].w;
+            }
+          }
+        }
+        store4(o / (kRowsPerBlock / 4), 4 * (o % (kRowsPerBlock / 4)), acc);
+      }
     }
   }
 
@@ -820,7 +896,7 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const __grid_consta
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  if (warp == kEpiWarp0) ptx::tmem_dealloc(tmem, kTmemCols);
+  if (warp == R::kEpiWarp0) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace nvfp4

@@ -165,9 +165,10 @@ def test_row_invariance_square(kernel):
 
 
 @kernel_param
-@pytest.mark.parametrize("N,K", [(7168, 5120), (5120, 17408), (300, 768)])
+@pytest.mark.parametrize("N,K", [(7168, 5120), (5120, 17408), (34816, 5120), (300, 768)])
 def test_row_invariance_other_shapes(N, K, kernel):
-    _row_invariance(N, K, seed=N % 97, Ms=(1, 2, 8, 9, 16, 17, 24, 32), kernel=kernel)
+    # M = 12 / 13 is where the tcgen05 kernel changes its decoder layout (16 / 8 decoder warps)
+    _row_invariance(N, K, seed=N % 97, Ms=(1, 2, 8, 9, 12, 13, 16, 17, 24, 32), kernel=kernel)
 
 
 @kernel_param
