@@ -403,7 +403,7 @@ nvfp4_status launch_main(const CUtensorMap& tm_codes, const CUtensorMap& tm_scal
   const int fused = silu_mul ? 0 : fused_mode(row_blocks, K, grid);
   if (!fused) {
     cudaLaunchConfig_t pcfg = {};
-    pcfg.gridDim = dim3((unsigned)nc);
+    pcfg.gridDim = dim3((unsigned)M);  // one block per activation row
     pcfg.blockDim = dim3(nvfp4::kPrepThreads);
     pcfg.stream = stream;
     pcfg.attrs = attr;

@@ -330,8 +330,9 @@ __device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
   return r;
 }
 
-// One block per operand row m < NC; rows M..NC-1 are written as zeros (their MMA columns are
-// never read).  Magnitudes are compared as bf16 bit patterns (a non-negative bf16 orders like
+// One block per activation row m < M.  Operand rows M..NC-1 are not written: whatever they hold
+// only reaches MMA columns M..NC-1, which no store reads (the epilogue and the split-K sum cover
+// rows m < M only), and their 2^-e is taken as 0.  Magnitudes are compared as bf16 bit patterns (a non-negative bf16 orders like
 // its bits).  Each thread keeps its first kPrepHeld chunks in registers between the two passes
 // and reads any further ones again.
 constexpr int kPrepHeld = 8;
@@ -364,11 +365,6 @@ __global__ void __launch_bounds__(kPrepThreads) x_prep_kernel(const uint16_t* __
   auto dst = [&](int64_t c) {
     return reinterpret_cast<uint4*>(x16 + (c >> 5) * xbytes + x_chunk_off<NC>(m, (int)(c & 31)));
   };
-  if (m >= M) {
-    for (int64_t c = tid; c < chunks; c += kPrepThreads) *dst(c) = make_uint4(0u, 0u, 0u, 0u);
-    if (tid == 0) xs[m] = 0.f;
-    return;
-  }
   const uint4* row = reinterpret_cast<const uint4*>(x + (int64_t)m * lda);
   const uint4* urow = row + chunks;  // the up half of a [gate | up] row
   auto load = [&](int64_t c) { return silu_mul ? bf16x8_silu_mul(__ldg(row + c), __ldg(urow + c)) : __ldg(row + c); };
@@ -684,7 +680,7 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1) skinny_kernel(const __
     } else {
       if (etid == 0)
         for (int j = 0; j < kStages && j < n_local; ++j) issue_x(j);
-      if (etid < kNmma) xs_smem[etid] = etid < NC ? p.xs[etid] : 0.f;
+      if (etid < kNmma) xs_smem[etid] = etid < M ? p.xs[etid] : 0.f;  // operand rows >= M are not written
     }
     int ks_last;
     const int n_seg = (int)(unit_rb(n_local - 1, ks_last) - rb0) + 1;  // row-block segments of the range
