@@ -35,17 +35,21 @@ SCALE_BYTES = [b for b in range(256) if (b & 0x7F) != 0x7F]
 
 @pytest.mark.parametrize("kernel", list(KERNELS))
 @pytest.mark.parametrize("out", ["bf16", "f32"])
-@pytest.mark.parametrize("M", [16, 32])
-def test_decode_table_exhaustive(kernel, out, M):
+@pytest.mark.parametrize("M,stride", [(16, 1), (32, 1), (16, 17), (12, 21)])
+def test_decode_table_exhaustive(kernel, out, M, stride):
     """Row n of the weight has scale byte SCALE_BYTES[n] in every block and code k % 16 at k;
-    activation row m is one-hot at k = m; gs = 1.  Then y[m, n] = e2m1(m % 16) * e4m3(s_n)
-    exactly: each element is a single product, which fp16, fp32 and bf16 all hold."""
+    activation row m is one-hot at k_m = stride m mod K; gs = 1.  Then y[m, n] =
+    e2m1(k_m % 16) * e4m3(s_n) exactly: each element is a single product, which fp16, fp32 and
+    bf16 all hold.  Strides 17 and 21 put the one-hot positions in both 128-k halves of the unit
+    and every 16-byte chunk of a row (all 16 codes at stride 17), and M = 12 runs the tcgen05
+    kernel's 16-decoder-warp layout, whose warps each convert one half."""
     N, K = len(SCALE_BYTES), 256
     code_k = np.arange(K) % 16
     codes = np.tile((code_k[0::2] | (code_k[1::2] << 4)).astype(np.uint8), (N, 1))
     scales = np.repeat(np.array(SCALE_BYTES, np.uint8)[:, None], K // 16, axis=1)
     x = torch.zeros((M, K), dtype=torch.float32)
-    x[torch.arange(M), torch.arange(M)] = 1.0
+    k_m = (stride * np.arange(M)) % K
+    x[torch.arange(M), torch.from_numpy(k_m)] = 1.0
     x = x.to(torch.bfloat16)
     f32 = out == "f32"
     plan = nb.nvfp4_plan_create_flags(N, K, nb.NVFP4_OUT_F32 if f32 else nb.NVFP4_OUT_BF16, KERNELS[kernel])
@@ -54,7 +58,8 @@ def test_decode_table_exhaustive(kernel, out, M):
                            y)
     torch.cuda.synchronize()
     assert nb.nvfp4_plan_check(plan) == nb.NVFP4_OK
-    want = np.array([[oracle.e2m1(m % 16) * oracle.e4m3(s) for s in SCALE_BYTES] for m in range(M)], np.float64)
+    want = np.array([[oracle.e2m1(int(k_m[m]) % 16) * oracle.e4m3(s) for s in SCALE_BYTES] for m in range(M)],
+                    np.float64)
     assert np.all(want.astype(np.float32).astype(np.float64) == want)          # exact in fp32
     got = y.float().cpu().numpy().astype(np.float64)
     if not f32:
