@@ -502,40 +502,27 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1) skinny_kernel(const __
                         p.x + (int64_t)m * p.lda + (int64_t)unit_kstep(q) * kKStep + lane * 8, pol);
     ptx::cp_async_commit();
     ptx::cp_async_wait(0);
-    // The warp's NC / 8 rows are walked together (their loads independent of one another), each
-    // loop over the block's k-slices kept rolled: this code runs once per launch.
-    constexpr int kRows = NC / 8;
-    uint32_t mx[kRows];
-#pragma unroll
-    for (int r = 0; r < kRows; ++r) mx[r] = 0u;
-    for (int q = 0; q < n_local; ++q) {
-#pragma unroll
-      for (int r = 0; r < kRows; ++r) {
-        const int m = pw + 8 * r;
-        if (m < M)
-          mx[r] = max(mx[r], bf16x8_maxmag(*reinterpret_cast<const uint4*>(smem + q * kStageBytes + kXOff +
-                                                                           x_chunk_off<NC>(m, lane))));
-      }
-    }
-    float f1[kRows], f2[kRows];
-#pragma unroll
-    for (int r = 0; r < kRows; ++r) {
-      const int m = pw + 8 * r;
-      const int e = x_exponent(__uint_as_float(warp_max_u32(mx[r]) << 16));  // -112 <= e <= 148
-      f1[r] = pow2i(e <= 127 ? e : e / 2);
-      f2[r] = pow2i(e <= 127 ? 0 : e - e / 2);
-      if (lane == 0) xs_smem[m] = m < M ? pow2i(-(e / 2)) * pow2i(-(e - e / 2)) : 0.f;  // 2^-e, exact
-    }
-    for (int q = 0; q < n_local; ++q) {
-#pragma unroll
-      for (int r = 0; r < kRows; ++r) {
-        const int m = pw + 8 * r;
+    // Row by row, every loop rolled: this code runs once per launch, so its instructions are
+    // fetched cold, and a compact loop body is fetched once and then re-executed.  Operand rows
+    // M..NC-1 are not written: they reach only MMA columns M..NC-1, which no store reads.
+#pragma unroll 1
+    for (int m = pw; m < M; m += 8) {
+      uint32_t mx = 0u;
+#pragma unroll 1
+      for (int q = 0; q < n_local; ++q)
+        mx = max(mx, bf16x8_maxmag(*reinterpret_cast<const uint4*>(smem + q * kStageBytes + kXOff +
+                                                                   x_chunk_off<NC>(m, lane))));
+      const int e = x_exponent(__uint_as_float(warp_max_u32(mx) << 16));  // -112 <= e <= 148
+      const float f1 = pow2i(e <= 127 ? e : e / 2), f2 = pow2i(e <= 127 ? 0 : e - e / 2);
+      if (lane == 0) xs_smem[m] = pow2i(-(e / 2)) * pow2i(-(e - e / 2));  // 2^-e, exact
+#pragma unroll 1
+      for (int q = 0; q < n_local; ++q) {
         uint4* slot = reinterpret_cast<uint4*>(smem + q * kStageBytes + kXOff + x_chunk_off<NC>(m, lane));
-        // rows M .. NC-1 are zero (their MMA columns are never read); f2 = 1 unless e > 127
-        *slot = m >= M ? make_uint4(0u, 0u, 0u, 0u)
-                       : (f2[r] == 1.f ? bf16x8_to_f16x8(*slot, f1[r]) : bf16x8_to_f16x8(*slot, f1[r], f2[r]));
+        *slot = e <= 127 ? bf16x8_to_f16x8(*slot, f1) : bf16x8_to_f16x8(*slot, f1, f2);
       }
     }
+    if (lane == 0)
+      for (int m = pw + 8 * ((M - pw + 7) / 8); m < kNmma; m += 8) xs_smem[m] = 0.f;
     ptx::fence_proxy_async_smem();  // operand writes -> the tensor core's (async proxy) reads
     ptx::named_bar_sync(kNbPrep, kNbPrepThreads);  // every operand row in place before any MMA
   };
