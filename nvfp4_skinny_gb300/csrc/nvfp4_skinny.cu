@@ -200,10 +200,17 @@ int fused_mode(int64_t row_blocks, int64_t K, int grid) {
 }
 
 // Decoder warps of the tcgen05 kernel: 16 (one thread per weight row and k-half, 768 threads)
-// for M <= 12, 8 (one thread per weight row, 512 threads) above.  Both compute every MMA, sum and
-// rounding identically, so a row's bits do not depend on the choice.
+// for M <= 12, and at every M on plans whose blocks stream at least kWideUnits units; else 8
+// (one thread per weight row, 512 threads).  With 16 warps the split-K sum holds one item per
+// thread, so above M = 12 it takes extra passes: worth it only where the faster unit rate of many
+// units outweighs them and a possible hand-over from calls of the other layout (measured
+// 1.5-3.5 us).  Both compute every MMA, sum and rounding identically, so a row's bits do not
+// depend on the choice.
 constexpr int kSmallM = 12;
-int decoder_warps(int M) { return M <= kSmallM ? 16 : 8; }
+constexpr int64_t kWideUnits = 40;
+int decoder_warps(int M, int64_t units, int grid) {
+  return M <= kSmallM || (units + grid - 1) / grid >= kWideUnits ? 16 : 8;
+}
 
 cudaError_t set_smem_limits() {
   cudaError_t e;
@@ -212,6 +219,8 @@ cudaError_t set_smem_limits() {
       (e = cudaFuncSetAttribute(nvfp4::skinny_kernel<32, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 nvfp4::kSmemBytes)) != cudaSuccess ||
       (e = cudaFuncSetAttribute(nvfp4::skinny_kernel<16, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                nvfp4::kSmemBytes)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(nvfp4::skinny_kernel<32, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 nvfp4::kSmemBytes)) != cudaSuccess)
     return e;
   const int gs = nvfp4::gemv::kSmemMaxBytes;
@@ -439,7 +448,7 @@ nvfp4_status launch_main(const CUtensorMap& tm_codes, const CUtensorMap& tm_scal
   p.units = row_blocks * p.S;
   p.row_blocks = row_blocks;
 
-  const int dw = decoder_warps(M);
+  const int dw = decoder_warps(M, row_blocks * (K / nvfp4::kKStep), grid);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(dw == 8 ? nvfp4::Roles<8>::kThreads : nvfp4::Roles<16>::kThreads);
@@ -452,7 +461,8 @@ nvfp4_status launch_main(const CUtensorMap& tm_codes, const CUtensorMap& tm_scal
     e = nc == 16 ? cudaLaunchKernelEx(&cfg, nvfp4::skinny_kernel<16, 8>, p)
                  : cudaLaunchKernelEx(&cfg, nvfp4::skinny_kernel<32, 8>, p);
   else
-    e = cudaLaunchKernelEx(&cfg, nvfp4::skinny_kernel<16, 16>, p);  // M <= 12
+    e = nc == 16 ? cudaLaunchKernelEx(&cfg, nvfp4::skinny_kernel<16, 16>, p)
+                 : cudaLaunchKernelEx(&cfg, nvfp4::skinny_kernel<32, 16>, p);
   return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
@@ -842,7 +852,10 @@ nvfp4_status nvfp4_plan_get_info(nvfp4_plan_t plan, nvfp4_plan_info* info) {
   info->k_step = clu ? nvfp4::cluster::kUnitK : mma ? plan->gg.wk * nvfp4::gemv::kUnitK : nvfp4::kKStep;
   info->stages = clu ? plan->cg.depth[nvfp4::cluster::kMaxNT] : mma ? plan->gg.depth : nvfp4::kStages;
   // tcgen05: the block size of calls with M > 12 (calls with M <= 12 use Roles<16>, 768 threads)
-  info->threads = clu ? nvfp4::cluster::kThreads : mma ? nvfp4::gemv::kThreads : nvfp4::Roles<8>::kThreads;
+  info->threads = clu ? nvfp4::cluster::kThreads
+                : mma ? nvfp4::gemv::kThreads
+                      : (decoder_warps(32, plan->units, plan->grid) == 16 ? nvfp4::Roles<16>::kThreads
+                                                                          : nvfp4::Roles<8>::kThreads);
   info->grid = plan->grid;
   info->sm_count = plan->sm_count;
   info->device = plan->device;

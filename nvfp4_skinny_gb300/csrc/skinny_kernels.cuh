@@ -842,11 +842,12 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1) skinny_kernel(const __
         if (two) store4(o2 / (kRowsPerBlock / 4), 4 * (o2 % (kRowsPerBlock / 4)), acc1);
       }
     } else {
-      // DW = 16 runs only for M <= 12 (the host's rule), so every item has its own thread: its
-      // parts (up to 8 at a time) are all loaded before any is added, in block order
-      static_assert(DW != 16 || NC == 16, "the 16-warp layout runs only for M <= 12");
-      const int o = (int)threadIdx.x;
-      if (o < n_items) {
+      // one item per thread and pass (80 registers leave room for one item's parts only): its
+      // parts (up to 8 at a time) are all loaded before any is added, in block order.  For
+      // M <= 12 one pass covers every item; above, the host runs this layout only on plans whose
+      // blocks stream many units, where the extra passes are a small part of the call.
+#pragma unroll 1
+      for (int o = (int)threadIdx.x; o < n_items; o += R::kThreads) {
         const float* base = p.partials + 4 * (int64_t)o;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
