@@ -12,9 +12,9 @@
 // place.  Otherwise x_prep_kernel runs first.  The choice depends on (N, K, grid) only.
 //
 // skinny_kernel<NC, DW>: persistent and warp-specialised, one block per SM, DW decoder warps
-// then 4 epilogue and 4 issuer warps.  DW = 16 (24 warps, 80 registers a thread) for M <= 12,
-// DW = 8 (16 warps, 128 registers) above; the two compute every MMA, sum and rounding
-// identically, so the choice changes no bit:
+// then 4 epilogue and 4 issuer warps.  DW = 16 (24 warps, 80 registers a thread) for M <= 12 and
+// on plans whose blocks stream at least 40 units, DW = 8 (16 warps, 128 registers) otherwise;
+// the two compute every MMA, sum and rounding identically, so the choice changes no bit:
 //   decoders     DW = 8: one weight row per thread, both k-halves of every unit in turn;
 //                DW = 16: one (weight row, k-half of 128) per thread, warps 0-7 taking half 0
 //                and warps 8-15 half 1, so each sub-partition has four decoder warps whose
@@ -22,9 +22,10 @@
 //                on blocks of 20 or more units).  With 80 registers its split-K reduction keeps
 //                one item's parts in flight per thread, which covers every item in one round
 //                trip only for M <= 12; above, the 8-warp layout's two items per thread are
-//                faster.  One rule for every plan: calls of different layouts back to back
-//                measured 1.5-3.5 us slower at the hand-over.  E2M1 x E4M3 -> fp16 with the hardware
-//                converters (exact: at most 6 significant bits), written to tensor memory as
+//                faster unless the blocks' many units outweigh the extra passes.  Calls of
+//                different layouts back to back measured 1.5-3.5 us slower at the hand-over, so
+//                the rule keeps one layout per M for every plan of fewer than 40 units per
+//                block.  E2M1 x E4M3 -> fp16 with the hardware converters (exact: at most 6 significant bits), written to tensor memory as
 //                the MMA's A operand.  The weights arrive by 2-D tensor copies (TMA) of a
 //                256-row x 256-k block of codes (128-byte swizzle) and of its block scales into
 //                a 4-stage shared-memory ring; the last decoder warp to take a stage's bytes
@@ -47,7 +48,8 @@
 // Work split ("10 Kernels" 10.1 Row invariance): a unit is (row block of 256 weight rows,
 // k-step of 256).  The units, row-block-major, are split into `grid` contiguous, equal ranges;
 // grid = min(units, SMs), or fewer blocks of u <= 4 units each when such ranges never straddle a
-// row block (chosen on the host).  Which block computes which part of a row's sum, the order of the
+// row block, or whole row blocks per block when that keeps at least 85 % of the SMs busy (chosen
+// on the host).  Which block computes which part of a row's sum, the order of the
 // MMAs and the order in which parts are added all depend on (N, K, grid) only.  Activation
 // row m is column m of every MMA, its exponent e depends on row m alone, and nothing a column
 // computes depends on another column, so a row's bits do not depend on M.
