@@ -462,6 +462,10 @@ def test_plan_info_independent_of_M(kernel):
             whole = [rb // k for k in range(1, rb + 1) if rb % k == 0 and rb // k <= sms][:1]
             whole = [g for g in whole if 20 * g >= 17 * sms]  # whole row blocks, >= 85 % of the SMs
             assert info["grid"] == (aligned or whole or [min(units, sms)])[0]
+            # the block size of calls with M > 12: 16 decoder warps (768 threads) on plans whose
+            # blocks stream at least 40 units, else 8 (512); M <= 12 always runs 16
+            wide = -(-units // info["grid"]) >= 40
+            assert info["threads"] == (768 if wide else 512)
         else:  # the register-direct kernel runs two blocks per SM
             assert info["grid"] == min(info["units"], 2 * info["sm_count"])
         assert info["warps_rows"] * info["warps_k"] * 32 == (info["threads"] if kernel == "mma" else 32)
